@@ -1,0 +1,206 @@
+/*
+ * moe.h -- C ABI of the top-k gated Mixture-of-Experts FFN layer, forward pass,
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer (sources: "Qwen2-MoE代码解析：MoE架构原理、工程实现与部署避坑指南",
+ * jsqmd.com, sections 3.1, 3.3, 3.4; the Qwen2-MoE module article, mlqm.cn,
+ * sections 2.2 and 3.2; the MoE sparse-activation article, wmrh.cn, section 2.2):
+ *
+ *   l      = x Wg^T (+ gate_bias)                      router scores      [T, E]
+ *   p      = softmax(l)                                                   [T, E]
+ *   ids    = top-k of l, largest first, ties to the lower expert index    [T, K]
+ *   w      = p[ids] / sum_j p[ids_j]                   renormalised       [T, K]
+ *   group slots s = t*K + j by expert, stable in s; keep the first
+ *   `capacity` slots of each expert (capacity <= 0: keep all)
+ *   y_s    = W2[e] GELU(W1[e] x_t (+ b1[e])) (+ b2[e]) for kept slot s of expert e
+ *   out[t] = sum_j w[t,j] * y_{t*K+j}   (dropped slots add nothing)
+ *   aux    = E * sum_i (count_i / (T*K)) * (sum_t p[t,i] / T)
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are DEVICE pointers owned by the caller, dense and
+ *     row-major, 16-byte aligned, unless a call says otherwise.  Weights are
+ *     read-only.  The library keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on it: they enqueue kernels and return.  They never
+ *     allocate device memory and never synchronise, except moe_get_device_error.
+ *   - `ws` is a caller-owned device workspace of at least moe_workspace_size()
+ *     bytes, 256-byte aligned.  Calls that overlap on the GPU must not share one.
+ *   - Return value: MOE_OK (0) or a negative moe_status.  Arguments are checked
+ *     on the host before any launch; on error nothing is enqueued, except for
+ *     MOE_ERR_CUDA (a launch failed; outputs are undefined).
+ *   - Element types follow desc->dtype: MOE_BF16 -> x, Wg, W1, W2, x_perm,
+ *     h_perm, y_perm and out are bf16; MOE_F32 -> all of them are fp32.
+ *     Router logits, routing weights, biases and the loss are always fp32;
+ *     indices and counts are int32.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,      /* bad argument: null pointer, shape, alignment */
+  MOE_ERR_UNSUPPORTED = -2,  /* valid layer the library does not implement   */
+  MOE_ERR_WORKSPACE = -3,    /* ws is NULL or smaller than moe_workspace_size */
+  MOE_ERR_CUDA = -4,         /* a CUDA runtime / driver call failed          */
+  MOE_ERR_TIMEOUT = -5,      /* a kernel gave up a bounded wait (device flag) */
+  MOE_ERR_DEVICE = -6        /* a kernel's own bounds check fired (device flag) */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* desc->flags bits */
+#define MOE_FLAG_HOST_IO    (1u << 0) /* moe_layer_forward: x and out are host pointers */
+#define MOE_FLAG_SIMT_FFN   (1u << 1) /* bf16: CUDA-core expert FFN instead of tensor cores (testing) */
+#define MOE_FLAG_NO_DECODE  (1u << 2) /* never take the small-batch weight-streaming FFN */
+#define MOE_FLAG_SIMT_ROUTER (1u << 3) /* bf16: CUDA-core router instead of tensor cores (testing) */
+
+/*
+ * Layer description.  Field names follow the Qwen2MoEConfig fields of the
+ * Qwen2-MoE module article (mlqm.cn), section 2.2: E = num_experts,
+ * K = num_experts_per_tok, capacity = expert_capacity.
+ * Limits: T >= 0; 1 <= K <= 8; K <= E <= 256; H, F >= 8 and multiples of 8;
+ * T * K < 2^31.
+ */
+typedef struct moe_desc {
+  int64_t T;         /* tokens (batch * sequence, flattened)                 */
+  int32_t H;         /* hidden size                                          */
+  int32_t E;         /* number of experts                                    */
+  int32_t K;         /* experts chosen per token (top-k)                     */
+  int32_t F;         /* expert FFN width                                     */
+  int32_t capacity;  /* slots kept per expert; <= 0 means no limit           */
+  int32_t dtype;     /* moe_dtype                                            */
+  uint32_t flags;    /* MOE_FLAG_*                                           */
+} moe_desc;
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(int status);
+
+/* ceil(T / E) * K, the expert_capacity of the Qwen2-MoE module article
+ * (mlqm.cn), section 2.2.  Returns -1 if E <= 0 or K <= 0. */
+int64_t moe_capacity_default(int64_t T, int32_t E, int32_t K);
+
+/* Rows of the permuted buffers (x_perm, h_perm, y_perm) needed for `desc`:
+ * min(T*K, E*capacity) with a capacity, else T*K.  -1 if desc is invalid. */
+int64_t moe_max_rows(const moe_desc* desc);
+
+/* Bytes of device workspace every call below needs for `desc` (the same value
+ * for all of them).  It holds routing results, dispatch tables, the permuted
+ * activations and a device error word.  Returns MOE_ERR_INVALID for a bad desc. */
+int moe_workspace_size(const moe_desc* desc, size_t* bytes);
+
+/*
+ * Router: gate linear, softmax, top-k, renormalisation (jsqmd.com section 3.1:
+ * `gate` is nn.Linear(hidden, num_experts, bias=False), then F.softmax,
+ * torch.topk and the division by the sum of the k weights; mlqm.cn section 3.2
+ * steps 1-2).
+ *   x         [T, H]  dtype
+ *   Wg        [E, H]  dtype (nn.Linear [out, in] layout)
+ *   gate_bias [E] fp32 or NULL (added to the scores; the pages' gate has none)
+ *   logits    [T, E] fp32 out, or NULL: the scores l, fp32-accumulated
+ *   ids       [T, K] int32 out: chosen experts, largest score first, equal
+ *             scores ordered by ascending expert index
+ *   w         [T, K] fp32 out: p[ids] / sum_j p[ids_j]  (sum to 1)
+ *   psum      [E] fp32 out, or NULL: sum over tokens of p[t, e], summed in a
+ *             fixed order (deterministic)
+ */
+int moe_router_topk(const moe_desc* desc, const void* x, const void* Wg,
+                    const float* gate_bias, float* logits, int32_t* ids,
+                    float* w, float* psum, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/*
+ * Dispatch: group the T*K slots by expert (jsqmd.com section 3.1 item 3:
+ * scatter + argsort by expert id) with the capacity rule of jsqmd.com section
+ * 3.4 (tokens over an expert's capacity are dropped).  Slot s = t*K + j.
+ * Within an expert, slots keep ascending s order, so with a capacity the
+ * earliest tokens are kept.
+ *   ids     [T, K] int32 in (each value in [0, E); a token's K ids distinct)
+ *   x       [T, H] dtype in, or NULL to skip the gather
+ *   count   [E]    int32 out: slots routed to each expert, before dropping
+ *   offs    [E+1]  int32 out: first permuted row of each expert; offs[E] = rows
+ *   src     [moe_max_rows] int32 out: slot held by permuted row r (r < offs[E])
+ *   pos     [T*K]  int32 out: permuted row of slot s, or -1 if dropped
+ *   x_perm  [moe_max_rows, H] dtype out (if x != NULL): x_perm[r] = x[src[r] / K]
+ *   dropped [1]    int32 out, or NULL: number of dropped slots
+ * Out-of-range ids make the kernel set MOE_ERR_DEVICE in the workspace error
+ * word (read it with moe_get_device_error); such slots are dropped.
+ */
+int moe_dispatch(const moe_desc* desc, const int32_t* ids, const void* x,
+                 int32_t* count, int32_t* offs, int32_t* src, int32_t* pos,
+                 void* x_perm, int32_t* dropped, void* ws, size_t ws_bytes,
+                 void* stream);
+
+/*
+ * Expert FFN over the permuted rows: for each expert e and each row r in
+ * [offs[e], offs[e+1]):
+ *   h_perm[r] = GELU(W1[e] x_perm[r] + b1[e])       (GELU erf form)
+ *   y_perm[r] = W2[e] h_perm[r] + b2[e]
+ * (mlqm.cn section 2.2: every expert is Linear - GELU - Linear).  On the bf16
+ * path the products are accumulated in fp32 and h and y are rounded to bf16.
+ *   x_perm [rows, H] dtype in; offs [E+1] int32 in (device; read on device only)
+ *   W1 [E, F, H] dtype; W2 [E, H, F] dtype (nn.Linear [out, in] layout)
+ *   b1 [E, F] fp32 or NULL; b2 [E, H] fp32 or NULL
+ *   h_perm [moe_max_rows, F] dtype out (intermediate, kept for inspection)
+ *   y_perm [moe_max_rows, H] dtype out
+ * bf16 with K-major operands runs on the tcgen05 tensor cores; fp32 runs on
+ * CUDA cores; T <= 16 runs a weight-streaming kernel (unless MOE_FLAG_NO_DECODE).
+ */
+int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs,
+                   const void* W1, const float* b1, const void* W2, const float* b2,
+                   void* h_perm, void* y_perm, void* ws, size_t ws_bytes,
+                   void* stream);
+
+/*
+ * Combine: out[t] = sum_{j=0..K-1} w[t,j] * y_perm[pos[t*K+j]], summed in fp32
+ * in the order j = 0..K-1, then stored in dtype; slots with pos < 0 add
+ * nothing (jsqmd.com section 3.1 item 2; wmrh.cn section 2.2).  No residual.
+ *   y_perm [rows, H] dtype; pos [T*K] int32; w [T, K] fp32; out [T, H] dtype
+ */
+int moe_combine(const moe_desc* desc, const void* y_perm, const int32_t* pos,
+                const float* w, void* out, void* stream);
+
+/*
+ * Load-balancing loss (jsqmd.com section 3.3):
+ *   loss = E * sum_i f_i * P_i,  P_i = psum[i] / T,  f_i = count[i] / (T*K).
+ * The raw value is returned; the caller scales it by router_aux_loss_coef.
+ *   psum [E] fp32; count [E] int32; loss [1] fp32 out (device)
+ */
+int moe_aux_loss(const moe_desc* desc, const float* psum, const int32_t* count,
+                 float* loss, void* stream);
+
+/*
+ * The whole layer: router -> dispatch -> expert FFN -> combine (+ aux loss),
+ * enqueued on one stream with no host synchronisation (mlqm.cn section 3.2).
+ *   x [T, H], out [T, H] dtype: device pointers, or host pointers if
+ *     desc->flags has MOE_FLAG_HOST_IO (then the call copies x in and out
+ *     through the workspace on `stream`; pinned host memory is fastest, and
+ *     `out` is valid once the stream has been synchronised)
+ *   aux [1] fp32 out or NULL; count [E] int32 out or NULL; dropped [1] int32
+ *     out or NULL (device pointers)
+ */
+int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg,
+                      const float* gate_bias, const void* W1, const float* b1,
+                      const void* W2, const float* b2, void* out, float* aux,
+                      int32_t* count, int32_t* dropped, void* ws, size_t ws_bytes,
+                      void* stream);
+
+/*
+ * Read and clear the workspace's device error word.  Synchronises `stream`.
+ * *code receives MOE_OK, MOE_ERR_TIMEOUT (a tensor-core kernel gave up a
+ * bounded wait) or MOE_ERR_DEVICE (an index check fired).  Returns MOE_OK or
+ * MOE_ERR_CUDA.
+ */
+int moe_get_device_error(void* ws, int32_t* code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */
