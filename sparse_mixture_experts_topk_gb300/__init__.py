@@ -1,0 +1,176 @@
+"""Python binding of the GB300 MoE layer library (``libmoe.so``).
+
+Argument marshalling only: each function below passes device pointers, sizes
+and the CUDA stream to the C entry point of the same name declared in
+``include/moe.h``; every step of the layer runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.  There is no fallback: if the
+library is missing or fails to load, every call raises.
+
+Tensor arguments are ``torch.Tensor`` objects (contiguous, on the current
+device) or ``None`` where the C call accepts NULL.  bf16 layers take
+``torch.bfloat16`` tensors, fp32 layers ``torch.float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
+    "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "lib", "library_path", "make_desc",
+    "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
+    "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
+    "moe_layer_forward", "moe_get_device_error", "workspace",
+]
+
+MOE_F32, MOE_BF16 = 0, 1
+MOE_FLAG_HOST_IO = 1 << 0
+MOE_FLAG_SIMT_FFN = 1 << 1
+MOE_FLAG_NO_DECODE = 1 << 2
+MOE_FLAG_SIMT_ROUTER = 1 << 3
+
+MOE_OK = 0
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "_lib", "libmoe.so")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {moe_status_string(code)} ({code})")
+        self.code = code
+
+
+class MoeDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("F", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_capacity_default": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
+    "moe_max_rows": (ctypes.c_int64, [ctypes.POINTER(MoeDesc)]),
+    "moe_workspace_size": (ctypes.c_int, [ctypes.POINTER(MoeDesc), ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_router_topk": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]),
+    "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]),
+    "moe_expert_ffn": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]),
+    "moe_combine": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 5),
+    "moe_aux_loss": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 4),
+    "moe_layer_forward": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]),
+    "moe_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libmoe.so`` (built by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"MoE CUDA library not built: {library_path} is missing "
+                               "(run __graft_entry__.build() or python -m "
+                               "sparse_mixture_experts_topk_gb300.build)")
+        L = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def make_desc(T, H, E, K, F, capacity=0, dtype=MOE_BF16, flags=0) -> MoeDesc:
+    return MoeDesc(int(T), int(H), int(E), int(K), int(F), int(capacity), int(dtype), int(flags))
+
+
+def moe_status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def moe_capacity_default(T: int, E: int, K: int) -> int:
+    return int(lib().moe_capacity_default(int(T), int(E), int(K)))
+
+
+def moe_max_rows(desc: MoeDesc) -> int:
+    return int(lib().moe_max_rows(ctypes.byref(desc)))
+
+
+def moe_workspace_size(desc: MoeDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def workspace(desc: MoeDesc, device=None):
+    """A zero-filled device workspace of ``moe_workspace_size(desc)`` bytes."""
+    import torch
+    return torch.zeros(max(moe_workspace_size(desc), 256), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def moe_router_topk(desc, x, Wg, gate_bias, logits, ids, w, psum, ws, stream=None):
+    _check("moe_router_topk", lib().moe_router_topk(
+        ctypes.byref(desc), _ptr(x), _ptr(Wg), _ptr(gate_bias), _ptr(logits), _ptr(ids), _ptr(w),
+        _ptr(psum), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_dispatch(desc, ids, x, count, offs, src, pos, x_perm, dropped, ws, stream=None):
+    _check("moe_dispatch", lib().moe_dispatch(
+        ctypes.byref(desc), _ptr(ids), _ptr(x), _ptr(count), _ptr(offs), _ptr(src), _ptr(pos),
+        _ptr(x_perm), _ptr(dropped), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_expert_ffn(desc, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, ws, stream=None):
+    _check("moe_expert_ffn", lib().moe_expert_ffn(
+        ctypes.byref(desc), _ptr(x_perm), _ptr(offs), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2),
+        _ptr(h_perm), _ptr(y_perm), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_combine(desc, y_perm, pos, w, out, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        ctypes.byref(desc), _ptr(y_perm), _ptr(pos), _ptr(w), _ptr(out), _stream(stream)))
+
+
+def moe_aux_loss(desc, psum, count, loss, stream=None):
+    _check("moe_aux_loss", lib().moe_aux_loss(
+        ctypes.byref(desc), _ptr(psum), _ptr(count), _ptr(loss), _stream(stream)))
+
+
+def moe_layer_forward(desc, x, Wg, gate_bias, W1, b1, W2, b2, out, aux, count, dropped, ws,
+                      stream=None):
+    _check("moe_layer_forward", lib().moe_layer_forward(
+        ctypes.byref(desc), _ptr(x), _ptr(Wg), _ptr(gate_bias), _ptr(W1), _ptr(b1), _ptr(W2),
+        _ptr(b2), _ptr(out), _ptr(aux), _ptr(count), _ptr(dropped), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_get_device_error(ws, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check("moe_get_device_error", lib().moe_get_device_error(_ptr(ws), ctypes.byref(code),
+                                                              _stream(stream)))
+    return int(code.value)

@@ -1,0 +1,307 @@
+// C ABI of the MoE layer library: argument checks, workspace layout and the
+// order of launches.  All device work is in the other translation units.
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+
+bool stream_ffn_eligible(const Shape& s);
+cudaError_t launch_ffn_simt(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
+                            const void* W1, const float* b1, const void* W2, const float* b2,
+                            void* h_perm, void* y_perm, cudaStream_t st);
+cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
+                              const float* b1, const void* W2, const float* b2, void* h_perm,
+                              void* y_perm, int* err, cudaStream_t st);
+// Tensor-core path; returns cudaErrorNotSupported when it does not apply.
+cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
+                          const void* W1, const float* b1, const void* W2, const float* b2,
+                          void* h_perm, void* y_perm, int* err, cudaStream_t st);
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
+                       const void* W1, const float* b1, const void* W2, const float* b2,
+                       void* h_perm, void* y_perm, int* err, cudaStream_t st) {
+  if (s.T == 0 || max_rows == 0) return cudaSuccess;
+  if (stream_ffn_eligible(s))
+    return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+  if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
+    cudaError_t r = launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+    if (r != cudaErrorNotSupported) return r;
+  }
+  return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
+}
+
+namespace {
+
+struct Layout {
+  size_t err, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
+  size_t x_perm, h_perm, x_stage, out_stage, total;
+  int64_t rows;
+};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int64_t rows_for(const moe_desc& d) {
+  const int64_t S = d.T * (int64_t)d.K;
+  if (d.capacity > 0) {
+    const int64_t c = (int64_t)d.E * d.capacity;
+    return c < S ? c : S;
+  }
+  return S;
+}
+
+int check_desc(const moe_desc* d) {
+  if (!d) return MOE_ERR_INVALID;
+  if (d->T < 0 || d->K < 1 || d->K > 8 || d->E < d->K || d->E > 256) return MOE_ERR_INVALID;
+  if (d->H < 8 || d->H % 8 || d->F < 8 || d->F % 8) return MOE_ERR_INVALID;
+  if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_INVALID;
+  if (d->T * (int64_t)d->K >= ((int64_t)1 << 31)) return MOE_ERR_INVALID;
+  if (d->T > 0 && (int64_t)d->H * d->T >= ((int64_t)1 << 40)) return MOE_ERR_INVALID;
+  return MOE_OK;
+}
+
+Shape shape_of(const moe_desc& d) {
+  Shape s;
+  s.T = d.T; s.H = d.H; s.E = d.E; s.K = d.K; s.F = d.F;
+  s.C = d.capacity > 0 ? d.capacity : 0;
+  s.dtype = d.dtype; s.flags = d.flags;
+  return s;
+}
+
+Layout layout_of(const moe_desc& d) {
+  const Shape s = shape_of(d);
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t S = (size_t)s.S(), E = (size_t)s.E, es = s.esize();
+  L.rows = rows_for(d);
+  L.err = take(256);
+  L.ids = take(S * 4);
+  L.w = take(S * 4);
+  L.psum_part = take((size_t)router_partials(s) * E * 4);
+  L.psum = take(E * 4);
+  L.blk_hist = take((size_t)dispatch_blocks(s) * E * 4);
+  L.blk_base = take((size_t)dispatch_blocks(s) * E * 4);
+  L.count = take(E * 4);
+  L.offs = take((E + 1) * 4);
+  L.dropped = take(4);
+  L.aux = take(4);
+  L.src = take((size_t)L.rows * 4);
+  L.pos = take(S * 4);
+  L.x_perm = take((size_t)L.rows * s.H * es);   // also holds y_perm in the layer call
+  L.h_perm = take((size_t)L.rows * s.F * es);
+  L.x_stage = L.out_stage = 0;
+  if (d.flags & MOE_FLAG_HOST_IO) {
+    L.x_stage = take((size_t)s.T * s.H * es);
+    L.out_stage = take((size_t)s.T * s.H * es);
+  }
+  L.total = off;
+  return L;
+}
+
+int check_ws(const moe_desc& d, const void* ws, size_t ws_bytes) {
+  if (!ws || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < layout_of(d).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename P> P* at(void* ws, size_t off) { return reinterpret_cast<P*>((char*)ws + off); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID: return "MOE_ERR_INVALID: bad argument (null pointer, shape or alignment)";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: layer not implemented by this library";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: a kernel index check fired";
+    default: return "unknown moe status";
+  }
+}
+
+int64_t moe_capacity_default(int64_t T, int32_t E, int32_t K) {
+  if (E <= 0 || K <= 0 || T < 0) return -1;
+  return (T + E - 1) / E * K;
+}
+
+int64_t moe_max_rows(const moe_desc* desc) {
+  if (check_desc(desc) != MOE_OK) return -1;
+  return rows_for(*desc);
+}
+
+int moe_workspace_size(const moe_desc* desc, size_t* bytes) {
+  if (check_desc(desc) != MOE_OK || !bytes) return MOE_ERR_INVALID;
+  *bytes = layout_of(*desc).total;
+  return MOE_OK;
+}
+
+int moe_router_topk(const moe_desc* desc, const void* x, const void* Wg, const float* gate_bias,
+                    float* logits, int32_t* ids, float* w, float* psum, void* ws, size_t ws_bytes,
+                    void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const moe_desc& d = *desc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (d.T > 0 && (!x || !Wg || !ids || !w)) return MOE_ERR_INVALID;
+  if ((x && !aligned16(x)) || (Wg && !aligned16(Wg))) return MOE_ERR_INVALID;
+  const Layout L = layout_of(d);
+  const Shape s = shape_of(d);
+  cudaStream_t st = (cudaStream_t)stream;
+  float* part = psum ? at<float>(ws, L.psum_part) : nullptr;
+  cudaError_t e = launch_router(s, x, Wg, gate_bias, logits, ids, w, part, at<int>(ws, L.err), st);
+  if (e == cudaSuccess && psum) e = launch_psum_reduce(s, part, psum, st);
+  return cuda_status(e);
+}
+
+int moe_dispatch(const moe_desc* desc, const int32_t* ids, const void* x, int32_t* count, int32_t* offs,
+                 int32_t* src, int32_t* pos, void* x_perm, int32_t* dropped, void* ws, size_t ws_bytes,
+                 void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const moe_desc& d = *desc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (!count || !offs || (d.T > 0 && (!ids || !src || !pos))) return MOE_ERR_INVALID;
+  if (x && (!x_perm || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID;
+  const Layout L = layout_of(d);
+  const Shape s = shape_of(d);
+  DispatchOut o;
+  memset(&o, 0, sizeof(o));
+  o.count = count; o.offs = offs; o.src = src; o.pos = pos; o.dropped = dropped;
+  o.blk_hist = at<int32_t>(ws, L.blk_hist);
+  o.blk_base = at<int32_t>(ws, L.blk_base);
+  return cuda_status(launch_dispatch(s, ids, x, x_perm, o, at<int>(ws, L.err), (cudaStream_t)stream));
+}
+
+int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs, const void* W1,
+                   const float* b1, const void* W2, const float* b2, void* h_perm, void* y_perm,
+                   void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const moe_desc& d = *desc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (!x_perm || !offs || !W1 || !W2 || !h_perm || !y_perm) return MOE_ERR_INVALID;
+  if (!aligned16(x_perm) || !aligned16(W1) || !aligned16(W2) || !aligned16(h_perm) || !aligned16(y_perm))
+    return MOE_ERR_INVALID;
+  const Layout L = layout_of(d);
+  const Shape s = shape_of(d);
+  return cuda_status(launch_ffn(s, L.rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm,
+                                at<int>(ws, L.err), (cudaStream_t)stream));
+}
+
+int moe_combine(const moe_desc* desc, const void* y_perm, const int32_t* pos, const float* w, void* out,
+                void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const moe_desc& d = *desc;
+  if (d.T > 0 && (!y_perm || !pos || !w || !out)) return MOE_ERR_INVALID;
+  if (d.T > 0 && (!aligned16(y_perm) || !aligned16(out))) return MOE_ERR_INVALID;
+  return cuda_status(launch_combine(shape_of(d), y_perm, pos, w, out, (cudaStream_t)stream));
+}
+
+int moe_aux_loss(const moe_desc* desc, const float* psum, const int32_t* count, float* loss,
+                 void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (!psum || !count || !loss) return MOE_ERR_INVALID;
+  return cuda_status(launch_aux(shape_of(*desc), psum, count, loss, (cudaStream_t)stream));
+}
+
+int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const float* gate_bias,
+                      const void* W1, const float* b1, const void* W2, const float* b2, void* out,
+                      float* aux, int32_t* count, int32_t* dropped, void* ws, size_t ws_bytes,
+                      void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const moe_desc& d = *desc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (!Wg || !W1 || !W2) return MOE_ERR_INVALID;
+  if (d.T > 0 && (!x || !out)) return MOE_ERR_INVALID;
+  if (!aligned16(Wg) || !aligned16(W1) || !aligned16(W2)) return MOE_ERR_INVALID;
+  const bool host_io = (d.flags & MOE_FLAG_HOST_IO) != 0;
+  if (!host_io && d.T > 0 && (!aligned16(x) || !aligned16(out))) return MOE_ERR_INVALID;
+  const Layout L = layout_of(d);
+  const Shape s = shape_of(d);
+  cudaStream_t st = (cudaStream_t)stream;
+  int* err = at<int>(ws, L.err);
+  const size_t xbytes = (size_t)s.T * s.H * s.esize();
+  const void* xd = x;
+  void* outd = out;
+  cudaError_t e = cudaSuccess;
+  if (host_io && s.T > 0) {
+    xd = at<void>(ws, L.x_stage);
+    outd = at<void>(ws, L.out_stage);
+    e = cudaMemcpyAsync((void*)xd, x, xbytes, cudaMemcpyHostToDevice, st);
+  }
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  float* part = at<float>(ws, L.psum_part);
+  if (e == cudaSuccess) e = launch_router(s, xd, Wg, gate_bias, nullptr, ids, w, part, err, st);
+  if (e == cudaSuccess) {
+    DispatchOut o;
+    memset(&o, 0, sizeof(o));
+    o.count = at<int32_t>(ws, L.count);
+    o.offs = at<int32_t>(ws, L.offs);
+    o.src = at<int32_t>(ws, L.src);
+    o.pos = at<int32_t>(ws, L.pos);
+    o.dropped = at<int32_t>(ws, L.dropped);
+    o.blk_hist = at<int32_t>(ws, L.blk_hist);
+    o.blk_base = at<int32_t>(ws, L.blk_base);
+    o.psum_part = part;
+    o.psum = at<float>(ws, L.psum);
+    o.aux = aux;
+    o.count_copy = count;
+    o.dropped_copy = dropped;
+    e = launch_dispatch(s, ids, xd, at<void>(ws, L.x_perm), o, err, st);
+  }
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h_perm = at<void>(ws, L.h_perm);
+  void* y_perm = x_perm;   // x_perm is dead once the first product has run
+  if (e == cudaSuccess)
+    e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err, st);
+  if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
+  if (e == cudaSuccess && host_io && s.T > 0)
+    e = cudaMemcpyAsync(out, outd, xbytes, cudaMemcpyDeviceToHost, st);
+  return cuda_status(e);
+}
+
+int moe_get_device_error(void* ws, int32_t* code, void* stream) {
+  if (!ws || !code) return MOE_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = h == kDevOk ? MOE_OK : (h == kDevTimeout ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE);
+  return MOE_OK;
+}
+
+}  // extern "C"

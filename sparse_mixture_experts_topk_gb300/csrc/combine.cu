@@ -1,0 +1,112 @@
+// Combine (weighted unpermute) and the load-balancing loss.
+//
+// Combine: the k expert outputs of a token are summed with the renormalised
+// routing weights (Qwen2-MoE code walkthrough, jsqmd.com, section 3.1 item 2;
+// MoE sparse-activation article, wmrh.cn, section 2.2, Dispatcher).  A slot
+// that the capacity dropped contributes nothing.  The sum runs in fp32 in the
+// order j = 0..K-1, so the result is deterministic.
+//
+// Loss: jsqmd.com section 3.3, load_balancing_loss: E * sum_i f_i * P_i with
+// P_i the mean router probability of expert i and f_i its share of the slots.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+// One warp per token; each lane owns 16-byte column vectors of the row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ pos,
+               const float* __restrict__ w, int64_t Tn, int K, int vec_per_row,
+               uint4* __restrict__ out) {
+  constexpr int V = Vec<T>::N;
+  constexpr int kUnroll = 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = warp0; t < Tn; t += nwarps) {
+    int p[8];
+    float wt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < K) {
+        p[j] = pos[t * K + j];
+        wt[j] = w[t * K + j];
+      }
+    }
+    for (int v0 = lane; v0 < vec_per_row; v0 += 32 * kUnroll) {
+      float acc[kUnroll][V];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[u][i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < K && p[j] >= 0) {
+          uint4 raw[kUnroll];
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + 32 * u;
+            if (v < vec_per_row) raw[u] = __ldcs(y_perm + (int64_t)p[j] * vec_per_row + v);
+          }
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + 32 * u;
+            if (v < vec_per_row) {
+              float f[V];
+              Vec<T>::unpack(raw[u], f);
+#pragma unroll
+              for (int i = 0; i < V; ++i) acc[u][i] = fmaf(wt[j], f[i], acc[u][i]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < vec_per_row) __stcs(out + t * vec_per_row + v, Vec<T>::pack(acc[u]));
+      }
+    }
+  }
+}
+
+__global__ void aux_kernel(const float* __restrict__ psum, const int32_t* __restrict__ count,
+                           int E, int64_t Tn, int K, float* __restrict__ loss) {
+  __shared__ float sa[256];
+  const int e = threadIdx.x;
+  sa[e] = (e < E && Tn > 0) ? ((float)count[e] / (float)(Tn * K)) * (psum[e] / (float)Tn) : 0.f;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (e < o) sa[e] += sa[e + o];
+    __syncthreads();
+  }
+  if (e == 0) *loss = (float)E * sa[0];
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* pos, const float* w,
+                           void* out, cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  const int vec = (int)((int64_t)s.H * s.esize() / 16);
+  int64_t grid = (s.T + 7) / 8;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (grid > cap) grid = cap;
+  if (s.dtype == MOE_BF16)
+    combine_kernel<bf16><<<(unsigned)grid, 256, 0, st>>>((const uint4*)y_perm, pos, w, s.T, s.K, vec,
+                                                        (uint4*)out);
+  else
+    combine_kernel<float><<<(unsigned)grid, 256, 0, st>>>((const uint4*)y_perm, pos, w, s.T, s.K, vec,
+                                                         (uint4*)out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_aux(const Shape& s, const float* psum, const int32_t* count, float* loss,
+                       cudaStream_t st) {
+  aux_kernel<<<1, 256, 0, st>>>(psum, count, s.E, s.T, s.K, loss);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,229 @@
+// Dispatch: group the T*K routing slots by expert, stable in slot order, with
+// the per-expert capacity, and gather the token rows into expert-contiguous
+// order.
+//
+// Qwen2-MoE code walkthrough (jsqmd.com), section 3.1 item 3: tokens are
+// regrouped by expert id with a scatter and an argsort; section 3.4: an
+// expert takes at most expert_capacity tokens and the rest are dropped.  The
+// Qwen2-MoE module article (mlqm.cn), section 2.2, gives the capacity
+// ceil(total_tokens / num_experts) * num_experts_per_tok.
+//
+// No sort is run.  Slots are cut into blocks of consecutive slots:
+//   1. hist:    per block, how many of its slots go to each expert;
+//   2. scan:    per expert, exclusive prefix over blocks (rank base of each
+//               block), totals, capacity cut, exclusive prefix over experts
+//               (offs), dropped count; optionally the probability sums and
+//               the load-balancing loss;
+//   3. scatter: per block, the stable rank of each slot among the block's
+//               slots of the same expert (warp match + per-warp counts), so
+//               rank = block base + in-block rank; kept iff rank < capacity;
+//   4. gather:  x_perm[r] = x[src[r] / K], one warp per row, 16-byte vectors.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kDispThreads = 256;
+constexpr int kDispWarps = kDispThreads / 32;
+
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslots,
+                     int32_t* __restrict__ blk_hist, int* err) {
+  __shared__ int hist[256];
+  for (int e = threadIdx.x; e < E; e += kDispThreads) hist[e] = 0;
+  __syncthreads();
+  const int64_t s0 = (int64_t)blockIdx.x * bslots;
+  const int64_t s1 = min(S, s0 + bslots);
+  for (int64_t s = s0 + threadIdx.x; s < s1; s += kDispThreads) {
+    const int e = ids[s];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else set_error(err, kDevBadIndex);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kDispThreads) blk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One block; thread e owns expert e (E <= 256).
+__global__ void __launch_bounds__(256)
+dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, int C,
+                     int32_t* __restrict__ blk_base, int32_t* __restrict__ count,
+                     int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
+                     const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
+                     float* __restrict__ aux, int64_t Tn, int K, int32_t* __restrict__ count_copy,
+                     int32_t* __restrict__ dropped_copy) {
+  __shared__ int sk[256];
+  __shared__ int sd[256];
+  __shared__ float sa[256];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    int64_t b = 0;
+    // batches of independent loads, then the dependent running sum
+    for (; b + 8 <= nblk; b += 8) {
+      int h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = blk_hist[(b + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        blk_base[(b + i) * E + e] = run;
+        run += h[i];
+      }
+    }
+    for (; b < nblk; ++b) {
+      const int h = blk_hist[b * E + e];
+      blk_base[b * E + e] = run;
+      run += h;
+    }
+  }
+  const int kept = (e < E) ? ((C > 0 && run > C) ? C : run) : 0;
+  sk[e] = kept;
+  sd[e] = (e < E) ? run - kept : 0;
+  __syncthreads();
+  // inclusive scan of kept (Hillis-Steele, 256 entries)
+  for (int o = 1; o < 256; o <<= 1) {
+    const int v = (e >= o) ? sk[e - o] : 0;
+    const int d = (e >= o) ? sd[e - o] : 0;
+    __syncthreads();
+    sk[e] += v;
+    sd[e] += d;
+    __syncthreads();
+  }
+  if (e < E) {
+    count[e] = run;
+    if (count_copy) count_copy[e] = run;
+    offs[e] = sk[e] - kept;
+    if (e == E - 1) offs[E] = sk[e];
+  }
+  if (e == 255) {
+    if (dropped) *dropped = sd[255];
+    if (dropped_copy) *dropped_copy = sd[255];
+  }
+  if (psum_part) {
+    float p = 0.f;
+    if (e < E) {
+      for (int64_t r = 0; r < prows; ++r) p += psum_part[r * E + e];
+      if (psum) psum[e] = p;
+    }
+    if (aux) {
+      // E * sum_i (count_i / (T K)) * (psum_i / T), reduced in a fixed order
+      sa[e] = (e < E && Tn > 0) ? ((float)run / (float)(Tn * K)) * (p / (float)Tn) : 0.f;
+      __syncthreads();
+      for (int o = 128; o > 0; o >>= 1) {
+        if (e < o) sa[e] += sa[e + o];
+        __syncthreads();
+      }
+      if (e == 0) *aux = (float)E * sa[0];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
+                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offs,
+                        int32_t* __restrict__ pos, int32_t* __restrict__ src) {
+  __shared__ int wcnt[kDispWarps][256];
+  __shared__ int running[256];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t s0 = (int64_t)blockIdx.x * bslots;
+  const int64_t s1 = min(S, s0 + bslots);
+  for (int e = tid; e < E; e += kDispThreads) running[e] = blk_base[(int64_t)blockIdx.x * E + e];
+  for (int64_t c0 = s0; c0 < s1; c0 += kDispThreads) {
+    for (int i = tid; i < kDispWarps * 256; i += kDispThreads) (&wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t s = c0 + tid;
+    int e = -1;
+    if (s < s1) {
+      e = ids[s];
+      if (e < 0 || e >= E) e = -1;   // reported by the histogram pass
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned below = peers & lanemask_lt();
+    if (e >= 0 && below == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (s < s1) {
+      int p = -1;
+      if (e >= 0) {
+        int r = running[e] + __popc(below);
+        for (int w2 = 0; w2 < warp; ++w2) r += wcnt[w2][e];
+        if (C <= 0 || r < C) {
+          p = offs[e] + r;
+          src[p] = (int32_t)s;
+        }
+      }
+      pos[s] = p;
+    }
+    __syncthreads();
+    for (int e2 = tid; e2 < E; e2 += kDispThreads) {
+      int add = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kDispWarps; ++w2) add += wcnt[w2][e2];
+      running[e2] += add;
+    }
+    __syncthreads();
+  }
+}
+
+// x_perm[r] = x[src[r] / K] for r < offs[E]; one warp per row.
+__global__ void __launch_bounds__(256)
+dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
+                       const int32_t* __restrict__ offs, int E, int K, int vec_per_row,
+                       uint4* __restrict__ x_perm) {
+  const int64_t rows = offs[E];
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = warp0; r < rows; r += nwarps) {
+    const int64_t t = src[r] / K;
+    const uint4* a = x + t * vec_per_row;
+    uint4* b = x_perm + r * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 u0 = a[v], u1 = a[v + 32], u2 = a[v + 64], u3 = a[v + 96];
+      b[v] = u0; b[v + 32] = u1; b[v + 64] = u2; b[v + 96] = u3;
+    }
+    for (; v < vec_per_row; v += 32) b[v] = a[v];
+  }
+}
+
+}  // namespace
+
+int dispatch_block_slots(const Shape& s) {
+  // at most 64 blocks so the per-expert scan over blocks stays short
+  int64_t b = (s.S() + 63) / 64;
+  if (b < 2048) b = 2048;
+  b = (b + kDispThreads - 1) / kDispThreads * kDispThreads;
+  return (int)b;
+}
+
+int64_t dispatch_blocks(const Shape& s) {
+  const int64_t b = dispatch_block_slots(s);
+  return (s.S() + b - 1) / b;
+}
+
+cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
+                            const DispatchOut& o, int* err, cudaStream_t st) {
+  const int64_t S = s.S();
+  const int bslots = dispatch_block_slots(s);
+  const int64_t nblk = dispatch_blocks(s);
+  if (nblk > 0) {
+    dispatch_hist_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, bslots, o.blk_hist, err);
+  }
+  dispatch_scan_kernel<<<1, 256, 0, st>>>(o.blk_hist, nblk, s.E, s.C, o.blk_base, o.count, o.offs,
+                                          o.dropped, o.psum_part, o.psum_part ? router_partials(s) : 0,
+                                          o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy);
+  if (nblk > 0) {
+    dispatch_scatter_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, s.C, bslots,
+                                                                     o.blk_base, o.offs, o.pos, o.src);
+  }
+  if (x && x_perm && S > 0) {
+    const int vec = (int)((int64_t)s.H * s.esize() / 16);
+    const int grid = sm_count() * 8;
+    dispatch_gather_kernel<<<grid, 256, 0, st>>>((const uint4*)x, o.src, o.offs, s.E, s.K, vec,
+                                                  (uint4*)x_perm);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

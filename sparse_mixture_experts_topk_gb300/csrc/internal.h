@@ -1,0 +1,68 @@
+// Host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Device error word (first error wins); lives at offset 0 of the workspace.
+enum DevErr : int { kDevOk = 0, kDevTimeout = 1, kDevBadIndex = 2 };
+
+struct Shape {
+  int64_t T;
+  int H, E, K, F, C;   // C <= 0: no capacity limit
+  int dtype;           // MOE_F32 | MOE_BF16
+  uint32_t flags;
+  int64_t S() const { return T * (int64_t)K; }
+  size_t esize() const { return dtype == MOE_BF16 ? 2 : 4; }
+};
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// ---------------------------------------------------------------- router
+// Rows of the per-block probability partial sums the router writes.
+int64_t router_partials(const Shape& s);
+cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
+                          float* logits, int32_t* ids, float* w, float* psum_part, int* err,
+                          cudaStream_t st);
+// psum[e] = sum over partial rows in order.
+cudaError_t launch_psum_reduce(const Shape& s, const float* psum_part, float* psum, cudaStream_t st);
+
+// ---------------------------------------------------------------- dispatch
+int64_t dispatch_blocks(const Shape& s);
+int dispatch_block_slots(const Shape& s);
+struct DispatchOut {
+  int32_t* count;      // [E]
+  int32_t* offs;       // [E+1]
+  int32_t* src;        // [rows]
+  int32_t* pos;        // [S]
+  int32_t* dropped;    // [1] or null
+  int32_t* blk_hist;   // [nblk * E] scratch
+  int32_t* blk_base;   // [nblk * E] scratch
+  // optional extras folded into the scan kernel
+  const float* psum_part;  // partial rows or null
+  float* psum;             // [E] or null
+  float* aux;              // [1] or null (needs psum_part)
+  int32_t* count_copy;     // [E] or null
+  int32_t* dropped_copy;   // [1] or null
+};
+cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
+                            const DispatchOut& o, int* err, cudaStream_t st);
+
+// ---------------------------------------------------------------- expert FFN
+cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
+                       const void* W1, const float* b1, const void* W2, const float* b2,
+                       void* h_perm, void* y_perm, int* err, cudaStream_t st);
+
+// ---------------------------------------------------------------- combine / aux
+cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* pos, const float* w,
+                           void* out, cudaStream_t st);
+cudaError_t launch_aux(const Shape& s, const float* psum, const int32_t* count, float* loss,
+                       cudaStream_t st);
+
+}  // namespace moe

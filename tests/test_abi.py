@@ -1,0 +1,103 @@
+"""The C ABI library loads, exports every symbol include/moe.h declares, and
+rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mixture_experts_topk_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mixture_experts_topk_gb300 import build
+    build.build()
+    return moe.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "moe_layer_forward" in names and len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+        # the binding exposes the same name
+        assert hasattr(moe, n), n
+
+
+def test_capacity_and_rows(lib):
+    assert moe.moe_capacity_default(8192, 32, 2) == 512
+    assert moe.moe_capacity_default(16384, 32, 4) == 2048
+    assert moe.moe_capacity_default(1, 32, 2) == 2
+    assert moe.moe_capacity_default(10, 0, 2) == -1
+    d = moe.make_desc(16384, 3584, 32, 4, 2560, capacity=2048)
+    assert moe.moe_max_rows(d) == 65536
+    d = moe.make_desc(16384, 3584, 32, 4, 2560, capacity=100)
+    assert moe.moe_max_rows(d) == 3200
+    d = moe.make_desc(8192, 3584, 32, 2, 2560)
+    assert moe.moe_max_rows(d) == 16384
+
+
+def test_workspace_size_grows_with_shape(lib):
+    a = moe.moe_workspace_size(moe.make_desc(64, 256, 8, 2, 512))
+    b = moe.moe_workspace_size(moe.make_desc(8192, 3584, 32, 2, 2560))
+    c = moe.moe_workspace_size(moe.make_desc(8192, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_HOST_IO))
+    assert 0 < a < b < c
+    # x_perm + h_perm dominate: rows * (H + F) * 2 bytes
+    assert b >= 16384 * (3584 + 2560) * 2
+
+
+@pytest.mark.parametrize("bad", [
+    dict(K=0), dict(K=9), dict(E=1, K=2), dict(E=257), dict(H=12), dict(F=4), dict(T=-1),
+    dict(dtype=7), dict(T=1 << 30, K=4),
+])
+def test_bad_desc_rejected(lib, bad):
+    args = dict(T=64, H=256, E=8, K=2, F=512, capacity=0, dtype=moe.MOE_BF16, flags=0)
+    args.update(bad)
+    d = moe.make_desc(**args)
+    n = ctypes.c_size_t(0)
+    assert lib.moe_workspace_size(ctypes.byref(d), ctypes.byref(n)) == -1
+    assert lib.moe_max_rows(ctypes.byref(d)) == -1
+    rc = lib.moe_layer_forward(ctypes.byref(d), *([256] * 12), 1 << 30, None)
+    assert rc == -1
+
+
+def test_host_checks_before_any_launch(lib):
+    d = moe.make_desc(64, 256, 8, 2, 512)
+    need = moe.moe_workspace_size(d)
+    A = 1 << 20          # fake, aligned addresses: never dereferenced on these paths
+    P = [A] * 11         # x .. dropped; the workspace follows
+    # workspace missing / too small / misaligned
+    assert lib.moe_layer_forward(ctypes.byref(d), *P, None, need, None) == -3
+    assert lib.moe_layer_forward(ctypes.byref(d), *P, A, need - 1, None) == -3
+    assert lib.moe_layer_forward(ctypes.byref(d), *P, A + 16, need, None) == -3
+    # a required pointer missing
+    Q = list(P); Q[1] = None          # Wg
+    assert lib.moe_layer_forward(ctypes.byref(d), *Q, A, need, None) == -1
+    # a misaligned tensor
+    Q = list(P); Q[0] = A + 2         # x
+    assert lib.moe_layer_forward(ctypes.byref(d), *Q, A, need, None) == -1
+    assert lib.moe_combine(ctypes.byref(d), A + 8, A, A, A, None) == -1
+    assert lib.moe_aux_loss(ctypes.byref(d), None, A, A, None) == -1
+    assert lib.moe_router_topk(ctypes.byref(d), A, A, None, None, None, A, None, A, need, None) == -1
+    assert lib.moe_expert_ffn(ctypes.byref(d), A, A, A, None, A, None, A, None, A, need, None) == -1
+    assert lib.moe_dispatch(ctypes.byref(d), A, None, None, A, A, A, None, None, A, need, None) == -1
+    assert lib.moe_get_device_error(None, None, None) == -1
+
+
+def test_status_strings(lib):
+    for c in (0, -1, -2, -3, -4, -5, -6):
+        assert moe.moe_status_string(c).startswith("MOE_")
+    assert "unknown" in moe.moe_status_string(42)

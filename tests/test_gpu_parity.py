@@ -1,0 +1,187 @@
+"""GPU parity: every entry point of the CUDA library against the fp64 oracle on
+the same seeded inputs.
+
+Integer results (expert ids, counts, offsets, the permutation, dropped slots)
+are compared bit-exactly, with the oracle's routing fed the GPU's own fp32
+router scores so that both sides take every top-k decision on the same
+numbers.  Floating-point results use the tolerances in ``harness``:
+  scores        max|d| / max|ref| per row <= 1e-4
+  weights       |d| <= 2e-6 (fp32 softmax of the same scores)
+  h, y (bf16)   |d| <= 2^-7 |ref| + 1e-6 (one bf16 ulp: the rounding of an
+                fp32 vs fp64 accumulation can land on either neighbour)
+  out           max-abs <= 2e-2 and rel-L2 <= 1e-2 against the oracle whose
+                h and y are rounded to bf16 (fp32 layers: rel-L2 <= 1e-4)
+"""
+import numpy as np
+import pytest
+
+from sparse_mixture_experts_topk_gb300 import workloads as W
+import sparse_mixture_experts_topk_gb300 as moe
+from oracle import moe_oracle as O
+
+from harness import (Dev, run_stages, run_layer, to_np, as_f64, logits_rel_err, out_errors,
+                     LOGITS_REL, W_ABS, PSUM_REL, OUT_MAXABS_BF16, OUT_REL_L2_BF16, OUT_REL_L2_F32)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny_f32": W.WORKLOADS["tiny"],
+    "ragged_bf16": W.small("ragged_bf16", T=333, H=512, E=8, K=2, F=768),
+    "cap_zipf_k4": W.small("cap_zipf_k4", T=300, H=256, E=8, K=4, F=384,
+                           capacity=W.capacity_ceil(300, 8, 4) // 2, gate_bias="zipf"),
+    "ffn_bias": W.small("ffn_bias", T=200, H=256, E=16, K=2, F=256, ffn_bias=True, gate_bias="zipf"),
+    "e64_k8": W.small("e64_k8", T=129, H=128, E=64, K=8, F=136),
+    "e256_k3": W.small("e256_k3", T=70, H=64, E=256, K=3, F=64),
+    "f32_ragged": W.small("f32_ragged", T=150, H=96, E=6, K=2, F=200, dtype=W.F32, ffn_bias=True),
+    "decode4": W.small("decode4", T=4, H=512, E=16, K=2, F=256, x_kind="decode_distinct"),
+    "one_token": W.small("one_token", T=1, H=256, E=8, K=2, F=128),
+    "k1": W.small("k1", T=96, H=128, E=4, K=1, F=64),
+    "k_eq_e": W.small("k_eq_e", T=40, H=64, E=4, K=4, F=64),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mixture_experts_topk_gb300 import build
+    build.build()
+    moe.lib()
+
+
+def _ulp_tol(ref):
+    return np.abs(ref) * 2.0 ** -7 + 1e-6
+
+
+def _check_routing(w, inp, r, x64, Wg64):
+    """Router scores, ids, weights and probability sums."""
+    gl = to_np(r["logits"]).astype(np.float64)
+    ref_l = O.gate_logits(x64, Wg64, inp.gate_bias)
+    assert logits_rel_err(gl, ref_l) <= LOGITS_REL
+    ids_o, w_o, p_o = O.route(gl, w.K)
+    np.testing.assert_array_equal(to_np(r["ids"]), ids_o)
+    np.testing.assert_allclose(to_np(r["w"]), w_o, rtol=0, atol=W_ABS)
+    ps = p_o.sum(axis=0)
+    np.testing.assert_allclose(to_np(r["psum"]), ps, rtol=PSUM_REL, atol=1e-6)
+    return gl, ids_o, w_o, p_o
+
+
+def _check_dispatch(w, r, ids_o, x_bytes):
+    d = O.dispatch(ids_o, w.E, w.capacity)
+    np.testing.assert_array_equal(to_np(r["count"]), d["count"])
+    np.testing.assert_array_equal(to_np(r["offs"]), d["offs"])
+    R = int(d["offs"][-1])
+    np.testing.assert_array_equal(to_np(r["src"])[:R], d["src"])
+    np.testing.assert_array_equal(to_np(r["pos"]), d["pos"])
+    assert int(to_np(r["dropped"])[0]) == d["dropped"]
+    xp = to_np(r["x_perm"])[:R]
+    np.testing.assert_array_equal(xp, x_bytes[d["src"] // w.K])
+    return d
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_stages_and_layer_small(name):
+    w = SMALL[name]
+    inp = W.generate(w)
+    dev = Dev(inp)
+    bf = w.dtype == W.BF16
+    x64, Wg64 = O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype)
+    W164, W264 = O.widen(inp.W1, w.dtype), O.widen(inp.W2, w.dtype)
+    r = run_stages(dev)
+    assert r["device_error"] == 0
+    gl, ids_o, w_o, p_o = _check_routing(w, inp, r, x64, Wg64)
+    d = _check_dispatch(w, r, ids_o, inp.x)
+    R = int(d["offs"][-1])
+
+    # expert FFN, one product at a time
+    xp = as_f64(r["x_perm"])[:R]
+    h_gpu = as_f64(r["h_perm"])[:R]
+    y_gpu = as_f64(r["y_perm"])[:R]
+    for e in range(w.E):
+        a, b = int(d["offs"][e]), int(d["offs"][e + 1])
+        if a == b:
+            continue
+        b1 = None if inp.b1 is None else inp.b1[e].astype(np.float64)
+        b2 = None if inp.b2 is None else inp.b2[e].astype(np.float64)
+        pre = xp[a:b] @ W164[e].T + (0 if b1 is None else b1)
+        h_ref = O.gelu(pre)
+        y_ref = h_gpu[a:b] @ W264[e].T + (0 if b2 is None else b2)
+        if bf:
+            h_ref, y_ref = O.round_bf16(h_ref), O.round_bf16(y_ref)
+            assert (np.abs(h_gpu[a:b] - h_ref) <= _ulp_tol(h_ref)).all(), name
+            assert (np.abs(y_gpu[a:b] - y_ref) <= _ulp_tol(y_ref)).all(), name
+        else:
+            np.testing.assert_allclose(h_gpu[a:b], h_ref, rtol=1e-5, atol=1e-5)
+            np.testing.assert_allclose(y_gpu[a:b], y_ref, rtol=1e-5, atol=1e-5)
+
+    # combine of the GPU's own expert outputs
+    out_gpu = as_f64(r["out"])
+    out_ref = O.combine(y_gpu, d["pos"], w_o)
+    tol = (np.abs(out_ref) * 2.0 ** -8 + 1e-5) if bf else (np.abs(out_ref) * 1e-6 + 1e-6)
+    assert (np.abs(out_gpu - out_ref) <= tol).all()
+    # load-balancing loss
+    aux_ref = O.aux_loss(p_o, d["count"], w.K)
+    assert abs(float(to_np(r["aux"])[0]) - aux_ref) <= 1e-5 * max(1.0, abs(aux_ref))
+
+    # the whole layer: identical to the stages, and within tolerance of the oracle
+    L = run_layer(dev)
+    assert L["device_error"] == 0
+    np.testing.assert_array_equal(to_np(L["out"]), to_np(r["out"]))
+    np.testing.assert_array_equal(to_np(L["count"]), d["count"])
+    assert int(to_np(L["dropped"])[0]) == d["dropped"]
+    assert abs(float(to_np(L["aux"])[0]) - aux_ref) <= 1e-5 * max(1.0, abs(aux_ref))
+    ref = O.layer_forward(x64, Wg64, W164, W264, w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
+                          b1=None if inp.b1 is None else inp.b1.astype(np.float64),
+                          b2=None if inp.b2 is None else inp.b2.astype(np.float64),
+                          bf16=bf, logits=gl)
+    mx, rel = out_errors(out_gpu, ref["out"])
+    if bf:
+        assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
+    else:
+        assert rel <= OUT_REL_L2_F32, rel
+
+
+def test_layer_is_deterministic():
+    w = SMALL["cap_zipf_k4"]
+    dev = Dev(W.generate(w))
+    a = run_layer(dev)
+    b = run_layer(dev)
+    np.testing.assert_array_equal(to_np(a["out"]), to_np(b["out"]))
+    assert to_np(a["aux"])[0] == to_np(b["aux"])[0]
+
+
+def test_all_logits_tied_pick_lowest_experts():
+    w = W.small("tied", T=50, H=64, E=8, K=3, F=64)
+    inp = W.generate(w)
+    inp.Wg[:] = 0                       # every score is 0
+    r = run_stages(Dev(inp))
+    ids = to_np(r["ids"])
+    assert (ids == np.arange(3)[None, :]).all()
+    np.testing.assert_allclose(to_np(r["w"]), 1.0 / 3.0, atol=1e-7)
+    assert float(to_np(r["aux"])[0]) == pytest.approx(1.0, abs=1e-6)   # uniform P -> L = 1
+
+
+def test_empty_batch():
+    w = W.small("empty", T=0, H=64, E=4, K=2, F=64)
+    inp = W.generate(w)
+    dev = Dev(inp)
+    r = run_stages(dev)
+    assert (to_np(r["count"]) == 0).all() and (to_np(r["offs"]) == 0).all()
+    L = run_layer(dev)
+    assert L["out"].numel() == 0 and int(to_np(L["dropped"])[0]) == 0
+
+
+def test_host_io_layer_matches_device_layer():
+    torch = pytest.importorskip("torch")
+    w = SMALL["ragged_bf16"]
+    dev = Dev(W.generate(w))
+    ref = run_layer(dev)
+    d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity, moe.MOE_BF16, moe.MOE_FLAG_HOST_IO)
+    ws = moe.workspace(d)
+    xh = dev.x.cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    aux = torch.empty(1, device="cuda")
+    moe.moe_layer_forward(d, xh, dev.Wg, None, dev.W1, None, dev.W2, None, outh, aux, None, None, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(outh.view(torch.int16), ref["out"].cpu().view(torch.int16))
