@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Throughput of the top-k gated MoE FFN layer forward pass on GB300.
+
+One step = one ``moe_layer_forward`` (router, dispatch, expert FFN, combine,
+load-balancing loss) over one batch resident in HBM.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Multi-GPU (torchrun): every rank runs its own batch through its own copy of the
+layer (weak scaling, no collective on the data path); rank 0 reports the
+aggregate tokens/s over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the oracle's numpy BLAS uses every host core; set before numpy loads
+_CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mixture_experts_topk_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE layer tokens/s at 1 GB300; % of bf16 tensor peak (GEMM) and HBM BW"
+FLUSH_BYTES = 512 << 20          # > 129 MB L2
+LAUNCHES_PER_STEP = 8            # router, hist, scan, scatter, gather, 2 x FFN, combine
+STAGES = ["router", "dispatch", "ffn_first", "ffn_second", "combine"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def describe(w: W.Workload) -> str:
+    cap = f" capacity={w.capacity}" if w.capacity > 0 else ""
+    return f"{w.name}: T={w.T} H={w.H} E={w.E} k={w.K} F={w.F} {w.dtype}{cap}"
+
+
+def work_counts(w: W.Workload, rows: int, used_experts: int):
+    """Algorithmic work of one layer pass: FLOPs of each expert product over
+    the kept rows, and the bytes each stage must move once."""
+    es = 2 if w.dtype == W.BF16 else 4
+    S = w.S
+    return {
+        "ffn_flops_per_product": 2.0 * rows * w.H * w.F,
+        "router": w.T * w.H * es + w.E * w.H * es + S * 8,                 # x, Wg; ids + w
+        "dispatch": w.T * w.H * es + rows * w.H * es + S * 4 * 2 + S * 4,  # x, x_perm, pos+src, ids
+        "combine": rows * w.H * es + w.T * w.H * es + S * 8,               # y_perm, out; pos + w
+        "ffn_first_bytes": used_experts * w.F * w.H * es + rows * (w.H + w.F) * es,
+        "ffn_second_bytes": used_experts * w.F * w.H * es + rows * (w.H + w.F) * es,
+    }
+
+
+class Clocks:
+    """nvidia-smi samples (arrival time, fields) while the GPU works."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self, t0: float, t1: float):
+        def pick(a, b):
+            return [f for (t, f) in self.samples if a <= t <= b and len(f) >= 7]
+        sel = pick(t0, t1)
+        window = "timed region"
+        if len(sel) < 3:                       # short region: add the loaded second before it
+            sel = pick(t0 - 1.5, t1)
+            window = "timed region + 1.5 s of warm-up under the same load"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(f[0]) for f in sel if num(f[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for f in sel for i in range(4) if f[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(sel[0][1]), "power_w_max": max(num(f[2]) or 0 for f in sel),
+                "reasons": reasons, "samples": len(sel), "window": window}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ffn_tc.cu", "tc_ptx.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_mixture_experts_topk_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the first expert product from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))
+        e = d[workload]
+        if e.get("source_hash") == source_hash():
+            return e
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def widen_inputs(inp: W.LayerInputs):
+    from oracle import moe_oracle as O
+    dt = inp.w.dtype
+    return (O.widen(inp.x, dt), O.widen(inp.Wg, dt), O.widen(inp.W1, dt), O.widen(inp.W2, dt))
+
+
+def oracle_rate(inp: W.LayerInputs, wide, n_tokens: int):
+    """Seconds for the oracle's whole layer on the first n tokens of the batch."""
+    from oracle import moe_oracle as O
+    x, Wg, W1, W2 = wide
+    w = inp.w
+    cap = W.capacity_ceil(n_tokens, w.E, w.K) if w.capacity > 0 else 0
+    t0 = time.perf_counter()
+    O.layer_forward(x[:n_tokens], Wg, W1, W2, w.K, capacity=cap, gate_bias=inp.gate_bias,
+                    bf16=(w.dtype == W.BF16))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp: W.LayerInputs, target_s: float):
+    wide = widen_inputs(inp)
+    n = 64
+    dt = oracle_rate(inp, wide, n)
+    while dt < target_s / 3 and n < inp.w.T:
+        n = min(inp.w.T, n * 4 if dt < target_s / 12 else n * 2)
+        dt = oracle_rate(inp, wide, n)
+    return {"value": n / dt, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, whole layer on the first {n} of {inp.w.T} tokens "
+                      f"({dt:.1f} s); weights widened to fp64 beforehand (untimed)"}
+
+
+def run_reference(args, w: W.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = W.generate(w)
+    wide = widen_inputs(inp)
+    budget = 150.0 / max(1, args.steps + args.warmup)     # seconds per step
+    n = 16
+    while n < w.T and oracle_rate(inp, wide, n) < budget / 2.5:
+        n *= 2
+    for _ in range(args.warmup):
+        oracle_rate(inp, wide, n)
+    times = [oracle_rate(inp, wide, n) for _ in range(args.steps)]
+    tot = sum(times)
+    value = n * args.steps / tot
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": describe(w), "sample_tokens_per_step": n},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+                             "sample": f"fp64 numpy oracle, whole layer on the first {n} of {w.T} "
+                                       f"tokens per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU path
+
+def to_dev(a, torch):
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_ours(args, w: W.Workload):
+    import torch
+    import torch.distributed as dist
+    import sparse_mixture_experts_topk_gb300 as moe
+    from sparse_mixture_experts_topk_gb300 import build as _b
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0:
+        _b.build()
+    if world > 1:
+        dist.barrier()
+    moe.lib()
+
+    # every rank has its own batch (weak scaling); weights are replicated
+    wr = W.Workload(**{**w.__dict__, "seed": w.seed + rank}) if world > 1 else w
+    inp = W.generate(wr)
+    x, Wg, W1, W2 = (to_dev(a, torch) for a in (inp.x, inp.Wg, inp.W1, inp.W2))
+    gb = to_dev(inp.gate_bias, torch)
+    dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
+    d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
+                      moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32)
+    ws = moe.workspace(d)
+    out = torch.empty((w.T, w.H), dtype=dt, device="cuda")
+    aux = torch.empty(1, device="cuda")
+    count = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    dropped = torch.empty(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_layer_forward(d, x, Wg, gb, W1, None, W2, None, out, aux, count, dropped, ws)
+
+    clocks = Clocks(local) if rank == 0 else None
+    # warm-up: W steps, and at least 1.5 s under load so clocks settle
+    t_w = time.time()
+    i = 0
+    while i < args.warmup or time.time() - t_w < args.min_warmup_s:
+        flush.zero_()
+        step()
+        i += 1
+        if i % 20 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error(ws) != 0:
+        raise RuntimeError("device error flag set during warm-up")
+    c = count.cpu().numpy()
+    rows = int(np.minimum(c, w.capacity).sum()) if w.capacity > 0 else int(c.sum())
+    used = int((c > 0).sum())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()                     # L2 flushed between timed steps
+        moe.moe_profile_events(evs[k])
+        step()
+    moe.moe_profile_events(None)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    per_step = [evs[k][0].elapsed_time(evs[k][5]) for k in range(args.steps)]
+    stage_ms = {name: statistics.mean(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps))
+                for j, name in enumerate(STAGES)}
+    total_ms = sum(per_step)
+    if world > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if moe.moe_get_device_error(ws) != 0:
+        raise RuntimeError("device error flag set in the timed region")
+
+    # end to end: pinned host x in, host out back, through the public call
+    e2e_line = None
+    if not args.no_e2e:
+        e2e_line = run_e2e(args, moe, torch, w, d, x, Wg, gb, W1, W2, aux, flush, stream, world, dist)
+    if clocks:
+        clocks.stop()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, tflops, src = peaks()
+    work = work_counts(w, rows, used)
+    value = world * w.T * args.steps / (total_ms / 1e3)
+    f1, f2 = stage_ms["ffn_first"], stage_ms["ffn_second"]
+    dom, dom_ms = ("ffn_first", f1) if f1 >= f2 else ("ffn_second", f2)
+    achieved = work["ffn_flops_per_product"] / (dom_ms / 1e3) / 1e12
+    traffic = ncu_traffic(w.name)
+    stages = {}
+    for name in STAGES:
+        ms = stage_ms[name]
+        if name.startswith("ffn"):
+            tf = work["ffn_flops_per_product"] / (ms / 1e3) / 1e12
+            stages[name] = {"ms": ms, "tflops": tf, "frac_bf16_peak": tf / tflops}
+        else:
+            gbs = work[name] / (ms / 1e3) / 1e9
+            stages[name] = {"ms": ms, "gbs": gbs, "frac_hbm": gbs / hbm}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "global_batch_tokens": world * w.T,
+                   "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write)",
+                   "parallelism": f"replicas x{world}", "kept_rows": rows, "used_experts": used},
+        "roofline": {"kernel": f"grouped_gemm_tc ({dom})", "bound": "tensor",
+                     "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                     "frac": achieved / tflops, "peak_source": f"{src} bf16 (burst)",
+                     "traffic": (traffic["dram_bytes_per_launch"] if traffic and dom == "ffn_first"
+                                 else None),
+                     "algorithmic_flops_per_launch": work["ffn_flops_per_product"]},
+        "stages": stages,
+        "e2e": e2e_line,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks.summary(t0, t1) if clocks else None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        del x, W1, W2
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, moe, torch, w, d, x, Wg, gb, W1, W2, aux, flush, stream, world, dist):
+    dh = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity, d.dtype, moe.MOE_FLAG_HOST_IO)
+    wsh = moe.workspace(dh)
+    xh = x.cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        moe.moe_layer_forward(dh, xh, Wg, gb, W1, None, W2, None, outh, aux, None, None, wsh)
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 50))
+    tot = 0.0
+    for _ in range(n):
+        flush.zero_()
+        torch.cuda.synchronize()
+        a = time.perf_counter()
+        moe.moe_layer_forward(dh, xh, Wg, gb, W1, None, W2, None, outh, aux, None, None, wsh)
+        stream.synchronize()
+        tot += time.perf_counter() - a
+    if world > 1:
+        tt = torch.tensor([tot], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        tot = float(tt.item())
+    if moe.moe_get_device_error(wsh) != 0:
+        raise RuntimeError("device error flag set in the end-to-end loop")
+    return {"value": world * w.T * n / tot, "unit": "tokens/s",
+            "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+            "d2h_bytes_per_step": int(outh.numel() * outh.element_size()),
+            "steps": n, "timing": "wall clock per call: H2D of x from pinned memory, the layer, "
+                                  "D2H of out, stream sync"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.5)
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -192,6 +192,18 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg,
                       void* stream);
 
 /*
+ * Stage timing for moe_layer_forward on the calling host thread (no
+ * counterpart on the pages; a tracing aid in the spirit of the profiler runs
+ * they describe).  `events` holds 6 cudaEvent_t created by the caller; each
+ * later moe_layer_forward on this thread records them on its stream at the
+ * stage boundaries: [0] start, [1] router done, [2] dispatch done, [3] first
+ * expert product done, [4] second product done, [5] combine done.
+ * events = NULL or n = 0 switches it off.  MOE_ERR_INVALID if n < 6 or an
+ * event is NULL.
+ */
+int moe_profile_events(void* const* events, int n);
+
+/*
  * Read and clear the workspace's device error word.  Synchronises `stream`.
  * *code receives MOE_OK, MOE_ERR_TIMEOUT (a tensor-core kernel gave up a
  * bounded wait) or MOE_ERR_DEVICE (an index check fired).  Returns MOE_OK or

@@ -20,7 +20,7 @@ __all__ = [
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "lib", "library_path", "make_desc",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
-    "moe_layer_forward", "moe_get_device_error", "workspace",
+    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "workspace",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -60,6 +60,7 @@ _SIGS = {
     "moe_aux_loss": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 4),
     "moe_layer_forward": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]),
     "moe_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "moe_profile_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
 }
 
 _lib = None
@@ -174,3 +175,16 @@ def moe_get_device_error(ws, stream=None) -> int:
     _check("moe_get_device_error", lib().moe_get_device_error(_ptr(ws), ctypes.byref(code),
                                                               _stream(stream)))
     return int(code.value)
+
+
+def moe_profile_events(events) -> None:
+    """Record the 6 given ``torch.cuda.Event`` objects at the stage boundaries of
+    every later ``moe_layer_forward`` on this thread; ``None`` switches it off."""
+    if not events:
+        _check("moe_profile_events", lib().moe_profile_events(None, 0))
+        return
+    for ev in events:            # torch creates the CUDA event on first record
+        if not ev.cuda_event:
+            ev.record()
+    arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+    _check("moe_profile_events", lib().moe_profile_events(arr, len(events)))

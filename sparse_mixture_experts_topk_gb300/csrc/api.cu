@@ -20,6 +20,15 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
                           const void* W1, const float* b1, const void* W2, const float* b2,
                           void* h_perm, void* y_perm, int* err, cudaStream_t st);
 
+namespace {
+thread_local cudaEvent_t g_prof[kMarks];
+thread_local bool g_prof_on = false;
+}  // namespace
+
+void prof_mark(int mark, cudaStream_t st) {
+  if (g_prof_on && mark >= 0 && mark < kMarks) cudaEventRecord(g_prof[mark], st);
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -38,10 +47,10 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
   if (s.T == 0 || max_rows == 0) return cudaSuccess;
   if (stream_ffn_eligible(s))
     return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
-  if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
-    cudaError_t r = launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
-    if (r != cudaErrorNotSupported) return r;
-  }
+  // bf16 runs on the tensor cores; there is no silent fallback (an
+  // unsupported shape or a missing tensor-map entry point is an error)
+  if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN))
+    return launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
   return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
 }
 
@@ -125,7 +134,10 @@ int check_ws(const moe_desc& d, const void* ws, size_t ws_bytes) {
 
 template <typename P> P* at(void* ws, size_t off) { return reinterpret_cast<P*>((char*)ws + off); }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+}
 
 }  // namespace
 }  // namespace moe
@@ -255,6 +267,7 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   const void* xd = x;
   void* outd = out;
   cudaError_t e = cudaSuccess;
+  prof_mark(kMarkStart, st);
   if (host_io && s.T > 0) {
     xd = at<void>(ws, L.x_stage);
     outd = at<void>(ws, L.out_stage);
@@ -264,6 +277,7 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   float* w = at<float>(ws, L.w);
   float* part = at<float>(ws, L.psum_part);
   if (e == cudaSuccess) e = launch_router(s, xd, Wg, gate_bias, nullptr, ids, w, part, err, st);
+  prof_mark(kMarkRouter, st);
   if (e == cudaSuccess) {
     DispatchOut o;
     memset(&o, 0, sizeof(o));
@@ -281,15 +295,32 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
     o.dropped_copy = dropped;
     e = launch_dispatch(s, ids, xd, at<void>(ws, L.x_perm), o, err, st);
   }
+  prof_mark(kMarkDispatch, st);
   void* x_perm = at<void>(ws, L.x_perm);
   void* h_perm = at<void>(ws, L.h_perm);
   void* y_perm = x_perm;   // x_perm is dead once the first product has run
   if (e == cudaSuccess)
     e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err, st);
+  prof_mark(kMarkSecond, st);
   if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
+  prof_mark(kMarkCombine, st);
   if (e == cudaSuccess && host_io && s.T > 0)
     e = cudaMemcpyAsync(out, outd, xbytes, cudaMemcpyDeviceToHost, st);
   return cuda_status(e);
+}
+
+int moe_profile_events(void* const* events, int n) {
+  if (!events || n <= 0) {
+    g_prof_on = false;
+    return MOE_OK;
+  }
+  if (n < kMarks) return MOE_ERR_INVALID;
+  for (int i = 0; i < kMarks; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID;
+    g_prof[i] = (cudaEvent_t)events[i];
+  }
+  g_prof_on = true;
+  return MOE_OK;
 }
 
 int moe_get_device_error(void* ws, int32_t* code, void* stream) {

@@ -166,6 +166,7 @@ cudaError_t run_simt(const Shape& s, int64_t max_rows, const void* x_perm, const
   dim3 g1((s.F + kBN - 1) / kBN, (unsigned)mtiles);
   grouped_gemm_simt_kernel<T, true><<<g1, kGemmThreads, 0, st>>>(
       (const T*)x_perm, offs, s.E, (const T*)W1, b1, s.F, s.H, (T*)h_perm);
+  prof_mark(kMarkFirst, st);
   dim3 g2((s.H + kBN - 1) / kBN, (unsigned)mtiles);
   grouped_gemm_simt_kernel<T, false><<<g2, kGemmThreads, 0, st>>>(
       (const T*)h_perm, offs, s.E, (const T*)W2, b2, s.H, s.F, (T*)y_perm);
@@ -180,6 +181,7 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
   dim3 g1((s.F + per_block - 1) / per_block, s.E);
   stream_ffn_kernel<T, true><<<g1, kStreamWarps * 32, 0, st>>>(
       (const T*)x_perm, offs, (const T*)W1, b1, s.F, s.H, (T*)h_perm, err);
+  prof_mark(kMarkFirst, st);
   dim3 g2((s.H + per_block - 1) / per_block, s.E);
   stream_ffn_kernel<T, false><<<g2, kStreamWarps * 32, 0, st>>>(
       (const T*)h_perm, offs, (const T*)W2, b2, s.H, s.F, (T*)y_perm, err);

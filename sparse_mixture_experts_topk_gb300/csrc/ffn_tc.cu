@@ -1,8 +1,344 @@
-// Tensor-core expert FFN: not available in this build; the CUDA-core path runs.
+// Expert FFN on the 5th-generation tensor cores: a persistent grouped GEMM
+// with TMA-staged bf16 tiles, tcgen05.mma accumulating in TMEM, and a fused
+// epilogue (bias, erf-GELU for the first product, bf16 rounding).
+//
+// Each expert is Linear -> GELU -> Linear (Qwen2-MoE module article,
+// mlqm.cn, section 2.2).  For expert e with permuted rows [offs[e], offs[e+1]):
+//   first product:  h = GELU(x_perm W1[e]^T + b1[e])   A = x_perm [rows, H], B = W1[e] [F, H]
+//   second product: y = h W2[e]^T + b2[e]              A = h_perm [rows, F], B = W2[e] [H, F]
+// Both operands are K-major (K contiguous), the nn.Linear [out, in] layout.
+//
+// Work unit: a 128 x BN output tile of one expert.  Tiles are numbered expert
+// by expert, n-tile by n-tile, m-tile fastest, so CTAs running at the same
+// time share each weight tile through L2; every CTA walks the tile list with
+// a stride of the grid size.  Warp roles inside a CTA (192 threads):
+//   warp 0     TMA producer: A and B k-blocks (64 elements = 128 bytes, 128B
+//              swizzle) into a ring of shared-memory stages;
+//   warp 1     MMA issuer (one thread): 4 x tcgen05.mma (K = 16 each) per
+//              stage into one of two TMEM accumulators; owns TMEM alloc;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (one row per thread),
+//              bias, GELU, bf16, 16-byte stores; frees the accumulator.
+// Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Every mbarrier wait is bounded: on expiry the kernel records a timeout in
+// the workspace error word, the other roles see the abort flag, in-flight
+// TMA loads and MMAs are drained (again with a bound), TMEM is freed and the
+// kernel returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
+
 namespace moe {
-cudaError_t launch_ffn_tc(const Shape&, int64_t, const void*, const int32_t*, const void*, const float*,
-                          const void*, const float*, void*, void*, int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;              // bf16 elements per k-block = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any healthy wait
+
+template <int BN>
+struct Cfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (196 * 1024) / kStageBytes > 8 ? 8 : (196 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes;
+  static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, BN);
+};
+
+template <int BN, bool kGelu>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const int32_t* __restrict__ offs, int E, int N, int K,
+                       const float* __restrict__ bias, bf16* __restrict__ C, int* err) {
+  using Cf = Cfg<BN>;
+  constexpr int S = Cf::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_offs[257];
+  __shared__ int s_tstart[257];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ __align__(8) uint64_t s_bar[2 * S + 5];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA = tc::smem_u32(smem);
+  const uint32_t sB = sA + S * Cf::kABytes;
+  auto full = [&](int s) { return tc::smem_u32(&s_bar[s]); };
+  auto empty = [&](int s) { return tc::smem_u32(&s_bar[S + s]); };
+  auto tfull = [&](int a) { return tc::smem_u32(&s_bar[2 * S + a]); };
+  auto tempty = [&](int a) { return tc::smem_u32(&s_bar[2 * S + 2 + a]); };
+  const uint32_t done_bar = tc::smem_u32(&s_bar[2 * S + 4]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = (N + BN - 1) / BN;
+  const int nk = (K + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    // per-expert tile counts and their exclusive prefix (E <= 256: 8 per lane)
+    int loc[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      int v = 0;
+      if (e < E) {
+        const int o0 = offs[e], o1 = offs[e + 1];
+        v = ((o1 - o0 + kBM - 1) / kBM) * nt;
+        s_offs[e] = o0;
+        if (e == E - 1) s_offs[E] = o1;
+      }
+      loc[i] = v;
+      sum += v;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) s_tstart[e] = run;
+      run += loc[i];
+    }
+    if (lane == 31) s_tstart[E] = incl;
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        tc::mbar_init(full(s), 1);
+        tc::mbar_init(empty(s), 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        tc::mbar_init(tfull(a), 1);
+        tc::mbar_init(tempty(a), 128);
+      }
+      tc::mbar_init(done_bar, 1);
+      s_abort = 0;
+      tc::fence_barrier_init();
+      tc::fence_proxy_async_smem();
+      tc::prefetch_tmap(&tmA);
+      tc::prefetch_tmap(&tmB);
+    }
+  } else if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(&s_tmem), Cf::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int total = s_tstart[E];
+
+  auto decode = [&](int t, int& e, int& row0, int& row_end, int& n0) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tstart[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int mt = (s_offs[e + 1] - s_offs[e] + kBM - 1) / kBM;
+    const int local = t - s_tstart[e];
+    row0 = s_offs[e] + (local % mt) * kBM;
+    row_end = s_offs[e + 1];
+    n0 = (local / mt) * BN;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t filled = 0, fill_par = 0;   // per-stage: ever filled / parity of the last fill
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int e, row0, row_end, n0;
+        decode(t, e, row0, row_end, n0);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(full(stage), Cf::kStageBytes);
+          tc::tma_load_2d(sA + stage * Cf::kABytes, &tmA, full(stage), kb * kBK, row0);
+          tc::tma_load_2d(sB + stage * Cf::kBBytes, &tmB, full(stage), kb * kBK, e * N + n0);
+          filled |= 1u << stage;
+          fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        set_error(err, kDevTimeout);
+        s_abort = 1;
+        // let every load already issued land before the CTA can exit
+        for (int s = 0; s < S; ++s)
+          if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!tc::mbar_wait(tempty(acc), acc_phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(full(stage), phase, &s_abort, kWaitNs)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t a0 = sA + stage * Cf::kABytes, b0 = sB + stage * Cf::kBBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc::mma_bf16(d, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(b0 + k * 32), Cf::kIdesc,
+                         (kb | k) != 0);
+          tc::tc_commit(empty(stage));
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc::tc_commit(tfull(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) {
+        set_error(err, kDevTimeout);
+        s_abort = 1;
+      }
+      // every MMA this thread issued must finish before TMEM is released
+      tc::tc_commit(done_bar);
+      tc::mbar_wait(done_bar, 0, nullptr, kWaitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;   // TMEM lanes 32q..32q+31 belong to this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, row0, row_end, n0;
+      decode(t, e, row0, row_end, n0);
+      if (!tc::mbar_wait(tfull(acc), acc_phase, &s_abort, kWaitNs)) {
+        set_error(err, kDevTimeout);
+        s_abort = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      const int row = row0 + q * 32 + lane;
+      const bool row_ok = row < row_end;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const float* be = bias ? bias + (int64_t)e * N : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= N) break;
+        uint32_t r[32];
+        tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+        tc::tmem_wait_ld();
+        if (row_ok) {
+          bf16* dst = C + (int64_t)row * N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + g * 8 < N) {
+              float v[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float a = __uint_as_float(r[g * 8 + j]);
+                if (be) a += be[col0 + g * 8 + j];
+                v[j] = kGelu ? gelu_erf(a) : a;
+              }
+              *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(tempty(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, Cf::kTmemCols);
+  }
 }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] as a 2D tensor map with a 64 x box_rows box.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool kGelu>
+cudaError_t run_gemm(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
+                     const float* bias, void* C, int* err, cudaStream_t st) {
+  using Cf = Cfg<BN>;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
+  if (!make_map(&mb, B, (uint64_t)E * N, (uint64_t)K, BN)) return cudaErrorNotSupported;
+  auto k = grouped_gemm_tc_kernel<BN, kGelu>;
+  cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem);
+  if (r != cudaSuccess) return r;
+  k<<<sm_count(), kThreads, Cf::kSmem, st>>>(ma, mb, offs, E, N, K, bias, (bf16*)C, err);
+  return cudaGetLastError();
+}
+
+// 256-wide tiles unless 128-wide ones pad N less.
+bool wide_tile(int N) {
+  const int64_t p256 = (int64_t)((N + 255) / 256) * 256;
+  const int64_t p128 = (int64_t)((N + 127) / 128) * 128;
+  return p256 <= p128;
+}
+
+template <bool kGelu>
+cudaError_t run_product(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
+                        const float* bias, void* C, int* err, cudaStream_t st) {
+  if (wide_tile(N)) return run_gemm<256, kGelu>(A, rows, offs, E, B, N, K, bias, C, err, st);
+  return run_gemm<128, kGelu>(A, rows, offs, E, B, N, K, bias, C, err, st);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
+                          const void* W1, const float* b1, const void* W2, const float* b2,
+                          void* h_perm, void* y_perm, int* err, cudaStream_t st) {
+  if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
+  if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
+    return cudaErrorNotSupported;
+  if (!encode_fn()) return cudaErrorNotSupported;
+  cudaError_t r = run_product<true>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
+  if (r != cudaSuccess) return r;
+  prof_mark(kMarkFirst, st);
+  return run_product<false>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);
+}
+
 }  // namespace moe

@@ -24,6 +24,12 @@ struct Shape {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Stage-boundary events of moe_layer_forward (set by moe_profile_events; no-op
+// when unset).  Marks: 0 start, 1 router, 2 dispatch, 3 first product,
+// 4 second product, 5 combine.
+enum ProfMark { kMarkStart = 0, kMarkRouter, kMarkDispatch, kMarkFirst, kMarkSecond, kMarkCombine, kMarks };
+void prof_mark(int mark, cudaStream_t st);
+
 // ---------------------------------------------------------------- router
 // Rows of the per-block probability partial sums the router writes.
 int64_t router_partials(const Shape& s);

@@ -69,6 +69,8 @@ WORKLOADS = {
                          capacity=capacity_ceil(16384, 32, 4), gate_bias="zipf"),
     # long prefill with wide hidden and many narrow experts
     "wide": Workload("wide", T=32768, H=4096, E=64, K=2, F=1408),
+    # profiler-sized case: prefill layer dims with 8 experts (weights 294 MB > L2)
+    "ncu_medium": Workload("ncu_medium", T=4096, H=3584, E=8, K=2, F=2560),
 }
 
 
