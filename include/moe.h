@@ -138,6 +138,29 @@ int moe_dispatch(const moe_desc* desc, const int32_t* ids, const void* x,
                  void* stream);
 
 /*
+ * moe_dispatch without a workspace, for callers that cannot allocate device
+ * memory where they route tokens: code running inside an allocator or memory-
+ * pool callback, runtimes that reserve all device memory up front, plugin hosts
+ * that forbid allocation on their execution path.  The pages have no
+ * counterpart; this is a library convenience.
+ *   Same arguments and results as moe_dispatch, minus ws/ws_bytes, plus
+ *   device_error [1] int32 (device, or NULL): cleared by the call, then set to
+ *   a nonzero code if an id is out of range (such slots are dropped).
+ * The per-block histograms live in a 64 KiB array in device memory owned by
+ * the library (held by every GPU that loads it until the process exits).  The
+ * layer must fit it: E * blocks <= 8192, where blocks = ceil(T*K / 2048) for
+ * T*K <= 131072 and 64 above (so E <= 128 always fits, E = 256 up to
+ * T*K = 65536); larger layers get MOE_ERR_UNSUPPORTED.  The call allocates
+ * nothing.  The first call on each device looks up the array's address (make
+ * it before any stream capture).  All calls on a device share the array:
+ * calls that overlap on the GPU race and must be serialised by the caller.
+ */
+int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, const void* x,
+                         int32_t* count, int32_t* offs, int32_t* src, int32_t* pos,
+                         void* x_perm, int32_t* dropped, int32_t* device_error,
+                         void* stream);
+
+/*
  * Expert FFN over the permuted rows: for each expert e and each row r in
  * [offs[e], offs[e+1]):
  *   h_perm[r] = GELU(W1[e] x_perm[r] + b1[e])       (GELU erf form)

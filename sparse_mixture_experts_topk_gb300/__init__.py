@@ -19,7 +19,7 @@ __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "lib", "library_path", "make_desc",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
-    "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
+    "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "workspace",
 ]
 
@@ -55,6 +55,7 @@ _SIGS = {
     "moe_workspace_size": (ctypes.c_int, [ctypes.POINTER(MoeDesc), ctypes.POINTER(ctypes.c_size_t)]),
     "moe_router_topk": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 10),
     "moe_expert_ffn": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 5),
     "moe_aux_loss": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 4),
@@ -144,6 +145,16 @@ def moe_dispatch(desc, ids, x, count, offs, src, pos, x_perm, dropped, ws, strea
     _check("moe_dispatch", lib().moe_dispatch(
         ctypes.byref(desc), _ptr(ids), _ptr(x), _ptr(count), _ptr(offs), _ptr(src), _ptr(pos),
         _ptr(x_perm), _ptr(dropped), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_dispatch_noalloc(desc, ids, x, count, offs, src, pos, x_perm, dropped, device_error,
+                         stream=None):
+    """``moe_dispatch`` for callers that cannot allocate device memory: the
+    scratch is a fixed 64 KiB array inside the library, so no workspace is
+    passed.  Calls on one device must not overlap on the GPU."""
+    _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
+        ctypes.byref(desc), _ptr(ids), _ptr(x), _ptr(count), _ptr(offs), _ptr(src), _ptr(pos),
+        _ptr(x_perm), _ptr(dropped), _ptr(device_error), _stream(stream)))
 
 
 def moe_expert_ffn(desc, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, ws, stream=None):
