@@ -211,7 +211,7 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
     dispatch_hist_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, bslots, o.blk_hist, err);
   }
   dispatch_scan_kernel<<<1, 256, 0, st>>>(o.blk_hist, nblk, s.E, s.C, o.blk_base, o.count, o.offs,
-                                          o.dropped, o.psum_part, o.psum_part ? router_partials(s) : 0,
+                                          o.dropped, o.psum_part, o.psum_part ? router_partial_rows(s) : 0,
                                           o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy);
   if (nblk > 0) {
     dispatch_scatter_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, s.C, bslots,

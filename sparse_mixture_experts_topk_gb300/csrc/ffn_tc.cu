@@ -270,41 +270,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// Row-major bf16 matrix [rows, cols] as a 2D tensor map with a 64 x box_rows box.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BN, bool kGelu>
 cudaError_t run_gemm(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
                      const float* bias, void* C, int* err, cudaStream_t st) {
   using Cf = Cfg<BN>;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
-  if (!make_map(&mb, B, (uint64_t)E * N, (uint64_t)K, BN)) return cudaErrorNotSupported;
+  if (!tma_map_bf16(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
+  if (!tma_map_bf16(&mb, B, (uint64_t)E * N, (uint64_t)K, BN)) return cudaErrorNotSupported;
   auto k = grouped_gemm_tc_kernel<BN, kGelu>;
   cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem);
   if (r != cudaSuccess) return r;
@@ -334,7 +306,6 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
     return cudaErrorNotSupported;
-  if (!encode_fn()) return cudaErrorNotSupported;
   cudaError_t r = run_product<true>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);

@@ -1,6 +1,7 @@
 // Host-side launchers shared between the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -30,9 +31,19 @@ int sm_count();
 enum ProfMark { kMarkStart = 0, kMarkRouter, kMarkDispatch, kMarkFirst, kMarkSecond, kMarkCombine, kMarks };
 void prof_mark(int mark, cudaStream_t st);
 
+// Row-major bf16 matrix [rows, cols] as a 2D TMA tensor map with a box of
+// 64 columns (128 bytes, 128-byte swizzle) x box_rows rows; false on failure.
+bool tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
 // ---------------------------------------------------------------- router
-// Rows of the per-block probability partial sums the router writes.
+// Upper bound of the rows of per-block probability partial sums the router
+// writes (workspace sizing), and the rows the chosen router writes.
 int64_t router_partials(const Shape& s);
+int64_t router_partial_rows(const Shape& s);
+bool router_on_tensor_cores(const Shape& s);
+cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
+                             float* logits, int32_t* ids, float* w, float* psum_part, int* err,
+                             cudaStream_t st);
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                           float* logits, int32_t* ids, float* w, float* psum_part, int* err,
                           cudaStream_t st);

@@ -176,11 +176,16 @@ __global__ void psum_reduce_kernel(const float* __restrict__ part, int64_t rows,
 
 int64_t router_partials(const Shape& s) { return (s.T + kRouterTok - 1) / kRouterTok; }
 
+int64_t router_partial_rows(const Shape& s) {
+  return router_on_tensor_cores(s) ? (s.T + 127) / 128 : router_partials(s);
+}
+
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                           float* logits, int32_t* ids, float* w, float* psum_part, int* err,
                           cudaStream_t st) {
-  (void)err;
   if (s.T == 0) return cudaSuccess;
+  if (router_on_tensor_cores(s))
+    return launch_router_tc(s, x, Wg, gate_bias, logits, ids, w, psum_part, err, st);
   const size_t smem = sizeof(float) * (kRouterTok * (kRouterKC + 1) + s.E * (kRouterKC + 1) +
                                        kRouterTok * (s.E + 1));
   const int64_t grid = router_partials(s);
@@ -202,7 +207,7 @@ cudaError_t launch_psum_reduce(const Shape& s, const float* psum_part, float* ps
   if (s.T == 0) {
     return cudaMemsetAsync(psum, 0, sizeof(float) * s.E, st);
   }
-  psum_reduce_kernel<<<1, 256, 0, st>>>(psum_part, router_partials(s), s.E, psum);
+  psum_reduce_kernel<<<1, 256, 0, st>>>(psum_part, router_partial_rows(s), s.E, psum);
   return cudaGetLastError();
 }
 

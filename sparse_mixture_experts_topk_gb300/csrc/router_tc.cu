@@ -1,0 +1,321 @@
+// Router on the 5th-generation tensor cores (bf16 layers).
+//
+// Same operation as the CUDA-core router (Qwen2-MoE code walkthrough,
+// jsqmd.com, section 3.1: bias-free gate linear, softmax, top-k, division of
+// the k probabilities by their sum): scores l = x Wg^T (+ bias) accumulated in
+// fp32; the k largest scores, largest first, equal scores by ascending expert
+// index; w_j = exp(l_j - m) / sum_sel exp(l_i - m); p = softmax(l) summed per
+// expert for the load-balancing loss.
+//
+// The gate product is skinny (N = E <= 256) and its cost is reading x once,
+// so the kernel is built to stream x at HBM speed:
+//   * one 128-token tile per CTA group; x and Wg k-blocks (64 bf16 = 128
+//     bytes, 128B swizzle) arrive by TMA into a 4-stage ring;
+//   * one thread issues tcgen05.mma M=128, N=E rounded up to 16, K=16 into
+//     TMEM (fp32);
+//   * the hidden dimension is split over the `ks` CTAs of a thread-block
+//     cluster so that enough SMs pull x; each CTA copies its partial scores
+//     TMEM -> shared memory, and CTA rank 0 adds the others' partials over
+//     distributed shared memory in rank order (deterministic);
+//   * rank 0 then finishes each token in one thread: bias, top-k by insertion
+//     into k registers, softmax statistics, weights; the probabilities of the
+//     tile are summed per expert in token order into psum_part[tile].
+// Every mbarrier wait is bounded; on expiry the kernel records a timeout in
+// the error word, skips the remaining work, still meets both cluster
+// barriers, frees TMEM and returns.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTok = 128;        // tokens per tile = TMEM lanes
+constexpr int kBK = 64;          // bf16 per k-block
+constexpr int kThreads = 128;
+constexpr int kStages = 4;
+constexpr int kABytes = kTok * kBK * 2;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct RouterCfg {
+  int npad;        // MMA N: E rounded up to a multiple of 16 (>= 16)
+  int tmem_cols;   // power of two >= max(32, npad)
+  int b_bytes;     // one Wg k-block: npad rows x 128 bytes
+  size_t smem;     // dynamic shared memory
+};
+
+RouterCfg router_cfg(int E) {
+  RouterCfg c;
+  c.npad = E < 16 ? 16 : (E + 15) / 16 * 16;
+  c.tmem_cols = 32;
+  while (c.tmem_cols < c.npad) c.tmem_cols *= 2;
+  c.b_bytes = c.npad * 128;
+  const size_t ring = (size_t)kStages * (kABytes + c.b_bytes);
+  const size_t part = (size_t)kTok * (c.npad + 1) * sizeof(float);
+  c.smem = 1024 + (ring > part ? ring : part);
+  return c;
+}
+
+__global__ void __launch_bounds__(kThreads)
+router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
+                 int64_t Tn, int H, int E, int K, int npad, int tmem_cols, int ks,
+                 const float* __restrict__ gate_bias, float* __restrict__ logits,
+                 int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ psum_part,
+                 int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ __align__(8) uint64_t s_bar[2 * kStages + 1];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA = tc::smem_u32(smem);
+  const int b_bytes = npad * 128;
+  const uint32_t sB = sA + kStages * kABytes;
+  float* part = reinterpret_cast<float*>(smem);   // reuses the ring once the MMAs are done
+  const int ld = npad + 1;
+  auto full = [&](int s) { return tc::smem_u32(&s_bar[s]); };
+  auto empty = [&](int s) { return tc::smem_u32(&s_bar[kStages + s]); };
+  const uint32_t done_bar = tc::smem_u32(&s_bar[2 * kStages]);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t rank = ks > 1 ? tc::cluster_ctarank() : 0;
+  const int64_t tile = blockIdx.x / ks;
+  const int64_t t0 = tile * kTok;
+  const int nk = (H + kBK - 1) / kBK;
+  const int kb0 = (int)((int64_t)nk * rank / ks);
+  const int kb1 = (int)((int64_t)nk * (rank + 1) / ks);
+  const uint32_t idesc = tc::idesc_bf16_f32(kTok, npad);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(full(s), 1);
+      tc::mbar_init(empty(s), 1);
+    }
+    tc::mbar_init(done_bar, 1);
+    s_abort = 0;
+    tc::fence_barrier_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tmap(&tmX);
+    tc::prefetch_tmap(&tmG);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(&s_tmem), tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t filled = 0, fill_par = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
+        tc::mbar_arrive_expect_tx(full(stage), kABytes + b_bytes);
+        tc::tma_load_2d(sA + stage * kABytes, &tmX, full(stage), kb * kBK, (int)t0);
+        tc::tma_load_2d(sB + stage * b_bytes, &tmG, full(stage), kb * kBK, 0);
+        filled |= 1u << stage;
+        fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) {
+        set_error(err, kDevTimeout);
+        s_abort = 1;
+        for (int s = 0; s < kStages; ++s)
+          if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!tc::mbar_wait(full(stage), phase, &s_abort, kWaitNs)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t a0 = sA + stage * kABytes, b0 = sB + stage * b_bytes;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          tc::mma_bf16(tmem, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(b0 + k * 32), idesc,
+                       (kb > kb0 || k > 0) ? 1u : 0u);
+        tc::tc_commit(empty(stage));
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) {
+        set_error(err, kDevTimeout);
+        s_abort = 1;
+      }
+      tc::tc_commit(done_bar);   // arrives once every MMA above has finished
+    }
+    __syncwarp();
+  }
+
+  // every thread: its token's partial scores, TMEM -> shared memory
+  bool ok = tc::mbar_wait(done_bar, 0, nullptr, kWaitNs);
+  if (!ok) set_error(err, kDevTimeout);
+  ok = ok && !s_abort && kb1 > kb0;
+  tc::tc_fence_after();
+  __syncthreads();                 // the ring is free: every load landed and was consumed
+  const int row = threadIdx.x;     // warp w reads TMEM lanes 32w..32w+31
+  for (int c = 0; c < npad; c += 32) {
+    uint32_t r[32];
+    tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c + j < npad) part[row * ld + c + j] = ok ? __uint_as_float(r[j]) : 0.f;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, tmem_cols);
+  }
+  if (ks > 1) {
+    tc::cluster_sync();            // every rank's partial is in its shared memory
+    if (rank == 0) {
+      const uint32_t mine = tc::smem_u32(part + row * ld);
+      for (int r = 1; r < ks; ++r) {
+        const uint32_t peer = tc::map_peer(mine, (uint32_t)r);
+        for (int e = 0; e < E; ++e) part[row * ld + e] += tc::ld_peer_f32(peer + 4u * e);
+      }
+    }
+    tc::cluster_sync();            // peers keep their shared memory until rank 0 has read it
+  }
+  if (rank != 0) return;
+
+  // ------------------------------------------------------------ per token
+  const int64_t t = t0 + row;
+  float* lr = part + row * ld;
+  if (t < Tn) {
+    for (int e = 0; e < E; ++e) lr[e] += gate_bias ? gate_bias[e] : 0.f;
+  }
+  __syncthreads();
+  if (logits) {
+    const int64_t nt = (Tn - t0) < kTok ? (Tn - t0) : kTok;
+    for (int i = threadIdx.x; i < nt * E; i += kThreads) {
+      const int rr = i / E, e = i % E;
+      logits[(t0 + rr) * E + e] = part[rr * ld + e];
+    }
+  }
+  __syncthreads();
+  if (t < Tn) {
+    float tv[8];
+    int ti[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      tv[j] = -INFINITY;
+      ti[j] = 0x7fffffff;
+    }
+    float lv = -INFINITY;          // the k-th largest so far (its slot may be empty)
+    bool lempty = true;
+    for (int e = 0; e < E; ++e) {
+      const float v = lr[e];
+      // insert after any equal score already held (those have lower indices)
+      if (lempty || v > lv) {
+        bool placed = false;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+          if (j < K && !placed) {
+            if (j > 0 && (ti[j - 1] == 0x7fffffff || tv[j - 1] < v)) {
+              tv[j] = tv[j - 1];
+              ti[j] = ti[j - 1];
+            } else {
+              tv[j] = v;
+              ti[j] = e;
+              placed = true;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j == K - 1) {
+            lv = tv[j];
+            lempty = ti[j] == 0x7fffffff;
+          }
+        }
+      }
+    }
+    const float m = tv[0];
+    float zs = 0.f;
+    for (int e = 0; e < E; ++e) {
+      const float z = expf(lr[e] - m);
+      lr[e] = z;
+      zs += z;
+    }
+    const float inv = 1.f / zs;
+    for (int e = 0; e < E; ++e) lr[e] *= inv;
+    float zsel = 0.f, z[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      z[j] = j < K ? expf(tv[j] - m) : 0.f;
+      zsel += z[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < K) {
+        ids[t * K + j] = ti[j];
+        w[t * K + j] = z[j] / zsel;
+      }
+    }
+  } else {
+    for (int e = 0; e < E; ++e) lr[e] = 0.f;
+  }
+  __syncthreads();
+  if (psum_part) {
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      float s = 0.f;
+      for (int rr = 0; rr < kTok; ++rr) s += part[rr * ld + e];
+      psum_part[tile * E + e] = s;
+    }
+  }
+}
+
+}  // namespace
+
+bool router_on_tensor_cores(const Shape& s) {
+  return s.dtype == MOE_BF16 && s.H >= kBK && s.E <= 256 && !(s.flags & MOE_FLAG_SIMT_ROUTER);
+}
+
+cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
+                             float* logits, int32_t* ids, float* w, float* psum_part, int* err,
+                             cudaStream_t st) {
+  const RouterCfg c = router_cfg(s.E);
+  CUtensorMap mx, mg;
+  if (!tma_map_bf16(&mx, x, (uint64_t)s.T, (uint64_t)s.H, kTok)) return cudaErrorNotSupported;
+  if (!tma_map_bf16(&mg, Wg, (uint64_t)s.E, (uint64_t)s.H, (uint32_t)c.npad)) return cudaErrorNotSupported;
+  const int64_t tiles = (s.T + kTok - 1) / kTok;
+  const int nk = (s.H + kBK - 1) / kBK;
+  // split the hidden dimension over a cluster until the CTAs fill the GPU
+  const int per_sm = c.smem <= 110 * 1024 ? 2 : 1;
+  const int64_t slots = (int64_t)sm_count() * per_sm;
+  int ks = 1;
+  while (ks < 8 && tiles * ks * 2 <= slots && nk >= 2 * ks) ks *= 2;
+  auto kern = router_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * ks), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = c.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mx, mg, s.T, s.H, s.E, s.K, c.npad, c.tmem_cols, ks, gate_bias,
+                            logits, ids, w, psum_part, err);
+}
+
+}  // namespace moe

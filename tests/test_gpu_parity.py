@@ -185,3 +185,25 @@ def test_host_io_layer_matches_device_layer():
     moe.moe_layer_forward(d, xh, dev.Wg, None, dev.W1, None, dev.W2, None, outh, aux, None, None, ws)
     torch.cuda.synchronize()
     assert torch.equal(outh.view(torch.int16), ref["out"].cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "cap_zipf_k4"])
+def test_cuda_core_router_and_ffn_match_oracle(name):
+    """The CUDA-core router and expert FFN (kept for fp32 layers and as a
+    cross-check) on bf16 layers, against the same oracle checks."""
+    w = SMALL[name]
+    inp = W.generate(w)
+    dev = Dev(inp)
+    x64, Wg64 = O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype)
+    r = run_stages(dev, flags=moe.MOE_FLAG_SIMT_ROUTER | moe.MOE_FLAG_SIMT_FFN)
+    assert r["device_error"] == 0
+    gl, ids_o, w_o, p_o = _check_routing(w, inp, r, x64, Wg64)
+    d = _check_dispatch(w, r, ids_o, inp.x)
+    ref = O.layer_forward(x64, Wg64, O.widen(inp.W1, w.dtype), O.widen(inp.W2, w.dtype), w.K,
+                          capacity=w.capacity, gate_bias=inp.gate_bias, bf16=True, logits=gl)
+    mx, rel = out_errors(as_f64(r["out"]), ref["out"])
+    assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
+    # and the tensor-core path picks the same experts from its own scores
+    r2 = run_stages(dev)
+    gl2 = to_np(r2["logits"]).astype(np.float64)
+    assert logits_rel_err(gl2, gl) <= 2 * LOGITS_REL
