@@ -138,8 +138,11 @@ Layout layout_of(const moe_desc& d) {
   L.w = take(S * 4);
   L.psum_part = take((size_t)router_partials(s) * E * 4);
   L.psum = take(E * 4);
-  L.blk_hist = take((size_t)dispatch_blocks(s) * E * 4);
-  L.blk_base = take((size_t)dispatch_blocks(s) * E * 4);
+  // per-block dispatch tables: the standalone blocking or the router's 128-token tiles
+  const int64_t tiles = (s.T + kRouterTileTokens - 1) / kRouterTileTokens;
+  const int64_t nblk = dispatch_blocks(s) > tiles ? dispatch_blocks(s) : tiles;
+  L.blk_hist = take((size_t)nblk * E * 4);
+  L.blk_base = take((size_t)nblk * E * 4);
   L.count = take(E * 4);
   L.offs = take((E + 1) * 4);
   L.dropped = take(4);
@@ -307,11 +310,15 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* w = at<float>(ws, L.w);
   float* part = at<float>(ws, L.psum_part);
-  if (e == cudaSuccess) e = launch_router(s, xd, Wg, gate_bias, nullptr, ids, w, part, err, st);
+  const bool fused_hist = router_on_tensor_cores(s);
+  if (e == cudaSuccess)
+    e = launch_router(s, xd, Wg, gate_bias, nullptr, ids, w, part, err, st,
+                      fused_hist ? at<int32_t>(ws, L.blk_hist) : nullptr);
   prof_mark(kMarkRouter, st);
   if (e == cudaSuccess) {
     DispatchOut o;
     memset(&o, 0, sizeof(o));
+    o.hist_ready = fused_hist;
     o.count = at<int32_t>(ws, L.count);
     o.offs = at<int32_t>(ws, L.offs);
     o.src = at<int32_t>(ws, L.src);

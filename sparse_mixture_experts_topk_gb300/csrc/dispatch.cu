@@ -45,20 +45,36 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslo
   for (int e = threadIdx.x; e < E; e += kDispThreads) blk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
-// One block; thread e owns expert e (E <= 256).
+// One block; thread e owns expert e (E <= 256).  With `staged`, the
+// [nblk, E] histogram is first copied to shared memory with coalesced loads
+// and scanned there.
 __global__ void __launch_bounds__(256)
-dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, int C,
+dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, int C, int staged,
                      int32_t* __restrict__ blk_base, int32_t* __restrict__ count,
                      int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
                      const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
                      float* __restrict__ aux, int64_t Tn, int K, int32_t* __restrict__ count_copy,
                      int32_t* __restrict__ dropped_copy) {
+  extern __shared__ int sh[];          // [nblk, E] when staged
   __shared__ int sk[256];
   __shared__ int sd[256];
   __shared__ float sa[256];
   const int e = threadIdx.x;
+  const int64_t n = nblk * E;
   int run = 0;
-  if (e < E) {
+  if (staged) {
+    for (int64_t i = threadIdx.x; i < n; i += 256) sh[i] = blk_hist[i];
+    __syncthreads();
+    if (e < E) {
+      for (int64_t b = 0; b < nblk; ++b) {
+        const int h = sh[b * E + e];
+        sh[b * E + e] = run;
+        run += h;
+      }
+    }
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += 256) blk_base[i] = sh[i];
+  } else if (e < E) {
     int64_t b = 0;
     // batches of independent loads, then the dependent running sum
     for (; b + 8 <= nblk; b += 8) {
@@ -103,7 +119,16 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
   if (psum_part) {
     float p = 0.f;
     if (e < E) {
-      for (int64_t r = 0; r < prows; ++r) p += psum_part[r * E + e];
+      // rows added in order; eight loads in flight
+      int64_t r = 0;
+      for (; r + 8 <= prows; r += 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = psum_part[(r + i) * E + e];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p += v[i];
+      }
+      for (; r < prows; ++r) p += psum_part[r * E + e];
       if (psum) psum[e] = p;
     }
     if (aux) {
@@ -125,7 +150,7 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C
                         int32_t* __restrict__ pos, int32_t* __restrict__ src) {
   __shared__ int wcnt[kDispWarps][256];
   __shared__ int running[256];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t s0 = (int64_t)blockIdx.x * bslots;
   const int64_t s1 = min(S, s0 + bslots);
   for (int e = tid; e < E; e += kDispThreads) running[e] = blk_base[(int64_t)blockIdx.x * E + e];
@@ -205,14 +230,21 @@ int64_t dispatch_blocks(const Shape& s) {
 cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
                             const DispatchOut& o, int* err, cudaStream_t st) {
   const int64_t S = s.S();
-  const int bslots = dispatch_block_slots(s);
-  const int64_t nblk = dispatch_blocks(s);
-  if (nblk > 0) {
+  // blocks of slots: the router's 128-token tiles when it already counted
+  // them, else blocks sized for a short scan
+  const int bslots = o.hist_ready ? kRouterTileTokens * s.K : dispatch_block_slots(s);
+  const int64_t nblk = o.hist_ready ? (s.T + kRouterTileTokens - 1) / kRouterTileTokens
+                                    : dispatch_blocks(s);
+  if (nblk > 0 && !o.hist_ready) {
     dispatch_hist_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, bslots, o.blk_hist, err);
   }
-  dispatch_scan_kernel<<<1, 256, 0, st>>>(o.blk_hist, nblk, s.E, s.C, o.blk_base, o.count, o.offs,
-                                          o.dropped, o.psum_part, o.psum_part ? router_partial_rows(s) : 0,
-                                          o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy);
+  const size_t sm = (size_t)nblk * s.E * sizeof(int);
+  const int staged = sm <= 96 * 1024 ? 1 : 0;
+  if (staged && sm > 48 * 1024)
+    cudaFuncSetAttribute(dispatch_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  dispatch_scan_kernel<<<1, 256, staged ? sm : 0, st>>>(
+      o.blk_hist, nblk, s.E, s.C, staged, o.blk_base, o.count, o.offs, o.dropped, o.psum_part,
+      o.psum_part ? router_partial_rows(s) : 0, o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy);
   if (nblk > 0) {
     dispatch_scatter_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, s.C, bslots,
                                                                      o.blk_base, o.offs, o.pos, o.src);

@@ -41,12 +41,15 @@ bool tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
 int64_t router_partials(const Shape& s);
 int64_t router_partial_rows(const Shape& s);
 bool router_on_tensor_cores(const Shape& s);
+// tile_hist (nullable): [ceil(T/128), E] count of each 128-token tile's
+// chosen experts, in slot order blocks of 128*K slots.
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
-                             float* logits, int32_t* ids, float* w, float* psum_part, int* err,
-                             cudaStream_t st);
+                             float* logits, int32_t* ids, float* w, float* psum_part,
+                             int32_t* tile_hist, int* err, cudaStream_t st);
+constexpr int kRouterTileTokens = 128;
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                           float* logits, int32_t* ids, float* w, float* psum_part, int* err,
-                          cudaStream_t st);
+                          cudaStream_t st, int32_t* tile_hist = nullptr);
 // psum[e] = sum over partial rows in order.
 cudaError_t launch_psum_reduce(const Shape& s, const float* psum_part, float* psum, cudaStream_t st);
 
@@ -63,6 +66,7 @@ struct DispatchOut {
   int32_t* blk_base;   // [nblk * E] scratch
   // optional extras folded into the scan kernel
   const float* psum_part;  // partial rows or null
+  bool hist_ready;         // blk_hist already holds the router's per-tile counts
   float* psum;             // [E] or null
   float* aux;              // [1] or null (needs psum_part)
   int32_t* count_copy;     // [E] or null

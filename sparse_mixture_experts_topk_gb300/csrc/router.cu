@@ -182,10 +182,10 @@ int64_t router_partial_rows(const Shape& s) {
 
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                           float* logits, int32_t* ids, float* w, float* psum_part, int* err,
-                          cudaStream_t st) {
+                          cudaStream_t st, int32_t* tile_hist) {
   if (s.T == 0) return cudaSuccess;
   if (router_on_tensor_cores(s))
-    return launch_router_tc(s, x, Wg, gate_bias, logits, ids, w, psum_part, err, st);
+    return launch_router_tc(s, x, Wg, gate_bias, logits, ids, w, psum_part, tile_hist, err, st);
   const size_t smem = sizeof(float) * (kRouterTok * (kRouterKC + 1) + s.E * (kRouterKC + 1) +
                                        kRouterTok * (s.E + 1));
   const int64_t grid = router_partials(s);

@@ -19,7 +19,10 @@
 //     distributed shared memory in rank order (deterministic);
 //   * rank 0 then finishes each token in one thread: bias, top-k by insertion
 //     into k registers, softmax statistics, weights; the probabilities of the
-//     tile are summed per expert in token order into psum_part[tile].
+//     tile are summed per expert in token order into psum_part[tile], and the
+//     tile's chosen experts are counted into tile_hist[tile] (the dispatch
+//     histogram of the tile's 128*k slots, so the layer needs no separate
+//     histogram pass).
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the error word, skips the remaining work, still meets both cluster
 // barriers, frees TMEM and returns.
@@ -62,8 +65,9 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                  int64_t Tn, int H, int E, int K, int npad, int tmem_cols, int ks,
                  const float* __restrict__ gate_bias, float* __restrict__ logits,
                  int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ psum_part,
-                 int* err) {
+                 int32_t* __restrict__ tile_hist, int* err) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_hist[256];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ __align__(8) uint64_t s_bar[2 * kStages + 1];
@@ -87,6 +91,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   const int kb1 = (int)((int64_t)nk * (rank + 1) / ks);
   const uint32_t idesc = tc::idesc_bf16_f32(kTok, npad);
 
+  for (int e = threadIdx.x; e < 256; e += kThreads) s_hist[e] = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full(s), 1);
@@ -182,10 +187,18 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   if (ks > 1) {
     tc::cluster_sync();            // every rank's partial is in its shared memory
     if (rank == 0) {
+      // own + rank 1 + rank 2 + ... per score, in that order; 16 remote loads in flight
       const uint32_t mine = tc::smem_u32(part + row * ld);
       for (int r = 1; r < ks; ++r) {
         const uint32_t peer = tc::map_peer(mine, (uint32_t)r);
-        for (int e = 0; e < E; ++e) part[row * ld + e] += tc::ld_peer_f32(peer + 4u * e);
+        for (int e0 = 0; e0 < E; e0 += 16) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = (e0 + j < E) ? tc::ld_peer_f32(peer + 4u * (e0 + j)) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (e0 + j < E) part[row * ld + e0 + j] += v[j];
+        }
       }
     }
     tc::cluster_sync();            // peers keep their shared memory until rank 0 has read it
@@ -264,18 +277,20 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       if (j < K) {
         ids[t * K + j] = ti[j];
         w[t * K + j] = z[j] / zsel;
+        atomicAdd(&s_hist[ti[j]], 1);
       }
     }
   } else {
     for (int e = 0; e < E; ++e) lr[e] = 0.f;
   }
   __syncthreads();
-  if (psum_part) {
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    if (psum_part) {
       float s = 0.f;
       for (int rr = 0; rr < kTok; ++rr) s += part[rr * ld + e];
       psum_part[tile * E + e] = s;
     }
+    if (tile_hist) tile_hist[tile * E + e] = s_hist[e];
   }
 }
 
@@ -286,8 +301,8 @@ bool router_on_tensor_cores(const Shape& s) {
 }
 
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
-                             float* logits, int32_t* ids, float* w, float* psum_part, int* err,
-                             cudaStream_t st) {
+                             float* logits, int32_t* ids, float* w, float* psum_part,
+                             int32_t* tile_hist, int* err, cudaStream_t st) {
   const RouterCfg c = router_cfg(s.E);
   CUtensorMap mx, mg;
   if (!tma_map_bf16(&mx, x, (uint64_t)s.T, (uint64_t)s.H, kTok)) return cudaErrorNotSupported;
@@ -315,7 +330,7 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, s.T, s.H, s.E, s.K, c.npad, c.tmem_cols, ks, gate_bias,
-                            logits, ids, w, psum_part, err);
+                            logits, ids, w, psum_part, tile_hist, err);
 }
 
 }  // namespace moe
