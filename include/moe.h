@@ -60,6 +60,8 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 #define MOE_FLAG_SIMT_FFN   (1u << 1) /* bf16: CUDA-core expert FFN instead of tensor cores (testing) */
 #define MOE_FLAG_NO_DECODE  (1u << 2) /* never take the small-batch weight-streaming FFN */
 #define MOE_FLAG_SIMT_ROUTER (1u << 3) /* bf16: CUDA-core router instead of tensor cores (testing) */
+#define MOE_FLAG_GEMM_SINGLE (1u << 4) /* bf16: 128x256 single-SM expert GEMM tiles */
+#define MOE_FLAG_GEMM_PAIR   (1u << 5) /* bf16: 256x256 tiles on SM pairs (cta_group::2) */
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the
@@ -172,8 +174,10 @@ int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, const void* x
  *   b1 [E, F] fp32 or NULL; b2 [E, H] fp32 or NULL
  *   h_perm [moe_max_rows, F] dtype out (intermediate, kept for inspection)
  *   y_perm [moe_max_rows, H] dtype out
- * bf16 with K-major operands runs on the tcgen05 tensor cores; fp32 runs on
- * CUDA cores; T <= 16 runs a weight-streaming kernel (unless MOE_FLAG_NO_DECODE).
+ * bf16 with K-major operands runs on the tcgen05 tensor cores, either as
+ * 128x256 tiles per SM or as 256x256 tiles per SM pair (chosen from the shape
+ * unless a MOE_FLAG_GEMM_* flag forces one); fp32 runs on CUDA cores; T <= 16
+ * runs a weight-streaming kernel (unless MOE_FLAG_NO_DECODE).
  */
 int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs,
                    const void* W1, const float* b1, const void* W2, const float* b2,

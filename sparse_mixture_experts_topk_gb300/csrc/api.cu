@@ -17,10 +17,26 @@ cudaError_t launch_ffn_simt(const Shape& s, int64_t max_rows, const void* x_perm
 cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
                               const float* b1, const void* W2, const float* b2, void* h_perm,
                               void* y_perm, int* err, cudaStream_t st);
-// Tensor-core path; returns cudaErrorNotSupported when it does not apply.
+// Tensor-core paths; return cudaErrorNotSupported when they do not apply.
 cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                           const void* W1, const float* b1, const void* W2, const float* b2,
                           void* h_perm, void* y_perm, int* err, cudaStream_t st);
+cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
+                               const void* W1, const float* b1, const void* W2, const float* b2,
+                               void* h_perm, void* y_perm, int* err, cudaStream_t st);
+
+// SM-pair tiles move a third less data per SM for the same MMA work but pad
+// each expert's rows to 256 instead of 128 (and N to 256).  Estimated cost
+// of each: padded tile area over its relative load efficiency.
+bool use_pair_gemm(const Shape& s, int64_t rows) {
+  if (s.flags & MOE_FLAG_GEMM_PAIR) return true;
+  if (s.flags & MOE_FLAG_GEMM_SINGLE) return false;
+  const double r = (double)rows;
+  auto pad = [](int n, int t) { return (double)((n + t - 1) / t * t); };
+  const double single = (r + 64.0 * s.E) * (pad(s.F, 128) + pad(s.H, 128));
+  const double paired = (r + 128.0 * s.E) * (pad(s.F, 256) + pad(s.H, 256)) / 1.5;
+  return paired < single;
+}
 
 namespace {
 thread_local cudaEvent_t g_prof[kMarks];
@@ -80,8 +96,11 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
     return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
   // bf16 runs on the tensor cores; there is no silent fallback (an
   // unsupported shape or a missing tensor-map entry point is an error)
-  if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN))
+  if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
+    if (use_pair_gemm(s, max_rows))
+      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
     return launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+  }
   return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
 }
 

@@ -10,15 +10,16 @@
 // The gate product is skinny (N = E <= 256) and its cost is reading x once,
 // so the kernel is built to stream x at HBM speed:
 //   * one 128-token tile per CTA group; x and Wg k-blocks (64 bf16 = 128
-//     bytes, 128B swizzle) arrive by TMA into a 4-stage ring;
+//     bytes, 128B swizzle) arrive by TMA into a ring of up to 8 stages (as
+//     deep as shared memory allows with the grid in one wave);
 //   * one thread issues tcgen05.mma M=128, N=E rounded up to 16, K=16 into
 //     TMEM (fp32);
-//   * the hidden dimension is split over the `ks` CTAs of a thread-block
-//     cluster so that enough SMs pull x; each CTA copies its partial scores
+//   * when the tiles fill less than half the GPU, the hidden dimension is
+//     split over a CTA pair (a 2-CTA cluster); each CTA copies its partial scores
 //     TMEM -> shared memory, and CTA rank 0 adds the others' partials over
 //     distributed shared memory in rank order (deterministic);
-//   * rank 0 then finishes each token in one thread: bias, top-k by insertion
-//     into k registers, softmax statistics, weights; the probabilities of the
+//   * rank 0 then finishes each token in one thread: bias, top-k by a
+//     branch-free insertion into k registers, softmax statistics, weights; the probabilities of the
 //     tile are summed per expert in token order into psum_part[tile], and the
 //     tile's chosen experts are counted into tile_hist[tile] (the dispatch
 //     histogram of the tile's 128*k slots, so the layer needs no separate
@@ -37,24 +38,30 @@ namespace {
 constexpr int kTok = 128;        // tokens per tile = TMEM lanes
 constexpr int kBK = 64;          // bf16 per k-block
 constexpr int kThreads = 128;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kABytes = kTok * kBK * 2;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct RouterCfg {
+  int stages;      // ring depth
   int npad;        // MMA N: E rounded up to a multiple of 16 (>= 16)
   int tmem_cols;   // power of two >= max(32, npad)
   int b_bytes;     // one Wg k-block: npad rows x 128 bytes
   size_t smem;     // dynamic shared memory
 };
 
-RouterCfg router_cfg(int E) {
+// ctas_per_sm: how many CTAs each SM must hold for the grid to run in one wave
+RouterCfg router_cfg(int E, int ctas_per_sm) {
   RouterCfg c;
   c.npad = E < 16 ? 16 : (E + 15) / 16 * 16;
   c.tmem_cols = 32;
   while (c.tmem_cols < c.npad) c.tmem_cols *= 2;
   c.b_bytes = c.npad * 128;
-  const size_t ring = (size_t)kStages * (kABytes + c.b_bytes);
+  const size_t budget = (size_t)(200 * 1024) / (size_t)(ctas_per_sm < 1 ? 1 : ctas_per_sm);
+  c.stages = (int)(budget / (size_t)(kABytes + c.b_bytes));
+  if (c.stages > kMaxStages) c.stages = kMaxStages;
+  if (c.stages < 2) c.stages = 2;
+  const size_t ring = (size_t)c.stages * (kABytes + c.b_bytes);
   const size_t part = (size_t)kTok * (c.npad + 1) * sizeof(float);
   c.smem = 1024 + (ring > part ? ring : part);
   return c;
@@ -62,7 +69,7 @@ RouterCfg router_cfg(int E) {
 
 __global__ void __launch_bounds__(kThreads)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
-                 int64_t Tn, int H, int E, int K, int npad, int tmem_cols, int ks,
+                 int64_t Tn, int H, int E, int K, int npad, int tmem_cols, int ks, int kStages,
                  const float* __restrict__ gate_bias, float* __restrict__ logits,
                  int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ psum_part,
                  int32_t* __restrict__ tile_hist, int* err) {
@@ -70,7 +77,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   __shared__ int s_hist[256];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ __align__(8) uint64_t s_bar[2 * kStages + 1];
+  __shared__ __align__(8) uint64_t s_bar[2 * kMaxStages + 1];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA = tc::smem_u32(smem);
@@ -221,6 +228,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   }
   __syncthreads();
   if (t < Tn) {
+    // the k largest so far in (score descending, index ascending) order; a
+    // candidate bubbles down the list and swaps with every held entry it
+    // precedes in that order (empty slots hold -inf and the largest index).
+    // Fully unrolled, so the list stays in registers.
     float tv[8];
     int ti[8];
 #pragma unroll
@@ -228,32 +239,19 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       tv[j] = -INFINITY;
       ti[j] = 0x7fffffff;
     }
-    float lv = -INFINITY;          // the k-th largest so far (its slot may be empty)
-    bool lempty = true;
     for (int e = 0; e < E; ++e) {
-      const float v = lr[e];
-      // insert after any equal score already held (those have lower indices)
-      if (lempty || v > lv) {
-        bool placed = false;
+      float cv = lr[e];
+      int ci = e;
 #pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (j < K && !placed) {
-            if (j > 0 && (ti[j - 1] == 0x7fffffff || tv[j - 1] < v)) {
-              tv[j] = tv[j - 1];
-              ti[j] = ti[j - 1];
-            } else {
-              tv[j] = v;
-              ti[j] = e;
-              placed = true;
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j == K - 1) {
-            lv = tv[j];
-            lempty = ti[j] == 0x7fffffff;
-          }
+      for (int j = 0; j < 8; ++j) {
+        if (j < K) {
+          const bool take = cv > tv[j] || (cv == tv[j] && ci < ti[j]);
+          const float ov = tv[j];
+          const int oi = ti[j];
+          tv[j] = take ? cv : ov;
+          ti[j] = take ? ci : oi;
+          cv = take ? ov : cv;
+          ci = take ? oi : ci;
         }
       }
     }
@@ -303,17 +301,17 @@ bool router_on_tensor_cores(const Shape& s) {
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                              float* logits, int32_t* ids, float* w, float* psum_part,
                              int32_t* tile_hist, int* err, cudaStream_t st) {
-  const RouterCfg c = router_cfg(s.E);
+  const int64_t tiles = (s.T + kTok - 1) / kTok;
+  const int nk = (s.H + kBK - 1) / kBK;
+  const int sms = sm_count();
+  // split the hidden dimension over a CTA pair when that still fits one wave
+  // (wider splits measured slower: cluster scheduling and the reduction)
+  const int ks = (tiles * 2 <= sms && nk >= 2) ? 2 : 1;
+  const int per_sm = (int)((tiles * ks + sms - 1) / sms);
+  const RouterCfg c = router_cfg(s.E, per_sm);
   CUtensorMap mx, mg;
   if (!tma_map_bf16(&mx, x, (uint64_t)s.T, (uint64_t)s.H, kTok)) return cudaErrorNotSupported;
   if (!tma_map_bf16(&mg, Wg, (uint64_t)s.E, (uint64_t)s.H, (uint32_t)c.npad)) return cudaErrorNotSupported;
-  const int64_t tiles = (s.T + kTok - 1) / kTok;
-  const int nk = (s.H + kBK - 1) / kBK;
-  // split the hidden dimension over a cluster until the CTAs fill the GPU
-  const int per_sm = c.smem <= 110 * 1024 ? 2 : 1;
-  const int64_t slots = (int64_t)sm_count() * per_sm;
-  int ks = 1;
-  while (ks < 8 && tiles * ks * 2 <= slots && nk >= 2 * ks) ks *= 2;
   auto kern = router_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
   if (e != cudaSuccess) return e;
@@ -329,8 +327,8 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mx, mg, s.T, s.H, s.E, s.K, c.npad, c.tmem_cols, ks, gate_bias,
-                            logits, ids, w, psum_part, tile_hist, err);
+  return cudaLaunchKernelEx(&cfg, kern, mx, mg, s.T, s.H, s.E, s.K, c.npad, c.tmem_cols, ks, c.stages,
+                            gate_bias, logits, ids, w, psum_part, tile_hist, err);
 }
 
 }  // namespace moe

@@ -207,3 +207,64 @@ def test_cuda_core_router_and_ffn_match_oracle(name):
     r2 = run_stages(dev)
     gl2 = to_np(r2["logits"]).astype(np.float64)
     assert logits_rel_err(gl2, gl) <= 2 * LOGITS_REL
+
+
+def test_heavily_tied_scores_route_like_the_oracle():
+    """Small-integer x and gate weights make the fp32 scores exact integers
+    with many equal values; the expert ids must still match the oracle's
+    (score descending, index ascending) order exactly, on both routers."""
+    w = W.small("ties", T=700, H=64, E=16, K=4, F=64)
+    inp = W.generate(w)
+    rng = np.random.default_rng(99)
+    inp.x[:] = W.f32_to_bf16_bits(rng.integers(-1, 2, size=inp.x.shape).astype(np.float32))
+    inp.Wg[:] = W.f32_to_bf16_bits(rng.integers(-1, 2, size=inp.Wg.shape).astype(np.float32))
+    dev = Dev(inp)
+    for flags in (0, moe.MOE_FLAG_SIMT_ROUTER):
+        r = run_stages(dev, flags=flags)
+        gl = to_np(r["logits"]).astype(np.float64)
+        ref = O.gate_logits(O.widen(inp.x, "bf16"), O.widen(inp.Wg, "bf16"))
+        np.testing.assert_array_equal(gl, ref)                 # exact integers
+        ids_o, w_o, _ = O.route(gl, w.K)
+        np.testing.assert_array_equal(to_np(r["ids"]), ids_o)
+        np.testing.assert_allclose(to_np(r["w"]), w_o, rtol=0, atol=W_ABS)
+        srt = np.sort(gl, axis=1)
+        assert (srt[:, :-1] == srt[:, 1:]).any(axis=1).mean() > 0.9   # ties everywhere
+
+
+@pytest.mark.parametrize("kind", ["single", "pair"])
+@pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "ffn_bias", "cap_zipf_k4", "e256_k3", "one_token"])
+def test_expert_gemm_kernels_match_oracle(name, kind):
+    """Both tensor-core GEMM kernels (128x256 tiles per SM, 256x256 tiles per
+    SM pair) against the oracle, product by product, and the layer output."""
+    w = SMALL[name]
+    inp = W.generate(w)
+    dev = Dev(inp)
+    flag = moe.MOE_FLAG_GEMM_SINGLE if kind == "single" else moe.MOE_FLAG_GEMM_PAIR
+    flags = flag | moe.MOE_FLAG_NO_DECODE
+    r = run_stages(dev, flags=flags)
+    assert r["device_error"] == 0
+    x64, Wg64 = O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype)
+    gl, ids_o, w_o, p_o = _check_routing(w, inp, r, x64, Wg64)
+    d = _check_dispatch(w, r, ids_o, inp.x)
+    R = int(d["offs"][-1])
+    W164, W264 = O.widen(inp.W1, w.dtype), O.widen(inp.W2, w.dtype)
+    xp, h_gpu, y_gpu = as_f64(r["x_perm"])[:R], as_f64(r["h_perm"])[:R], as_f64(r["y_perm"])[:R]
+    for e in range(w.E):
+        a, b = int(d["offs"][e]), int(d["offs"][e + 1])
+        if a == b:
+            continue
+        b1 = 0 if inp.b1 is None else inp.b1[e].astype(np.float64)
+        b2 = 0 if inp.b2 is None else inp.b2[e].astype(np.float64)
+        h_ref = O.round_bf16(O.gelu(xp[a:b] @ W164[e].T + b1))
+        y_ref = O.round_bf16(h_gpu[a:b] @ W264[e].T + b2)
+        assert (np.abs(h_gpu[a:b] - h_ref) <= _ulp_tol(h_ref)).all(), (name, kind, e)
+        assert (np.abs(y_gpu[a:b] - y_ref) <= _ulp_tol(y_ref)).all(), (name, kind, e)
+    L = run_layer(dev, flags=flags)
+    assert L["device_error"] == 0
+    np.testing.assert_array_equal(to_np(L["out"]), to_np(r["out"]))
+    ref = O.layer_forward(x64, Wg64, W164, W264, w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
+                          b1=None if inp.b1 is None else inp.b1.astype(np.float64),
+                          b2=None if inp.b2 is None else inp.b2.astype(np.float64),
+                          bf16=True, logits=gl)
+    mx, rel = out_errors(as_f64(L["out"]), ref["out"])
+    assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
