@@ -37,7 +37,9 @@ from sparse_mixture_experts_topk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE layer tokens/s at 1 GB300; % of bf16 tensor peak (GEMM) and HBM BW"
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
-LAUNCHES_PER_STEP = 8            # router, hist, scan, scatter, gather, 2 x FFN, combine
+# kernels per layer pass on the bf16 tensor-core path: router (its tiles are
+# the dispatch histogram), scan, scatter, gather, 2 x expert GEMM, combine
+LAUNCHES_PER_STEP = 7
 STAGES = ["router", "dispatch", "ffn_first", "ffn_second", "combine"]
 
 
@@ -125,14 +127,14 @@ class Clocks:
 
 def source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("ffn_tc.cu", "tc_ptx.cuh", "common.cuh"):
+    for f in ("ffn_tc.cu", "ffn_tc2.cu", "tc_ptx.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "sparse_mixture_experts_topk_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the first expert product from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    """DRAM bytes per launch of each expert product from the committed ncu
+    summary (profiles/traffic.json), if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
@@ -327,11 +329,10 @@ def run_ours(args, w: W.Workload):
         "config": {"workload": describe(w), "global_batch_tokens": world * w.T,
                    "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write)",
                    "parallelism": f"replicas x{world}", "kept_rows": rows, "used_experts": used},
-        "roofline": {"kernel": f"grouped_gemm_tc ({dom})", "bound": "tensor",
+        "roofline": {"kernel": f"expert grouped GEMM ({dom})", "bound": "tensor",
                      "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
                      "frac": achieved / tflops, "peak_source": f"{src} bf16 (burst)",
-                     "traffic": (traffic["dram_bytes_per_launch"] if traffic and dom == "ffn_first"
-                                 else None),
+                     "traffic": traffic.get(dom) if traffic else None,
                      "algorithmic_flops_per_launch": work["ffn_flops_per_product"]},
         "stages": stages,
         "e2e": e2e_line,
