@@ -69,6 +69,11 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * K = num_experts_per_tok, capacity = expert_capacity.
  * Limits: T >= 0; 1 <= K <= 8; K <= E <= 256; H, F >= 8 and multiples of 8;
  * T * K < 2^31.
+ * temperature: the router softmax is taken of l / temperature (the MoE
+ * sparse-activation article, wmrh.cn, section 5.2: 1.0 by default, 2.0
+ * flattens, 0.5 sharpens).  It changes the routing weights and the
+ * load-balancing probabilities, not which experts are chosen.  <= 0 means 1;
+ * NaN or infinity is MOE_ERR_INVALID.
  */
 typedef struct moe_desc {
   int64_t T;         /* tokens (batch * sequence, flattened)                 */
@@ -79,6 +84,7 @@ typedef struct moe_desc {
   int32_t capacity;  /* slots kept per expert; <= 0 means no limit           */
   int32_t dtype;     /* moe_dtype                                            */
   uint32_t flags;    /* MOE_FLAG_*                                           */
+  float temperature; /* router softmax temperature; <= 0 means 1             */
 } moe_desc;
 
 /* Human-readable name of a status code (static storage). */
@@ -105,10 +111,12 @@ int moe_workspace_size(const moe_desc* desc, size_t* bytes);
  *   x         [T, H]  dtype
  *   Wg        [E, H]  dtype (nn.Linear [out, in] layout)
  *   gate_bias [E] fp32 or NULL (added to the scores; the pages' gate has none)
- *   logits    [T, E] fp32 out, or NULL: the scores l, fp32-accumulated
+ *   logits    [T, E] fp32 out, or NULL: the scores l, fp32-accumulated (before
+ *             the temperature is applied)
  *   ids       [T, K] int32 out: chosen experts, largest score first, equal
  *             scores ordered by ascending expert index
- *   w         [T, K] fp32 out: p[ids] / sum_j p[ids_j]  (sum to 1)
+ *   w         [T, K] fp32 out: p[ids] / sum_j p[ids_j]  (sum to 1), with
+ *             p = softmax(l / temperature)
  *   psum      [E] fp32 out, or NULL: sum over tokens of p[t, e], summed in a
  *             fixed order (deterministic)
  */

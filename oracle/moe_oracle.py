@@ -17,7 +17,8 @@ Sources (page title, section):
        num_experts) * num_experts_per_tok), section 3.2 (forward pass: router
        logits, softmax, top-k, per-expert gather, per-expert FFN).
   [A]  MoE sparse-activation article (wmrh.cn), section 2.2 (Router, Experts,
-       Dispatcher; the k expert outputs are summed with their weights).
+       Dispatcher; the k expert outputs are summed with their weights),
+       section 5.2 (the router softmax temperature, 1.0 by default).
 
 Readings taken where the pages are silent or garbled:
   * top-k is chosen on the logits (softmax is monotone), ties to the lower
@@ -75,10 +76,13 @@ def gate_logits(x: np.ndarray, Wg: np.ndarray, gate_bias=None) -> np.ndarray:
     return l
 
 
-def softmax(l: np.ndarray) -> np.ndarray:
-    """Softmax over the expert axis ([W] 3.1; [M] 3.2 step 2)."""
-    m = l.max(axis=1, keepdims=True)
-    z = np.exp(l - m)
+def softmax(l: np.ndarray, temperature: float = 1.0) -> np.ndarray:
+    """Softmax over the expert axis ([W] 3.1; [M] 3.2 step 2) of ``l / tau``;
+    the router temperature tau is 1 unless set ([A] 5.2: 2.0 flattens the
+    distribution, 0.5 sharpens it)."""
+    a = l / temperature
+    m = a.max(axis=1, keepdims=True)
+    z = np.exp(a - m)
     return z / z.sum(axis=1, keepdims=True)
 
 
@@ -96,10 +100,12 @@ def renormalised_weights(p: np.ndarray, ids: np.ndarray) -> np.ndarray:
     return sel / sel.sum(axis=1, keepdims=True)
 
 
-def route(l: np.ndarray, k: int):
-    """Softmax, top-k and renormalisation from given logits.  Returns
-    ``(ids [T,k], w [T,k], p [T,E])``."""
-    p = softmax(l)
+def route(l: np.ndarray, k: int, temperature: float = 1.0):
+    """Softmax (at the given temperature), top-k and renormalisation from
+    given logits.  Returns ``(ids [T,k], w [T,k], p [T,E])``.  The k experts
+    are the k largest scores whatever the temperature (tau > 0 keeps the
+    order); the temperature changes the probabilities and so the weights."""
+    p = softmax(l, temperature)
     ids = topk_select(l, k)
     return ids, renormalised_weights(p, ids), p
 
@@ -155,15 +161,31 @@ def gelu(a: np.ndarray) -> np.ndarray:
     return 0.5 * a * (1.0 + _erf(a / math.sqrt(2.0)))
 
 
+def silu(a: np.ndarray) -> np.ndarray:
+    """SiLU: ``a * sigmoid(a) = a / (1 + exp(-a))`` (exp overflows to inf for
+    very negative a, giving the exact limit -0)."""
+    with np.errstate(over="ignore"):
+        return a / (1.0 + np.exp(-a))
+
+
 def expert_ffn(xr: np.ndarray, W1e: np.ndarray, W2e: np.ndarray,
-               b1e=None, b2e=None, bf16: bool = False) -> np.ndarray:
+               b1e=None, b2e=None, bf16: bool = False, act: str = "gelu") -> np.ndarray:
     """One expert on rows ``xr [n, H]``: ``y = W2 GELU(W1 x + b1) + b2``.
     ``W1e [F, H]`` and ``W2e [H, F]`` use the nn.Linear ``[out, in]`` layout.
-    On the bf16 path h and y are rounded to bf16."""
+    On the bf16 path h and y are rounded to bf16.
+
+    ``act="swiglu"``: the three-matrix expert (W1, W2, W3) of the Qwen2-MoE
+    walkthrough, section 4.6, read as ``y = W2 (SiLU(W1 x) * (W3 x))``; here
+    ``W1e [2F, H]`` stacks W1 (rows 0..F-1) over W3 (rows F..2F-1) and ``b1e``
+    is ``[2F]``."""
     a = xr @ W1e.T
     if b1e is not None:
         a = a + b1e[None, :]
-    h = gelu(a)
+    if act == "swiglu":
+        F = W1e.shape[0] // 2
+        h = silu(a[:, :F]) * a[:, F:]
+    else:
+        h = gelu(a)
     if bf16:
         h = round_bf16(h)
     y = h @ W2e.T
@@ -216,7 +238,7 @@ def aux_loss_from_psum(psum: np.ndarray, count: np.ndarray, T: int, k: int) -> f
 # whole layer
 
 
-def expert_outputs(x, d, W1, W2, b1=None, b2=None, bf16=False, E=None, ids=None):
+def expert_outputs(x, d, W1, W2, b1=None, b2=None, bf16=False, E=None, ids=None, act="gelu"):
     """``y_perm [R, H]``: every kept slot through its expert, rows in permuted order."""
     E = W1.shape[0] if E is None else E
     R = int(d["offs"][E])
@@ -230,12 +252,12 @@ def expert_outputs(x, d, W1, W2, b1=None, b2=None, bf16=False, E=None, ids=None)
         toks = d["src"][r0:r1] // k
         y_perm[r0:r1] = expert_ffn(x[toks], W1[e], W2[e],
                                    None if b1 is None else b1[e],
-                                   None if b2 is None else b2[e], bf16)
+                                   None if b2 is None else b2[e], bf16, act)
     return y_perm
 
 
 def layer_forward(x, Wg, W1, W2, k, capacity=0, gate_bias=None, b1=None, b2=None,
-                  bf16=False, logits=None):
+                  bf16=False, logits=None, temperature=1.0, act="gelu"):
     """The full forward pass of [M] 3.2 with the weighted combine of [W] 3.1.
 
     All arrays are float64 values.  If ``logits`` is given (e.g. the GPU's fp32
@@ -244,15 +266,15 @@ def layer_forward(x, Wg, W1, W2, k, capacity=0, gate_bias=None, b1=None, b2=None
     T = x.shape[0]
     E = Wg.shape[0]
     l = gate_logits(x, Wg, gate_bias) if logits is None else np.asarray(logits, np.float64)
-    ids, w, p = route(l, k)
+    ids, w, p = route(l, k, temperature)
     d = dispatch(ids, E, capacity)
-    y_perm = expert_outputs(x, d, W1, W2, b1, b2, bf16, E, ids)
+    y_perm = expert_outputs(x, d, W1, W2, b1, b2, bf16, E, ids, act)
     out = combine(y_perm, d["pos"], w)
     return dict(logits=l, ids=ids, w=w, p=p, y_perm=y_perm, out=out,
                 aux=aux_loss(p, d["count"], k), **d)
 
 
-def token_outputs(x, ids, w, pos, W1, W2, tokens, b1=None, b2=None, bf16=False):
+def token_outputs(x, ids, w, pos, W1, W2, tokens, b1=None, b2=None, bf16=False, act="gelu"):
     """``out`` rows for a subset of tokens only, given the routing.  A token's
     output depends on its own row, its k choices and their kept/dropped state,
     so this is exact for each listed token."""
@@ -266,6 +288,6 @@ def token_outputs(x, ids, w, pos, W1, W2, tokens, b1=None, b2=None, bf16=False):
             e = int(ids[t, j])
             y = expert_ffn(x[t:t + 1], W1[e], W2[e],
                            None if b1 is None else b1[e],
-                           None if b2 is None else b2[e], bf16)
+                           None if b2 is None else b2[e], bf16, act)
             out[i] += w[t, j] * y[0]
     return out

@@ -46,7 +46,7 @@ class MoeError(RuntimeError):
 class MoeDesc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("F", ctypes.c_int32), ("capacity", ctypes.c_int32),
-                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32), ("temperature", ctypes.c_float)]
 
 
 _P = ctypes.c_void_p
@@ -108,8 +108,9 @@ def _check(fn, rc):
         raise MoeError(fn, rc)
 
 
-def make_desc(T, H, E, K, F, capacity=0, dtype=MOE_BF16, flags=0) -> MoeDesc:
-    return MoeDesc(int(T), int(H), int(E), int(K), int(F), int(capacity), int(dtype), int(flags))
+def make_desc(T, H, E, K, F, capacity=0, dtype=MOE_BF16, flags=0, temperature=1.0) -> MoeDesc:
+    return MoeDesc(int(T), int(H), int(E), int(K), int(F), int(capacity), int(dtype), int(flags),
+                   float(temperature))
 
 
 def moe_status_string(code: int) -> str:

@@ -130,6 +130,8 @@ int check_desc(const moe_desc* d) {
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_INVALID;
   if (d->T * (int64_t)d->K >= ((int64_t)1 << 31)) return MOE_ERR_INVALID;
   if (d->T > 0 && (int64_t)d->H * d->T >= ((int64_t)1 << 40)) return MOE_ERR_INVALID;
+  if (!(d->temperature == d->temperature) || d->temperature > 3.0e38f || d->temperature < -3.0e38f)
+    return MOE_ERR_INVALID;   // NaN or infinite
   return MOE_OK;
 }
 
@@ -138,6 +140,7 @@ Shape shape_of(const moe_desc& d) {
   s.T = d.T; s.H = d.H; s.E = d.E; s.K = d.K; s.F = d.F;
   s.C = d.capacity > 0 ? d.capacity : 0;
   s.dtype = d.dtype; s.flags = d.flags;
+  s.inv_tau = d.temperature > 0.f ? 1.f / d.temperature : 1.f;
   return s;
 }
 

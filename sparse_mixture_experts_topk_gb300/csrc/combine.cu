@@ -23,6 +23,7 @@ combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ pos
                uint4* __restrict__ out) {
   constexpr int V = Vec<T>::N;
   constexpr int kUnroll = 4;
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -75,6 +76,7 @@ combine_kernel(const uint4* __restrict__ y_perm, const int32_t* __restrict__ pos
 __global__ void aux_kernel(const float* __restrict__ psum, const int32_t* __restrict__ count,
                            int E, int64_t Tn, int K, float* __restrict__ loss) {
   __shared__ float sa[256];
+  pdl_enter();
   const int e = threadIdx.x;
   sa[e] = (e < E && Tn > 0) ? ((float)count[e] / (float)(Tn * K)) * (psum[e] / (float)Tn) : 0.f;
   __syncthreads();
@@ -95,18 +97,15 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* po
   const int64_t cap = (int64_t)sm_count() * 8;
   if (grid > cap) grid = cap;
   if (s.dtype == MOE_BF16)
-    combine_kernel<bf16><<<(unsigned)grid, 256, 0, st>>>((const uint4*)y_perm, pos, w, s.T, s.K, vec,
-                                                        (uint4*)out);
-  else
-    combine_kernel<float><<<(unsigned)grid, 256, 0, st>>>((const uint4*)y_perm, pos, w, s.T, s.K, vec,
-                                                         (uint4*)out);
-  return cudaGetLastError();
+    return launch_kernel(combine_kernel<bf16>, dim3((unsigned)grid), dim3(256), 0, st, 1,
+                         (const uint4*)y_perm, pos, w, s.T, s.K, vec, (uint4*)out);
+  return launch_kernel(combine_kernel<float>, dim3((unsigned)grid), dim3(256), 0, st, 1,
+                       (const uint4*)y_perm, pos, w, s.T, s.K, vec, (uint4*)out);
 }
 
 cudaError_t launch_aux(const Shape& s, const float* psum, const int32_t* count, float* loss,
                        cudaStream_t st) {
-  aux_kernel<<<1, 256, 0, st>>>(psum, count, s.E, s.T, s.K, loss);
-  return cudaGetLastError();
+  return launch_kernel(aux_kernel, dim3(1), dim3(256), 0, st, 1, psum, count, s.E, s.T, s.K, loss);
 }
 
 }  // namespace moe

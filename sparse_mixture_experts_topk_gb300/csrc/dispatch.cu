@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kDispThreads)
 dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslots,
                      int32_t* __restrict__ blk_hist, int* err) {
   __shared__ int hist[256];
+  pdl_enter();
   for (int e = threadIdx.x; e < E; e += kDispThreads) hist[e] = 0;
   __syncthreads();
   const int64_t s0 = (int64_t)blockIdx.x * bslots;
@@ -59,6 +60,7 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
   __shared__ int sk[256];
   __shared__ int sd[256];
   __shared__ float sa[256];
+  pdl_enter();
   const int e = threadIdx.x;
   const int64_t n = nblk * E;
   int run = 0;
@@ -150,6 +152,7 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C
                         int32_t* __restrict__ pos, int32_t* __restrict__ src) {
   __shared__ int wcnt[kDispWarps][256];
   __shared__ int running[256];
+  pdl_enter();
   const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t s0 = (int64_t)blockIdx.x * bslots;
   const int64_t s1 = min(S, s0 + bslots);
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
                        const int32_t* __restrict__ offs, int E, int K, int vec_per_row,
                        uint4* __restrict__ x_perm) {
+  pdl_enter();
   const int64_t rows = offs[E];
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -235,26 +239,28 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
   const int bslots = o.hist_ready ? kRouterTileTokens * s.K : dispatch_block_slots(s);
   const int64_t nblk = o.hist_ready ? (s.T + kRouterTileTokens - 1) / kRouterTileTokens
                                     : dispatch_blocks(s);
-  if (nblk > 0 && !o.hist_ready) {
-    dispatch_hist_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, bslots, o.blk_hist, err);
-  }
+  cudaError_t e = cudaSuccess;
+  if (nblk > 0 && !o.hist_ready)
+    e = launch_kernel(dispatch_hist_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
+                      bslots, o.blk_hist, err);
   const size_t sm = (size_t)nblk * s.E * sizeof(int);
   const int staged = sm <= 96 * 1024 ? 1 : 0;
-  if (staged && sm > 48 * 1024)
-    cudaFuncSetAttribute(dispatch_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  dispatch_scan_kernel<<<1, 256, staged ? sm : 0, st>>>(
-      o.blk_hist, nblk, s.E, s.C, staged, o.blk_base, o.count, o.offs, o.dropped, o.psum_part,
-      o.psum_part ? router_partial_rows(s) : 0, o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy);
-  if (nblk > 0) {
-    dispatch_scatter_kernel<<<(unsigned)nblk, kDispThreads, 0, st>>>(ids, S, s.E, s.C, bslots,
-                                                                     o.blk_base, o.offs, o.pos, o.src);
-  }
-  if (x && x_perm && S > 0) {
+  if (e == cudaSuccess && staged && sm > 48 * 1024)
+    e = cudaFuncSetAttribute(dispatch_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e == cudaSuccess)
+    e = launch_kernel(dispatch_scan_kernel, dim3(1), dim3(256), staged ? sm : 0, st, 1,
+                      (const int32_t*)o.blk_hist, nblk, s.E, s.C, staged, o.blk_base, o.count, o.offs,
+                      o.dropped, o.psum_part, o.psum_part ? router_partial_rows(s) : (int64_t)0, o.psum, o.aux,
+                      s.T, s.K, o.count_copy, o.dropped_copy);
+  if (e == cudaSuccess && nblk > 0)
+    e = launch_kernel(dispatch_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
+                      s.C, bslots, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos, o.src);
+  if (e == cudaSuccess && x && x_perm && S > 0) {
     const int vec = (int)((int64_t)s.H * s.esize() / 16);
-    const int grid = sm_count() * 8;
-    dispatch_gather_kernel<<<grid, 256, 0, st>>>((const uint4*)x, o.src, o.offs, s.E, s.K, vec,
-                                                  (uint4*)x_perm);
+    e = launch_kernel(dispatch_gather_kernel, dim3(sm_count() * 8), dim3(256), 0, st, 1, (const uint4*)x,
+                      (const int32_t*)o.src, (const int32_t*)o.offs, s.E, s.K, vec, (uint4*)x_perm);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -72,6 +72,7 @@ extern "C" int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, co
   s.T = d.T; s.H = d.H; s.E = d.E; s.K = d.K; s.F = d.F;
   s.C = d.capacity > 0 ? d.capacity : 0;
   s.dtype = d.dtype; s.flags = d.flags;
+  s.inv_tau = 1.f;
   const size_t table = (size_t)dispatch_blocks(s) * s.E * sizeof(int32_t);
   if (2 * table > kScratchBytes) return MOE_ERR_UNSUPPORTED;   // beyond the fixed scratch
   void* base = nullptr;

@@ -43,6 +43,7 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
   __shared__ int s_e, s_r0, s_r1;
   __shared__ float As[kBK][kBM + 4];
   __shared__ float Bs[kBK][kBN + 4];
+  pdl_enter();
   if (threadIdx.x == 0) {
     int e, r0, r1;
     if (!find_tile(offs, E, blockIdx.y, kBM, &e, &r0, &r1)) e = -1;
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32)
 stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs,
                   const T* __restrict__ B, const float* __restrict__ bias, int N, int K,
                   T* __restrict__ C, int* err) {
+  pdl_enter();
   const int e = blockIdx.y;
   const int r0 = offs[e], r1 = offs[e + 1];
   int m = r1 - r0;
@@ -164,13 +166,13 @@ cudaError_t run_simt(const Shape& s, int64_t max_rows, const void* x_perm, const
   const int64_t mtiles = (max_rows + kBM - 1) / kBM + s.E;
   if (mtiles > 65535) return cudaErrorInvalidConfiguration;
   dim3 g1((s.F + kBN - 1) / kBN, (unsigned)mtiles);
-  grouped_gemm_simt_kernel<T, true><<<g1, kGemmThreads, 0, st>>>(
-      (const T*)x_perm, offs, s.E, (const T*)W1, b1, s.F, s.H, (T*)h_perm);
+  cudaError_t e = launch_kernel(grouped_gemm_simt_kernel<T, true>, g1, dim3(kGemmThreads), 0, st, 1,
+                                (const T*)x_perm, offs, s.E, (const T*)W1, b1, s.F, s.H, (T*)h_perm);
+  if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
   dim3 g2((s.H + kBN - 1) / kBN, (unsigned)mtiles);
-  grouped_gemm_simt_kernel<T, false><<<g2, kGemmThreads, 0, st>>>(
-      (const T*)h_perm, offs, s.E, (const T*)W2, b2, s.H, s.F, (T*)y_perm);
-  return cudaGetLastError();
+  return launch_kernel(grouped_gemm_simt_kernel<T, false>, g2, dim3(kGemmThreads), 0, st, 1,
+                       (const T*)h_perm, offs, s.E, (const T*)W2, b2, s.H, s.F, (T*)y_perm);
 }
 
 template <typename T>
@@ -179,13 +181,13 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
                        int* err, cudaStream_t st) {
   const int per_block = kStreamWarps * kStreamRowsPerWarp;
   dim3 g1((s.F + per_block - 1) / per_block, s.E);
-  stream_ffn_kernel<T, true><<<g1, kStreamWarps * 32, 0, st>>>(
-      (const T*)x_perm, offs, (const T*)W1, b1, s.F, s.H, (T*)h_perm, err);
+  cudaError_t e = launch_kernel(stream_ffn_kernel<T, true>, g1, dim3(kStreamWarps * 32), 0, st, 1,
+                                (const T*)x_perm, offs, (const T*)W1, b1, s.F, s.H, (T*)h_perm, err);
+  if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
   dim3 g2((s.H + per_block - 1) / per_block, s.E);
-  stream_ffn_kernel<T, false><<<g2, kStreamWarps * 32, 0, st>>>(
-      (const T*)h_perm, offs, (const T*)W2, b2, s.H, s.F, (T*)y_perm, err);
-  return cudaGetLastError();
+  return launch_kernel(stream_ffn_kernel<T, false>, g2, dim3(kStreamWarps * 32), 0, st, 1,
+                       (const T*)h_perm, offs, (const T*)W2, b2, s.H, s.F, (T*)y_perm, err);
 }
 
 }  // namespace

@@ -77,6 +77,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
   const int nk = (K + kBK - 1) / kBK;
 
   if (warp == 0) {
+    pdl_enter();   // the tile table reads offs, written by the previous kernel
     // per-expert tile counts and their exclusive prefix (E <= 256: 8 per lane)
     int loc[8];
     int sum = 0;
@@ -130,6 +131,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (warp != 0) pdl_wait();
   const uint32_t tmem = s_tmem;
   const int total = s_tstart[E];
 
@@ -280,8 +282,8 @@ cudaError_t run_gemm(const void* A, int64_t rows, const int32_t* offs, int E, co
   auto k = grouped_gemm_tc_kernel<BN, kGelu>;
   cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem);
   if (r != cudaSuccess) return r;
-  k<<<sm_count(), kThreads, Cf::kSmem, st>>>(ma, mb, offs, E, N, K, bias, (bf16*)C, err);
-  return cudaGetLastError();
+  return launch_kernel(k, dim3(sm_count()), dim3(kThreads), Cf::kSmem, st, 1, ma, mb, offs, E, N, K, bias,
+                       (bf16*)C, err);
 }
 
 // 256-wide tiles unless 128-wide ones pad N less.

@@ -78,6 +78,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   constexpr uint32_t kIdesc = tc::idesc_bf16_f32(2 * kBM, 2 * kBNh);
 
   if (warp == 0) {
+    pdl_enter();   // the tile table reads offs, written by the previous kernel
     // per-expert pair-tile counts (256-row m-tiles x n-tiles) and their prefix
     int loc[8];
     int sum = 0;
@@ -132,6 +133,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   __syncthreads();
   tc::cluster_sync();             // both CTAs' barriers exist before either signals the other
   tc::tc_fence_after();
+  if (warp != 0) pdl_wait();
   const uint32_t tmem = s_tmem;
   const int total = s_tstart[E];
 
@@ -286,6 +288,8 @@ cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, co
   auto kern = grouped_gemm_pair_kernel<kGelu>;
   cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (r != cudaSuccess) return r;
+  // one resident pair per two SMs (persistent); never more pairs than fit at once
+  int pairs = sm_count() / 2;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -297,13 +301,11 @@ cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, co
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // one resident pair per two SMs (persistent); never more pairs than fit at once
-  int pairs = sm_count() / 2;
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   int fit = 0;
   if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < pairs) pairs = fit;
-  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, offs, E, N, K, bias, (bf16*)C, err);
+  return launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmem, st, 2, ma, mb, offs, E, N, K,
+                       bias, (bf16*)C, err);
 }
 
 }  // namespace

@@ -18,12 +18,40 @@ struct Shape {
   int H, E, K, F, C;   // C <= 0: no capacity limit
   int dtype;           // MOE_F32 | MOE_BF16
   uint32_t flags;
+  float inv_tau;       // 1 / router softmax temperature
   int64_t S() const { return T * (int64_t)K; }
   size_t esize() const { return dtype == MOE_BF16 ? 2 : 4; }
 };
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Launch with programmatic dependent launch allowed (the kernel waits for its
+// predecessor itself, see pdl_enter) and an optional cluster size.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 unsigned cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Stage-boundary events of moe_layer_forward (set by moe_profile_events; no-op
 // when unset).  Marks: 0 start, 1 router, 2 dispatch, 3 first product,

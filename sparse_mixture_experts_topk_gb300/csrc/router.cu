@@ -5,7 +5,9 @@
 // picks num_experts_per_tok experts, and the k probabilities are divided by
 // their sum.  Here the k experts are chosen on the fp32 scores themselves
 // (softmax is monotone), largest first, equal scores by ascending expert index,
-// and w_j = exp(l_j - m) / sum_sel exp(l_i - m), which equals p_j / sum_sel p.
+// and w_j = exp((l_j - m)/tau) / sum_sel exp((l_i - m)/tau), which equals
+// p_j / sum_sel p for p = softmax(l / tau) (tau = 1 unless the layer sets a
+// router temperature, MoE sparse-activation article, wmrh.cn, section 5.2).
 #include <float.h>
 
 #include "common.cuh"
@@ -38,7 +40,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <typename T>
 __global__ void __launch_bounds__(kRouterThreads)
 router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
-                   const float* __restrict__ gate_bias, int64_t Tn, int H, int E, int K,
+                   const float* __restrict__ gate_bias, int64_t Tn, int H, int E, int K, float inv_tau,
                    float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ w,
                    float* __restrict__ psum_part) {
   extern __shared__ float smem[];
@@ -48,6 +50,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t0 = (int64_t)blockIdx.x * kRouterTok;
   const int nt = (int)min((int64_t)kRouterTok, Tn - t0);
+  pdl_enter();
 
   float acc[32];
 #pragma unroll
@@ -105,7 +108,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) zs += expf(v[i] - m);
+      if (e < E) zs += expf((v[i] - m) * inv_tau);
     }
     zs = warp_sum(zs);
     unsigned taken = 0;
@@ -133,7 +136,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
         }
       }
       if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float z = expf(bv - m);
+      const float z = expf((bv - m) * inv_tau);
       sel_id[j] = bi;
       sel_z[j] = z;
       zsel += z;
@@ -150,7 +153,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) ls[tt * (E + 1) + e] = expf(v[i] - m) * inv;
+      if (e < E) ls[tt * (E + 1) + e] = expf((v[i] - m) * inv_tau) * inv;
     }
   }
   __syncthreads();
@@ -165,6 +168,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
 
 __global__ void psum_reduce_kernel(const float* __restrict__ part, int64_t rows, int E,
                                    float* __restrict__ psum) {
+  pdl_enter();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float s = 0.f;
     for (int64_t r = 0; r < rows; ++r) s += part[r * E + e];
@@ -192,23 +196,21 @@ cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const f
   if (s.dtype == MOE_BF16) {
     auto k = router_simt_kernel<bf16>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<(unsigned)grid, kRouterThreads, smem, st>>>((const bf16*)x, (const bf16*)Wg, gate_bias, s.T,
-                                                   s.H, s.E, s.K, logits, ids, w, psum_part);
-  } else {
-    auto k = router_simt_kernel<float>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<(unsigned)grid, kRouterThreads, smem, st>>>((const float*)x, (const float*)Wg, gate_bias,
-                                                   s.T, s.H, s.E, s.K, logits, ids, w, psum_part);
+    return launch_kernel(k, dim3((unsigned)grid), dim3(kRouterThreads), smem, st, 1, (const bf16*)x,
+                         (const bf16*)Wg, gate_bias, s.T, s.H, s.E, s.K, s.inv_tau, logits, ids, w, psum_part);
   }
-  return cudaGetLastError();
+  auto k = router_simt_kernel<float>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch_kernel(k, dim3((unsigned)grid), dim3(kRouterThreads), smem, st, 1, (const float*)x,
+                       (const float*)Wg, gate_bias, s.T, s.H, s.E, s.K, s.inv_tau, logits, ids, w, psum_part);
 }
 
 cudaError_t launch_psum_reduce(const Shape& s, const float* psum_part, float* psum, cudaStream_t st) {
   if (s.T == 0) {
     return cudaMemsetAsync(psum, 0, sizeof(float) * s.E, st);
   }
-  psum_reduce_kernel<<<1, 256, 0, st>>>(psum_part, router_partial_rows(s), s.E, psum);
-  return cudaGetLastError();
+  return launch_kernel(psum_reduce_kernel, dim3(1), dim3(256), 0, st, 1, (const float*)psum_part,
+                       router_partial_rows(s), s.E, psum);
 }
 
 }  // namespace moe

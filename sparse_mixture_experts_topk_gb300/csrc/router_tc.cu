@@ -4,8 +4,9 @@
 // jsqmd.com, section 3.1: bias-free gate linear, softmax, top-k, division of
 // the k probabilities by their sum): scores l = x Wg^T (+ bias) accumulated in
 // fp32; the k largest scores, largest first, equal scores by ascending expert
-// index; w_j = exp(l_j - m) / sum_sel exp(l_i - m); p = softmax(l) summed per
-// expert for the load-balancing loss.
+// index; w_j = exp((l_j - m)/tau) / sum_sel exp((l_i - m)/tau); p =
+// softmax(l / tau) summed per expert for the load-balancing loss (tau = 1
+// unless the layer sets a router temperature).
 //
 // The gate product is skinny (N = E <= 256) and its cost is reading x once,
 // so the kernel is built to stream x at HBM speed:
@@ -69,7 +70,7 @@ RouterCfg router_cfg(int E, int ctas_per_sm) {
 
 __global__ void __launch_bounds__(kThreads)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmG,
-                 int64_t Tn, int H, int E, int K, int npad, int tmem_cols, int ks, int kStages,
+                 int64_t Tn, int H, int E, int K, int npad, int tmem_cols, int ks, int kStages, float inv_tau,
                  const float* __restrict__ gate_bias, float* __restrict__ logits,
                  int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ psum_part,
                  int32_t* __restrict__ tile_hist, int* err) {
@@ -118,6 +119,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  pdl_enter();                     // first global access below
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
@@ -258,7 +260,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const float m = tv[0];
     float zs = 0.f;
     for (int e = 0; e < E; ++e) {
-      const float z = expf(lr[e] - m);
+      const float z = expf((lr[e] - m) * inv_tau);
       lr[e] = z;
       zs += z;
     }
@@ -267,7 +269,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     float zsel = 0.f, z[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      z[j] = j < K ? expf(tv[j] - m) : 0.f;
+      z[j] = j < K ? expf((tv[j] - m) * inv_tau) : 0.f;
       zsel += z[j];
     }
 #pragma unroll
@@ -315,20 +317,9 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, cons
   auto kern = router_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * ks), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = c.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)ks;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mx, mg, s.T, s.H, s.E, s.K, c.npad, c.tmem_cols, ks, c.stages,
-                            gate_bias, logits, ids, w, psum_part, tile_hist, err);
+  return launch_kernel(kern, dim3((unsigned)(tiles * ks)), dim3(kThreads), c.smem, st, (unsigned)ks, mx, mg, s.T,
+                       s.H, s.E, s.K, c.npad, c.tmem_cols, ks, c.stages, s.inv_tau, gate_bias, logits, ids, w, psum_part,
+                       tile_hist, err);
 }
 
 }  // namespace moe

@@ -43,6 +43,7 @@ class Workload:
     gate_bias: str = "none"       # "none" | "zipf"
     zipf_s: float = 1.2
     ffn_bias: bool = False
+    temperature: float = 1.0      # router softmax temperature
     seed: int = 0
 
     @property

@@ -47,7 +47,7 @@ def tdtype(w: W.Workload):
 
 def desc_of(w: W.Workload, flags: int = 0):
     return moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
-                         moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags)
+                         moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
 
 
 class Dev:

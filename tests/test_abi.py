@@ -61,10 +61,10 @@ def test_workspace_size_grows_with_shape(lib):
 
 @pytest.mark.parametrize("bad", [
     dict(K=0), dict(K=9), dict(E=1, K=2), dict(E=257), dict(H=12), dict(F=4), dict(T=-1),
-    dict(dtype=7), dict(T=1 << 30, K=4),
+    dict(dtype=7), dict(T=1 << 30, K=4), dict(temperature=float("nan")), dict(temperature=float("inf")),
 ])
 def test_bad_desc_rejected(lib, bad):
-    args = dict(T=64, H=256, E=8, K=2, F=512, capacity=0, dtype=moe.MOE_BF16, flags=0)
+    args = dict(T=64, H=256, E=8, K=2, F=512, capacity=0, dtype=moe.MOE_BF16, flags=0, temperature=1.0)
     args.update(bad)
     d = moe.make_desc(**args)
     n = ctypes.c_size_t(0)

@@ -37,6 +37,8 @@ SMALL = {
     "one_token": W.small("one_token", T=1, H=256, E=8, K=2, F=128),
     "k1": W.small("k1", T=96, H=128, E=4, K=1, F=64),
     "k_eq_e": W.small("k_eq_e", T=40, H=64, E=4, K=4, F=64),
+    "hot_router": W.small("hot_router", T=260, H=256, E=16, K=2, F=128, temperature=2.0),
+    "cold_router_f32": W.small("cold_router_f32", T=90, H=64, E=8, K=3, F=64, dtype=W.F32, temperature=0.5),
 }
 
 
@@ -59,7 +61,7 @@ def _check_routing(w, inp, r, x64, Wg64):
     gl = to_np(r["logits"]).astype(np.float64)
     ref_l = O.gate_logits(x64, Wg64, inp.gate_bias)
     assert logits_rel_err(gl, ref_l) <= LOGITS_REL
-    ids_o, w_o, p_o = O.route(gl, w.K)
+    ids_o, w_o, p_o = O.route(gl, w.K, w.temperature)
     np.testing.assert_array_equal(to_np(r["ids"]), ids_o)
     np.testing.assert_allclose(to_np(r["w"]), w_o, rtol=0, atol=W_ABS)
     ps = p_o.sum(axis=0)
@@ -134,7 +136,7 @@ def test_stages_and_layer_small(name):
     ref = O.layer_forward(x64, Wg64, W164, W264, w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
                           b1=None if inp.b1 is None else inp.b1.astype(np.float64),
                           b2=None if inp.b2 is None else inp.b2.astype(np.float64),
-                          bf16=bf, logits=gl)
+                          bf16=bf, logits=gl, temperature=w.temperature)
     mx, rel = out_errors(out_gpu, ref["out"])
     if bf:
         assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)

@@ -369,3 +369,78 @@ def test_activation_rate_arithmetic():
     assert per * g["layers"] * g["experts"] == g["total"]
     assert per * g["layers"] * g["active"] == g["active_params"]
     assert 100.0 * g["active"] / g["experts"] == g["rate_percent"]
+
+
+def test_softmax_temperature_closed_forms():
+    # tau scales the scores: softmax([0, ln 2, ln 3] at tau=0.5) = [1, 4, 9] / 14
+    p = O.softmax(np.array([[0.0, math.log(2.0), math.log(3.0)]]), temperature=0.5)
+    np.testing.assert_allclose(p[0], [1 / 14, 4 / 14, 9 / 14], rtol=0, atol=1e-15)
+    p = O.softmax(np.array([[0.0, math.log(4.0)]]), temperature=2.0)       # -> [1, 2] / 3
+    np.testing.assert_allclose(p[0], [1 / 3, 2 / 3], rtol=0, atol=1e-15)
+    rng = np.random.default_rng(12)
+    l = rng.standard_normal((20, 8)) * 3
+    np.testing.assert_array_equal(O.softmax(l, 1.0), O.softmax(l))
+
+
+def test_route_temperature_keeps_experts_changes_weights():
+    rng = np.random.default_rng(13)
+    l = rng.standard_normal((40, 8)) * 2
+    ids1, w1, _ = O.route(l, 3)
+    for tau in (0.5, 2.0, 1e6):
+        ids, w, p = O.route(l, 3, temperature=tau)
+        np.testing.assert_array_equal(ids, ids1)                 # order of scores unchanged
+        sel = np.take_along_axis(l, ids, 1) / tau
+        np.testing.assert_allclose(w, O.softmax(sel), rtol=1e-13)
+        np.testing.assert_allclose(w.sum(1), 1.0, atol=1e-15)
+    _, w_flat, _ = O.route(l, 3, temperature=1e6)                # very hot: uniform weights
+    np.testing.assert_allclose(w_flat, 1 / 3, atol=1e-5)
+    _, w_cold, _ = O.route(l, 3, temperature=1e-3)               # very cold: all on the top score
+    srt = np.sort(l, axis=1)
+    clear = srt[:, -1] - srt[:, -2] > 0.05                       # rows without a near-tie at the top
+    assert clear.sum() > 30
+    np.testing.assert_allclose(w_cold[clear, 0], 1.0, atol=1e-6)
+
+
+def test_silu_closed_forms():
+    # sigmoid(ln 3) = 3/4, sigmoid(0) = 1/2; silu(a) - silu(-a) = a
+    assert abs(O.silu(np.array([math.log(3.0)]))[0] - 0.75 * math.log(3.0)) < 1e-15
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    a = np.linspace(-8, 8, 81)
+    np.testing.assert_allclose(O.silu(a) - O.silu(-a), a, atol=1e-14)
+    assert O.silu(np.array([50.0]))[0] == 50.0 and abs(O.silu(np.array([-50.0]))[0]) < 1e-19
+
+
+def test_swiglu_expert_exact_integer_relu_regime():
+    """With |W1 x| >= 50 SiLU equals ReLU to double precision, so the SwiGLU
+    expert W2 (relu(W1 x) * (W3 x)) has an exact integer answer."""
+    rng = np.random.default_rng(14)
+    n, H, F = 3, 5, 6
+    for _ in range(20):
+        x = rng.integers(-3, 4, size=(n, H)).astype(np.float64)
+        Wgt = rng.integers(-3, 4, size=(F, H)).astype(np.float64) * 50.0
+        Wup = rng.integers(-3, 4, size=(F, H)).astype(np.float64)
+        W2 = rng.integers(-3, 4, size=(H, F)).astype(np.float64)
+        y = O.expert_ffn(x, np.concatenate([Wgt, Wup]), W2, act="swiglu")
+        for i in range(n):
+            for hh in range(H):
+                want = 0
+                for f in range(F):
+                    g = sum(int(Wgt[f, c]) * int(x[i, c]) for c in range(H))
+                    u = sum(int(Wup[f, c]) * int(x[i, c]) for c in range(H))
+                    want += int(W2[hh, f]) * max(g, 0) * u
+                assert abs(y[i, hh] - want) < 1e-9
+
+
+def test_swiglu_gate_and_up_roles():
+    """Unit up-projection leaves SiLU of the gate; unit gate at +inf leaves the up."""
+    rng = np.random.default_rng(15)
+    H = 8
+    x = rng.standard_normal((4, H))
+    Wgt = rng.standard_normal((H, H))
+    y = O.expert_ffn(x, np.concatenate([Wgt, np.zeros((H, H))]), np.eye(H), b1e=np.r_[np.zeros(H), np.ones(H)],
+                     act="swiglu")
+    np.testing.assert_allclose(y, O.silu(x @ Wgt.T), rtol=1e-14)
+    Wup = rng.standard_normal((H, H))
+    y = O.expert_ffn(x, np.concatenate([np.zeros((H, H)), Wup]), np.eye(H), b1e=np.r_[np.full(H, 60.0), np.zeros(H)],
+                     act="swiglu")
+    np.testing.assert_allclose(y, 60.0 * (x @ Wup.T), rtol=1e-13)
