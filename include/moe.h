@@ -62,6 +62,7 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 #define MOE_FLAG_SIMT_ROUTER (1u << 3) /* bf16: CUDA-core router instead of tensor cores (testing) */
 #define MOE_FLAG_GEMM_SINGLE (1u << 4) /* bf16: 128x256 single-SM expert GEMM tiles */
 #define MOE_FLAG_GEMM_PAIR   (1u << 5) /* bf16: 256x256 tiles on SM pairs (cta_group::2) */
+#define MOE_FLAG_SWIGLU      (1u << 6) /* experts are W2 (SiLU(W1 x) * W3 x); see moe_expert_ffn */
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the
@@ -180,6 +181,11 @@ int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, const void* x
  *   x_perm [rows, H] dtype in; offs [E+1] int32 in (device; read on device only)
  *   W1 [E, F, H] dtype; W2 [E, H, F] dtype (nn.Linear [out, in] layout)
  *   b1 [E, F] fp32 or NULL; b2 [E, H] fp32 or NULL
+ * With MOE_FLAG_SWIGLU the experts have three matrices W1, W2, W3 (the
+ * Qwen2-MoE walkthrough, jsqmd.com, section 4.6), read as
+ *   h_perm[r] = SiLU(W1[e] x + b1[e][:F]) * (W3[e] x + b1[e][F:])
+ * and the W1 argument holds W1 and W3 stacked per expert: [E, 2F, H] (rows
+ * 0..F-1 = W1, rows F..2F-1 = W3); b1 is then [E, 2F].
  *   h_perm [moe_max_rows, F] dtype out (intermediate, kept for inspection)
  *   y_perm [moe_max_rows, H] dtype out
  * bf16 with K-major operands runs on the tcgen05 tensor cores, either as

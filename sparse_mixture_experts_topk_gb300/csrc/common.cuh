@@ -55,6 +55,12 @@ template <> struct Vec<float> {
   }
 };
 
+// Expert epilogues: first product GELU or SwiGLU, second product plain.
+enum Epi : int { kEpiGelu = 0, kEpiPlain = 1, kEpiSwiglu = 2 };
+
+// SiLU: a * sigmoid(a) = a / (1 + exp(-a)).
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
 // GELU, erf form: 0.5 a (1 + erf(a / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float a) {
   return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));

@@ -34,15 +34,19 @@ __device__ __forceinline__ bool find_tile(const int32_t* __restrict__ offs, int 
   return false;
 }
 
-// C[r, n] = epi(sum_k A[r, k] B_e[n, k]) for one 64x64 tile.
-template <typename T, bool kGelu>
+// C[r, n] = epi(sum_k A[r, k] B_e[n, k]) for one 64x64 tile.  With
+// kEpi = kEpiSwiglu, B_e = [W1; W3] ([2N, K]) and C[r, n] =
+// SiLU(sum_k A W1[n, k] + b1[n]) * (sum_k A W3[n, k] + b1[N + n]).
+template <typename T, int kEpi>
 __global__ void __launch_bounds__(kGemmThreads)
 grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int E,
                          const T* __restrict__ B, const float* __restrict__ bias, int N, int K,
                          T* __restrict__ C) {
   __shared__ int s_e, s_r0, s_r1;
   __shared__ float As[kBK][kBM + 4];
+  constexpr bool kSwi = kEpi == kEpiSwiglu;
   __shared__ float Bs[kBK][kBN + 4];
+  __shared__ float Us[kBK][kBN + 4];      // up-projection tile (SwiGLU only)
   pdl_enter();
   if (threadIdx.x == 0) {
     int e, r0, r1;
@@ -54,9 +58,10 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
   if (e < 0) return;
   const int r0 = s_r0, r1 = s_r1;
   const int n0 = blockIdx.x * kBN;
-  const T* Be = B + (int64_t)e * N * K;
+  const T* Be = B + (int64_t)e * N * K * (kSwi ? 2 : 1);
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   float acc[4][4] = {};
+  float accu[4][4] = {};
   for (int k0 = 0; k0 < K; k0 += kBK) {
     {
       const int i = threadIdx.x;            // 256 threads x 4 elements
@@ -68,6 +73,7 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
         As[kq + j][row] = (r < r1 && k < K) ? to_f32(A[(int64_t)r * K + k]) : 0.f;
         const int n = n0 + row;
         Bs[kq + j][row] = (n < N && k < K) ? to_f32(Be[(int64_t)n * K + k]) : 0.f;
+        if (kSwi) Us[kq + j][row] = (n < N && k < K) ? to_f32(Be[(int64_t)(N + n) * K + k]) : 0.f;
       }
     }
     __syncthreads();
@@ -80,6 +86,12 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      if (kSwi) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) accu[i][j] = fmaf(a[i], Us[kk][tx * 4 + j], accu[i][j]);
+      }
     }
     __syncthreads();
   }
@@ -91,8 +103,12 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
       if (n >= N) continue;
-      float v = acc[i][j] + (bias ? bias[(int64_t)e * N + n] : 0.f);
-      if (kGelu) v = gelu_erf(v);
+      float v = acc[i][j] + (bias ? bias[(int64_t)e * N * (kSwi ? 2 : 1) + n] : 0.f);
+      if (kEpi == kEpiGelu) v = gelu_erf(v);
+      if (kSwi) {
+        const float u = accu[i][j] + (bias ? bias[(int64_t)e * N * 2 + N + n] : 0.f);
+        v = silu_f(v) * u;
+      }
       C[(int64_t)r * N + n] = from_f32<T>(v);
     }
   }
@@ -104,7 +120,9 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
 constexpr int kMaxRows = 16;
 constexpr int kStreamWarps = 8, kStreamRowsPerWarp = 4;
 
-template <typename T, bool kGelu>
+// With kEpi = kEpiSwiglu, B_e = [W1; W3] ([2N, K]) and output column n dots
+// the activation rows with gate row n and up row N + n.
+template <typename T, int kEpi>
 __global__ void __launch_bounds__(kStreamWarps * 32)
 stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs,
                   const T* __restrict__ B, const float* __restrict__ bias, int N, int K,
@@ -122,36 +140,47 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs,
   const int kv = K / V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint4* Av = reinterpret_cast<const uint4*>(A + (int64_t)r0 * K);
-  const T* Be = B + (int64_t)e * N * K;
+  constexpr bool kSwi = kEpi == kEpiSwiglu;
+  const T* Be = B + (int64_t)e * N * K * (kSwi ? 2 : 1);
   for (int q = 0; q < kStreamRowsPerWarp; ++q) {
     const int n = (blockIdx.x * kStreamWarps + warp) * kStreamRowsPerWarp + q;
     if (n >= N) break;
     const uint4* Bv = reinterpret_cast<const uint4*>(Be + (int64_t)n * K);
-    float acc[kMaxRows];
+    const uint4* Uv = reinterpret_cast<const uint4*>(Be + (int64_t)(N + n) * K);   // SwiGLU up row
+    float acc[kMaxRows], accu[kMaxRows];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+    for (int r = 0; r < kMaxRows; ++r) acc[r] = accu[r] = 0.f;
     for (int v = lane; v < kv; v += 32) {
-      float bw[V];
+      float bw[V], uw[V];
       Vec<T>::unpack(__ldcs(Bv + v), bw);
+      if (kSwi) Vec<T>::unpack(__ldcs(Uv + v), uw);
 #pragma unroll
       for (int r = 0; r < kMaxRows; ++r) {
         if (r < m) {
           float a[V];
           Vec<T>::unpack(__ldg(Av + (int64_t)r * kv + v), a);
 #pragma unroll
-          for (int i = 0; i < V; ++i) acc[r] = fmaf(a[i], bw[i], acc[r]);
+          for (int i = 0; i < V; ++i) {
+            acc[r] = fmaf(a[i], bw[i], acc[r]);
+            if (kSwi) accu[r] = fmaf(a[i], uw[i], accu[r]);
+          }
         }
       }
     }
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       if (r < m) {
-        float s = acc[r];
+        float s = acc[r], su = accu[r];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        for (int o = 16; o > 0; o >>= 1) {
+          s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (kSwi) su += __shfl_xor_sync(0xffffffffu, su, o);
+        }
         if (lane == 0) {
-          float v = s + (bias ? bias[(int64_t)e * N + n] : 0.f);
-          if (kGelu) v = gelu_erf(v);
+          const int64_t bstride = (int64_t)N * (kSwi ? 2 : 1);
+          float v = s + (bias ? bias[e * bstride + n] : 0.f);
+          if (kEpi == kEpiGelu) v = gelu_erf(v);
+          if (kSwi) v = silu_f(v) * (su + (bias ? bias[e * bstride + N + n] : 0.f));
           C[(int64_t)(r0 + r) * N + n] = from_f32<T>(v);
         }
       }
@@ -166,12 +195,14 @@ cudaError_t run_simt(const Shape& s, int64_t max_rows, const void* x_perm, const
   const int64_t mtiles = (max_rows + kBM - 1) / kBM + s.E;
   if (mtiles > 65535) return cudaErrorInvalidConfiguration;
   dim3 g1((s.F + kBN - 1) / kBN, (unsigned)mtiles);
-  cudaError_t e = launch_kernel(grouped_gemm_simt_kernel<T, true>, g1, dim3(kGemmThreads), 0, st, 1,
+  auto k1 = (s.flags & MOE_FLAG_SWIGLU) ? grouped_gemm_simt_kernel<T, kEpiSwiglu>
+                                        : grouped_gemm_simt_kernel<T, kEpiGelu>;
+  cudaError_t e = launch_kernel(k1, g1, dim3(kGemmThreads), 0, st, 1,
                                 (const T*)x_perm, offs, s.E, (const T*)W1, b1, s.F, s.H, (T*)h_perm);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
   dim3 g2((s.H + kBN - 1) / kBN, (unsigned)mtiles);
-  return launch_kernel(grouped_gemm_simt_kernel<T, false>, g2, dim3(kGemmThreads), 0, st, 1,
+  return launch_kernel(grouped_gemm_simt_kernel<T, kEpiPlain>, g2, dim3(kGemmThreads), 0, st, 1,
                        (const T*)h_perm, offs, s.E, (const T*)W2, b2, s.H, s.F, (T*)y_perm);
 }
 
@@ -181,12 +212,13 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
                        int* err, cudaStream_t st) {
   const int per_block = kStreamWarps * kStreamRowsPerWarp;
   dim3 g1((s.F + per_block - 1) / per_block, s.E);
-  cudaError_t e = launch_kernel(stream_ffn_kernel<T, true>, g1, dim3(kStreamWarps * 32), 0, st, 1,
+  auto k1 = (s.flags & MOE_FLAG_SWIGLU) ? stream_ffn_kernel<T, kEpiSwiglu> : stream_ffn_kernel<T, kEpiGelu>;
+  cudaError_t e = launch_kernel(k1, g1, dim3(kStreamWarps * 32), 0, st, 1,
                                 (const T*)x_perm, offs, (const T*)W1, b1, s.F, s.H, (T*)h_perm, err);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
   dim3 g2((s.H + per_block - 1) / per_block, s.E);
-  return launch_kernel(stream_ffn_kernel<T, false>, g2, dim3(kStreamWarps * 32), 0, st, 1,
+  return launch_kernel(stream_ffn_kernel<T, kEpiPlain>, g2, dim3(kStreamWarps * 32), 0, st, 1,
                        (const T*)h_perm, offs, (const T*)W2, b2, s.H, s.F, (T*)y_perm, err);
 }
 

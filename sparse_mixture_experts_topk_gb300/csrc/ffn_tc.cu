@@ -49,7 +49,10 @@ struct Cfg {
   static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, BN);
 };
 
-template <int BN, bool kGelu>
+// kEpi = kEpiSwiglu: B = [W1; W3] stacked per expert ([E, 2N, K]); a 256-wide
+// accumulator tile holds 128 gate columns then the matching 128 up columns,
+// and the tile writes SiLU(gate) * up for those 128 output columns.
+template <int BN, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const int32_t* __restrict__ offs, int E, int N, int K,
@@ -73,7 +76,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
   const uint32_t done_bar = tc::smem_u32(&s_bar[2 * S + 4]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = (N + BN - 1) / BN;
+  constexpr bool kSwi = kEpi == kEpiSwiglu;
+  static_assert(!kSwi || BN == 256, "SwiGLU tiles pair 128 gate with 128 up columns");
+  constexpr int kOut = kSwi ? BN / 2 : BN;     // output columns per tile
+  const int nt = (N + kOut - 1) / kOut;
   const int nk = (K + kBK - 1) / kBK;
 
   if (warp == 0) {
@@ -146,7 +152,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     const int local = t - s_tstart[e];
     row0 = s_offs[e] + (local % mt) * kBM;
     row_end = s_offs[e + 1];
-    n0 = (local / mt) * BN;
+    n0 = (local / mt) * kOut;
   };
 
   if (warp == 0) {
@@ -163,7 +169,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
           if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(full(stage), Cf::kStageBytes);
           tc::tma_load_2d(sA + stage * Cf::kABytes, &tmA, full(stage), kb * kBK, row0);
-          tc::tma_load_2d(sB + stage * Cf::kBBytes, &tmB, full(stage), kb * kBK, e * N + n0);
+          if (kSwi) {
+            tc::tma_load_2d(sB + stage * Cf::kBBytes, &tmB, full(stage), kb * kBK, 2 * e * N + n0);
+            tc::tma_load_2d(sB + stage * Cf::kBBytes + Cf::kBBytes / 2, &tmB, full(stage), kb * kBK,
+                            2 * e * N + N + n0);
+          } else {
+            tc::tma_load_2d(sB + stage * Cf::kBBytes, &tmB, full(stage), kb * kBK, e * N + n0);
+          }
           filled |= 1u << stage;
           fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -232,13 +244,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
       const int row = row0 + q * 32 + lane;
       const bool row_ok = row < row_end;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      const float* be = bias ? bias + (int64_t)e * N : nullptr;
+      const float* be = bias ? bias + (int64_t)e * (kSwi ? 2 * N : N) : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < kOut / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= N) break;
-        uint32_t r[32];
+        uint32_t r[32], u[kSwi ? 32 : 1];
         tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+        if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
         tc::tmem_wait_ld();
         if (row_ok) {
           bf16* dst = C + (int64_t)row * N + col0;
@@ -250,7 +263,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
               for (int j = 0; j < 8; ++j) {
                 float a = __uint_as_float(r[g * 8 + j]);
                 if (be) a += be[col0 + g * 8 + j];
-                v[j] = kGelu ? gelu_erf(a) : a;
+                if (kEpi == kEpiGelu) {
+                  v[j] = gelu_erf(a);
+                } else if (kSwi) {
+                  float b = __uint_as_float(u[(g * 8 + j) % (kSwi ? 32 : 1)]);
+                  if (be) b += be[N + col0 + g * 8 + j];
+                  v[j] = silu_f(a) * b;
+                } else {
+                  v[j] = a;
+                }
               }
               *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
             }
@@ -272,14 +293,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
   }
 }
 
-template <int BN, bool kGelu>
+template <int BN, int kEpi>
 cudaError_t run_gemm(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
                      const float* bias, void* C, int* err, cudaStream_t st) {
   using Cf = Cfg<BN>;
   CUtensorMap ma, mb;
   if (!tma_map_bf16(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
-  if (!tma_map_bf16(&mb, B, (uint64_t)E * N, (uint64_t)K, BN)) return cudaErrorNotSupported;
-  auto k = grouped_gemm_tc_kernel<BN, kGelu>;
+  constexpr bool kSwi = kEpi == kEpiSwiglu;
+  if (!tma_map_bf16(&mb, B, (uint64_t)E * N * (kSwi ? 2 : 1), (uint64_t)K, kSwi ? BN / 2 : BN))
+    return cudaErrorNotSupported;
+  auto k = grouped_gemm_tc_kernel<BN, kEpi>;
   cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem);
   if (r != cudaSuccess) return r;
   return launch_kernel(k, dim3(sm_count()), dim3(kThreads), Cf::kSmem, st, 1, ma, mb, offs, E, N, K, bias,
@@ -293,11 +316,11 @@ bool wide_tile(int N) {
   return p256 <= p128;
 }
 
-template <bool kGelu>
+template <int kEpi>
 cudaError_t run_product(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
                         const float* bias, void* C, int* err, cudaStream_t st) {
-  if (wide_tile(N)) return run_gemm<256, kGelu>(A, rows, offs, E, B, N, K, bias, C, err, st);
-  return run_gemm<128, kGelu>(A, rows, offs, E, B, N, K, bias, C, err, st);
+  if (kEpi == kEpiSwiglu || wide_tile(N)) return run_gemm<256, kEpi>(A, rows, offs, E, B, N, K, bias, C, err, st);
+  return run_gemm<128, kEpi == kEpiSwiglu ? kEpiPlain : kEpi>(A, rows, offs, E, B, N, K, bias, C, err, st);
 }
 
 }  // namespace
@@ -308,10 +331,12 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
     return cudaErrorNotSupported;
-  cudaError_t r = run_product<true>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
+  cudaError_t r = (s.flags & MOE_FLAG_SWIGLU)
+                      ? run_product<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st)
+                      : run_product<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
-  return run_product<false>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);
+  return run_product<kEpiPlain>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);
 }
 
 }  // namespace moe

@@ -48,7 +48,10 @@ constexpr int kTmemCols = 512;       // two 256-column accumulators
 constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-template <bool kGelu>
+// kEpi = kEpiSwiglu: B = [W1; W3] stacked per expert ([E, 2N, K]); the
+// leader loads 128 gate rows and the peer the matching 128 up rows, so each
+// CTA's 256 accumulator columns are gate | up for 128 output columns.
+template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const int32_t* __restrict__ offs, int E, int N, int K,
@@ -73,7 +76,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_ctarank();          // 0 = leader
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int nt = (N + 2 * kBNh - 1) / (2 * kBNh);
+  constexpr bool kSwi = kEpi == kEpiSwiglu;
+  constexpr int kOut = kSwi ? kBNh : 2 * kBNh;   // output columns per pair tile
+  const int nt = (N + kOut - 1) / kOut;
   const int nk = (K + kBK - 1) / kBK;
   constexpr uint32_t kIdesc = tc::idesc_bf16_f32(2 * kBM, 2 * kBNh);
 
@@ -148,7 +153,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const int local = t - s_tstart[e];
     row0 = s_offs[e] + (local % mt) * (2 * kBM) + (int)rank * kBM;   // this CTA's half
     row_end = s_offs[e + 1];
-    n0 = (local / mt) * (2 * kBNh);
+    n0 = (local / mt) * kOut;
   };
 
   if (warp == 0) {
@@ -166,7 +171,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           const uint32_t fbar = tc::map_peer(full(stage), 0);
           if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
           tc::tma_load_2d_pair(sA + stage * kABytes, &tmA, fbar, kb * kBK, row0);
-          tc::tma_load_2d_pair(sB + stage * kBBytes, &tmB, fbar, kb * kBK, e * N + n0 + (int)rank * kBNh);
+          tc::tma_load_2d_pair(sB + stage * kBBytes, &tmB, fbar, kb * kBK,
+                               kSwi ? 2 * e * N + (int)rank * N + n0 : e * N + n0 + (int)rank * kBNh);
           filled |= 1u << stage;
           fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -237,13 +243,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       const int row = row0 + q * 32 + lane;
       const bool row_ok = row < row_end;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kBNh);
-      const float* be = bias ? bias + (int64_t)e * N : nullptr;
+      const float* be = bias ? bias + (int64_t)e * (kSwi ? 2 * N : N) : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < 2 * kBNh / 32; ++c) {
+      for (int c = 0; c < kOut / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= N) break;
-        uint32_t r[32];
+        uint32_t r[32], u[kSwi ? 32 : 1];
         tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+        if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
         tc::tmem_wait_ld();
         if (row_ok) {
           bf16* dst = C + (int64_t)row * N + col0;
@@ -255,7 +262,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
               for (int j = 0; j < 8; ++j) {
                 float a = __uint_as_float(r[g * 8 + j]);
                 if (be) a += be[col0 + g * 8 + j];
-                v[j] = kGelu ? gelu_erf(a) : a;
+                if (kEpi == kEpiGelu) {
+                  v[j] = gelu_erf(a);
+                } else if (kSwi) {
+                  float b = __uint_as_float(u[(g * 8 + j) % (kSwi ? 32 : 1)]);
+                  if (be) b += be[N + col0 + g * 8 + j];
+                  v[j] = silu_f(a) * b;
+                } else {
+                  v[j] = a;
+                }
               }
               *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
             }
@@ -279,13 +294,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   }
 }
 
-template <bool kGelu>
+template <int kEpi>
 cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
                      const float* bias, void* C, int* err, cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!tma_map_bf16(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
-  if (!tma_map_bf16(&mb, B, (uint64_t)E * N, (uint64_t)K, kBNh)) return cudaErrorNotSupported;
-  auto kern = grouped_gemm_pair_kernel<kGelu>;
+  if (!tma_map_bf16(&mb, B, (uint64_t)E * N * (kEpi == kEpiSwiglu ? 2 : 1), (uint64_t)K, kBNh))
+    return cudaErrorNotSupported;
+  auto kern = grouped_gemm_pair_kernel<kEpi>;
   cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (r != cudaSuccess) return r;
   // one resident pair per two SMs (persistent); never more pairs than fit at once
@@ -316,10 +332,12 @@ cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_p
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
     return cudaErrorNotSupported;
-  cudaError_t r = run_pair<true>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
+  cudaError_t r = (s.flags & MOE_FLAG_SWIGLU)
+                      ? run_pair<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st)
+                      : run_pair<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
-  return run_pair<false>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);
+  return run_pair<kEpiPlain>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);
 }
 
 }  // namespace moe

@@ -44,6 +44,7 @@ class Workload:
     zipf_s: float = 1.2
     ffn_bias: bool = False
     temperature: float = 1.0      # router softmax temperature
+    act: str = "gelu"             # "gelu" (Linear-GELU-Linear) | "swiglu" (W2 (SiLU(W1 x) * W3 x))
     seed: int = 0
 
     @property
@@ -70,6 +71,8 @@ WORKLOADS = {
                          capacity=capacity_ceil(16384, 32, 4), gate_bias="zipf"),
     # long prefill with wide hidden and many narrow experts
     "wide": Workload("wide", T=32768, H=4096, E=64, K=2, F=1408),
+    # the prefill layer with SwiGLU experts (W1, W2, W3)
+    "prefill_swiglu": Workload("prefill_swiglu", T=8192, H=3584, E=32, K=2, F=2560, act="swiglu"),
     # profiler-sized case: prefill layer dims with 8 experts (weights 294 MB > L2)
     "ncu_medium": Workload("ncu_medium", T=4096, H=3584, E=8, K=2, F=2560),
 }
@@ -106,9 +109,11 @@ def gen_gate(w: Workload) -> np.ndarray:
 
 
 def gen_w1(w: Workload, e: int) -> np.ndarray:
-    """Expert e's first linear, ``[F, H]``."""
+    """Expert e's first linear, ``[F, H]``; for SwiGLU experts W1 and W3
+    stacked, ``[2F, H]`` (each an ``[F, H]`` Xavier-uniform linear)."""
     b = xavier_bound(w.H, w.F)
-    return _pack(_rng(w.seed, _S_W1, e).uniform(-b, b, size=(w.F, w.H)).astype(np.float32), w.dtype)
+    rows = 2 * w.F if w.act == "swiglu" else w.F
+    return _pack(_rng(w.seed, _S_W1, e).uniform(-b, b, size=(rows, w.H)).astype(np.float32), w.dtype)
 
 
 def gen_w2(w: Workload, e: int) -> np.ndarray:
@@ -134,7 +139,7 @@ def gen_gate_bias(w: Workload):
 def gen_ffn_bias(w: Workload):
     if not w.ffn_bias:
         return None, None
-    b1 = _rng(w.seed, _S_B1).uniform(-0.1, 0.1, size=(w.E, w.F)).astype(np.float32)
+    b1 = _rng(w.seed, _S_B1).uniform(-0.1, 0.1, size=(w.E, 2 * w.F if w.act == "swiglu" else w.F)).astype(np.float32)
     b2 = _rng(w.seed, _S_B2).uniform(-0.1, 0.1, size=(w.E, w.H)).astype(np.float32)
     return b1, b2
 
@@ -181,7 +186,7 @@ def generate(w: Workload) -> LayerInputs:
     Wg = gen_gate(w)
     x = gen_x(w, Wg)
     store = np.uint16 if w.dtype == BF16 else np.float32
-    W1 = np.empty((w.E, w.F, w.H), dtype=store)
+    W1 = np.empty((w.E, 2 * w.F if w.act == "swiglu" else w.F, w.H), dtype=store)
     W2 = np.empty((w.E, w.H, w.F), dtype=store)
     for e in range(w.E):
         W1[e] = gen_w1(w, e)

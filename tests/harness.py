@@ -46,6 +46,8 @@ def tdtype(w: W.Workload):
 
 
 def desc_of(w: W.Workload, flags: int = 0):
+    if w.act == "swiglu":
+        flags |= moe.MOE_FLAG_SWIGLU
     return moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                          moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
 

@@ -61,7 +61,7 @@ def oracle_rows(inp, ids, w_o, pos, tokens):
         W1e = O.widen(inp.W1[e], w.dtype)
         W2e = O.widen(inp.W2[e], w.dtype)
         xs = np.stack([O.widen(inp.x[slots[i][0]], w.dtype) for i in rows])
-        y[rows] = O.expert_ffn(xs, W1e, W2e, bf16=(w.dtype == W.BF16))
+        y[rows] = O.expert_ffn(xs, W1e, W2e, bf16=(w.dtype == W.BF16), act=w.act)
     mini_pos = np.full(len(tokens) * K, -1, dtype=np.int64)
     index = {s: i for i, s in enumerate(slots)}
     for a, t in enumerate(tokens):
@@ -71,7 +71,7 @@ def oracle_rows(inp, ids, w_o, pos, tokens):
     return O.combine(y, mini_pos, w_o[tokens])
 
 
-@pytest.mark.parametrize("name", ["decode1", "decode8", "prefill", "zipf_cap", "wide"])
+@pytest.mark.parametrize("name", ["decode1", "decode8", "prefill", "zipf_cap", "wide", "prefill_swiglu"])
 def test_full_size(name):
     w = W.WORKLOADS[name]
     inp = W.generate(w)

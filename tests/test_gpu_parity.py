@@ -39,6 +39,12 @@ SMALL = {
     "k_eq_e": W.small("k_eq_e", T=40, H=64, E=4, K=4, F=64),
     "hot_router": W.small("hot_router", T=260, H=256, E=16, K=2, F=128, temperature=2.0),
     "cold_router_f32": W.small("cold_router_f32", T=90, H=64, E=8, K=3, F=64, dtype=W.F32, temperature=0.5),
+    "swiglu_ragged": W.small("swiglu_ragged", T=333, H=512, E=8, K=2, F=384, act="swiglu", ffn_bias=True),
+    "swiglu_f32": W.small("swiglu_f32", T=120, H=96, E=6, K=2, F=136, dtype=W.F32, act="swiglu"),
+    # decode-sized batch (weight-streaming kernel) with x ~ N(0,1): the
+    # distinct-expert construction scales x by 64, and SiLU(g) * u would square
+    # that into outputs whose bf16 storage alone exceeds the 2e-2 bound
+    "swiglu_decode": W.small("swiglu_decode", T=4, H=512, E=16, K=2, F=200, act="swiglu"),
 }
 
 
@@ -107,7 +113,7 @@ def test_stages_and_layer_small(name):
         b1 = None if inp.b1 is None else inp.b1[e].astype(np.float64)
         b2 = None if inp.b2 is None else inp.b2[e].astype(np.float64)
         pre = xp[a:b] @ W164[e].T + (0 if b1 is None else b1)
-        h_ref = O.gelu(pre)
+        h_ref = O.silu(pre[:, :w.F]) * pre[:, w.F:] if w.act == "swiglu" else O.gelu(pre)
         y_ref = h_gpu[a:b] @ W264[e].T + (0 if b2 is None else b2)
         if bf:
             h_ref, y_ref = O.round_bf16(h_ref), O.round_bf16(y_ref)
@@ -136,7 +142,7 @@ def test_stages_and_layer_small(name):
     ref = O.layer_forward(x64, Wg64, W164, W264, w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
                           b1=None if inp.b1 is None else inp.b1.astype(np.float64),
                           b2=None if inp.b2 is None else inp.b2.astype(np.float64),
-                          bf16=bf, logits=gl, temperature=w.temperature)
+                          bf16=bf, logits=gl, temperature=w.temperature, act=w.act)
     mx, rel = out_errors(out_gpu, ref["out"])
     if bf:
         assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
@@ -234,7 +240,8 @@ def test_heavily_tied_scores_route_like_the_oracle():
 
 
 @pytest.mark.parametrize("kind", ["single", "pair"])
-@pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "ffn_bias", "cap_zipf_k4", "e256_k3", "one_token"])
+@pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "ffn_bias", "cap_zipf_k4", "e256_k3", "one_token",
+                                  "swiglu_ragged"])
 def test_expert_gemm_kernels_match_oracle(name, kind):
     """Both tensor-core GEMM kernels (128x256 tiles per SM, 256x256 tiles per
     SM pair) against the oracle, product by product, and the layer output."""
@@ -257,7 +264,8 @@ def test_expert_gemm_kernels_match_oracle(name, kind):
             continue
         b1 = 0 if inp.b1 is None else inp.b1[e].astype(np.float64)
         b2 = 0 if inp.b2 is None else inp.b2[e].astype(np.float64)
-        h_ref = O.round_bf16(O.gelu(xp[a:b] @ W164[e].T + b1))
+        pre = xp[a:b] @ W164[e].T + b1
+        h_ref = O.round_bf16(O.silu(pre[:, :w.F]) * pre[:, w.F:] if w.act == "swiglu" else O.gelu(pre))
         y_ref = O.round_bf16(h_gpu[a:b] @ W264[e].T + b2)
         assert (np.abs(h_gpu[a:b] - h_ref) <= _ulp_tol(h_ref)).all(), (name, kind, e)
         assert (np.abs(y_gpu[a:b] - y_ref) <= _ulp_tol(y_ref)).all(), (name, kind, e)
@@ -267,6 +275,6 @@ def test_expert_gemm_kernels_match_oracle(name, kind):
     ref = O.layer_forward(x64, Wg64, W164, W264, w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
                           b1=None if inp.b1 is None else inp.b1.astype(np.float64),
                           b2=None if inp.b2 is None else inp.b2.astype(np.float64),
-                          bf16=True, logits=gl)
+                          bf16=True, logits=gl, act=w.act)
     mx, rel = out_errors(as_f64(L["out"]), ref["out"])
     assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
