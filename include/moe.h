@@ -63,6 +63,12 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 #define MOE_FLAG_GEMM_SINGLE (1u << 4) /* bf16: 128x256 single-SM expert GEMM tiles */
 #define MOE_FLAG_GEMM_PAIR   (1u << 5) /* bf16: 256x256 tiles on SM pairs (cta_group::2) */
 #define MOE_FLAG_SWIGLU      (1u << 6) /* experts are W2 (SiLU(W1 x) * W3 x); see moe_expert_ffn */
+/* Testing only: with MOE_FLAG_GEMM_SINGLE, every CTA of the first expert
+ * product withholds its first operand load, so the MMA's bounded wait runs
+ * out (about 2 s): the kernel records MOE_ERR_TIMEOUT in the workspace error
+ * word, drains the loads it issued, frees its tensor memory and returns;
+ * outputs are undefined.  It exercises the timeout path without a fault. */
+#define MOE_FLAG_TEST_WAIT_TIMEOUT (1u << 7)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the

@@ -17,7 +17,8 @@ import os
 
 __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
-    "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU", "lib", "library_path", "make_desc",
+    "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU",
+    "MOE_FLAG_TEST_WAIT_TIMEOUT", "lib", "library_path", "make_desc",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "workspace",
@@ -31,6 +32,7 @@ MOE_FLAG_SIMT_ROUTER = 1 << 3
 MOE_FLAG_GEMM_SINGLE = 1 << 4
 MOE_FLAG_GEMM_PAIR = 1 << 5
 MOE_FLAG_SWIGLU = 1 << 6
+MOE_FLAG_TEST_WAIT_TIMEOUT = 1 << 7
 
 MOE_OK = 0
 

@@ -56,7 +56,7 @@ template <int BN, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const int32_t* __restrict__ offs, int E, int N, int K,
-                       const float* __restrict__ bias, bf16* __restrict__ C, int* err) {
+                       const float* __restrict__ bias, bf16* __restrict__ C, int* err, int stall) {
   using Cf = Cfg<BN>;
   constexpr int S = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -155,18 +155,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     n0 = (local / mt) * kOut;
   };
 
+  uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
+  bool producer = false;
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (tc::elect_one()) {
+      producer = true;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      uint32_t filled = 0, fill_par = 0;   // per-stage: ever filled / parity of the last fill
+      bool withhold = stall != 0;          // test hook: never arm or fill this CTA's first stage
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int e, row0, row_end, n0;
         decode(t, e, row0, row_end, n0);
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
+          if (withhold) {
+            withhold = false;
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           tc::mbar_arrive_expect_tx(full(stage), Cf::kStageBytes);
           tc::tma_load_2d(sA + stage * Cf::kABytes, &tmA, full(stage), kb * kBK, row0);
           if (kSwi) {
@@ -184,9 +192,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
       if (!ok) {
         set_error(err, kDevTimeout);
         s_abort = 1;
-        // let every load already issued land before the CTA can exit
-        for (int s = 0; s < S; ++s)
-          if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
       }
     }
     __syncwarp();
@@ -287,6 +292,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 
   tc::tc_fence_before();
   __syncthreads();
+  // after an abort, loads the producer issued but no MMA consumed must land before exit
+  if (producer && s_abort)
+    for (int s = 0; s < S; ++s)
+      if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, Cf::kTmemCols);
@@ -295,7 +304,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 
 template <int BN, int kEpi>
 cudaError_t run_gemm(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
-                     const float* bias, void* C, int* err, cudaStream_t st) {
+                     const float* bias, void* C, int* err, cudaStream_t st, int stall) {
   using Cf = Cfg<BN>;
   CUtensorMap ma, mb;
   if (!tma_map_bf16(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
@@ -306,7 +315,7 @@ cudaError_t run_gemm(const void* A, int64_t rows, const int32_t* offs, int E, co
   cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::kSmem);
   if (r != cudaSuccess) return r;
   return launch_kernel(k, dim3(sm_count()), dim3(kThreads), Cf::kSmem, st, 1, ma, mb, offs, E, N, K, bias,
-                       (bf16*)C, err);
+                       (bf16*)C, err, stall);
 }
 
 // 256-wide tiles unless 128-wide ones pad N less.
@@ -318,9 +327,10 @@ bool wide_tile(int N) {
 
 template <int kEpi>
 cudaError_t run_product(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
-                        const float* bias, void* C, int* err, cudaStream_t st) {
-  if (kEpi == kEpiSwiglu || wide_tile(N)) return run_gemm<256, kEpi>(A, rows, offs, E, B, N, K, bias, C, err, st);
-  return run_gemm<128, kEpi == kEpiSwiglu ? kEpiPlain : kEpi>(A, rows, offs, E, B, N, K, bias, C, err, st);
+                        const float* bias, void* C, int* err, cudaStream_t st, int stall = 0) {
+  if (kEpi == kEpiSwiglu || wide_tile(N))
+    return run_gemm<256, kEpi>(A, rows, offs, E, B, N, K, bias, C, err, st, stall);
+  return run_gemm<128, kEpi == kEpiSwiglu ? kEpiPlain : kEpi>(A, rows, offs, E, B, N, K, bias, C, err, st, stall);
 }
 
 }  // namespace
@@ -331,9 +341,10 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
     return cudaErrorNotSupported;
+  const int stall = (s.flags & MOE_FLAG_TEST_WAIT_TIMEOUT) ? 1 : 0;
   cudaError_t r = (s.flags & MOE_FLAG_SWIGLU)
-                      ? run_product<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st)
-                      : run_product<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
+                      ? run_product<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st, stall)
+                      : run_product<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st, stall);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
   return run_product<kEpiPlain>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);

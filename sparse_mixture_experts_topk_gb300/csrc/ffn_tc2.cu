@@ -156,13 +156,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     n0 = (local / mt) * kOut;
   };
 
+  uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
+  bool producer = false;
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (tc::elect_one()) {
+      producer = true;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      uint32_t filled = 0, fill_par = 0;
       for (int t = pair; t < total && ok; t += npairs) {
         int e, row0, row_end, n0;
         decode(t, e, row0, row_end, n0);
@@ -181,10 +183,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       if (!ok) {
         set_error(err, kDevTimeout);
         s_abort = 1;
-        // the pair's loads complete on the leader's barriers: it drains them
-        if (rank == 0)
-          for (int s = 0; s < S; ++s)
-            if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
       }
     }
     __syncwarp();
@@ -287,6 +285,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
   tc::tc_fence_before();
   __syncthreads();
+  // after an abort the leader drains its stage barriers, on which both CTAs'
+  // loads complete, before either CTA may leave
+  if (producer && rank == 0 && s_abort)
+    for (int s = 0; s < S; ++s)
+      if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
   tc::cluster_sync();             // neither CTA leaves while the other may still signal it
   if (warp == 1) {
     tc::tc_fence_after();

@@ -122,13 +122,15 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   pdl_enter();                     // first global access below
   const uint32_t tmem = s_tmem;
 
+  uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
+  bool producer = false;
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (tc::elect_one()) {
+      producer = true;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      uint32_t filled = 0, fill_par = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
         tc::mbar_arrive_expect_tx(full(stage), kABytes + b_bytes);
@@ -141,8 +143,6 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       if (!ok) {
         set_error(err, kDevTimeout);
         s_abort = 1;
-        for (int s = 0; s < kStages; ++s)
-          if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
       }
     }
     __syncwarp();
@@ -175,6 +175,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   // every thread: its token's partial scores, TMEM -> shared memory
   bool ok = tc::mbar_wait(done_bar, 0, nullptr, kWaitNs);
   if (!ok) set_error(err, kDevTimeout);
+  // after an abort, loads issued but never consumed land before the ring is reused
+  if (producer && (s_abort || !ok))
+    for (int s = 0; s < kStages; ++s)
+      if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
   ok = ok && !s_abort && kb1 > kb0;
   tc::tc_fence_after();
   __syncthreads();                 // the ring is free: every load landed and was consumed
