@@ -37,9 +37,10 @@ from sparse_mixture_experts_topk_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE layer tokens/s at 1 GB300; % of bf16 tensor peak (GEMM) and HBM BW"
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
-# kernels per layer pass on the bf16 tensor-core path: router (its tiles are
-# the dispatch histogram), scan, scatter, gather, 2 x expert GEMM, combine
-LAUNCHES_PER_STEP = 7
+# --gemm: the library's choice, or one expert GEMM kernel forced (descriptor
+# flags: single-SM tiles; SM pairs; SM pairs with token rows on the MMA's M
+# side for every product)
+GEMM_FLAGS = {"auto": 0, "single": 1 << 4, "pair": 1 << 5, "pair-rows": (1 << 5) | (1 << 8)}
 STAGES = ["router", "dispatch", "ffn_first", "ffn_second", "combine"]
 
 
@@ -241,9 +242,10 @@ def run_ours(args, w: W.Workload):
     x, Wg, W1, W2 = (to_dev(a, torch) for a in (inp.x, inp.Wg, inp.W1, inp.W2))
     gb = to_dev(inp.gate_bias, torch)
     dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
+    flags = (moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0) | GEMM_FLAGS[args.gemm]
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
-                      moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32,
-                      moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0, w.temperature)
+                      moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
+    launches_per_step = moe.moe_layer_launches(d)
     ws = moe.workspace(d)
     out = torch.empty((w.T, w.H), dtype=dt, device="cuda")
     aux = torch.empty(1, device="cuda")
@@ -358,14 +360,15 @@ def run_ours(args, w: W.Workload):
         "data": "synthetic",
         "config": {"workload": describe(w), "global_batch_tokens": world * w.T,
                    "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write)",
-                   "parallelism": f"replicas x{world}", "kept_rows": rows, "used_experts": used},
+                   "parallelism": f"replicas x{world}", "kept_rows": rows, "used_experts": used,
+                   "gemm": args.gemm},
         "roofline": roof,
         "stages": stages,
         "stage_timing": {"ms_per_step_with_stage_events": staged_step_ms,
                          "note": "per-stage CUDA events break kernel chaining; ms_per_step is timed "
                                  "with events around whole layer calls only"},
         "e2e": e2e_line,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps * 2,
+        "gpu_launches": launches_per_step * args.steps * 2,
         "clocks": clocks.summary(t0, t1) if clocks else None,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -418,6 +421,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.5)
+    ap.add_argument("--gemm", default="auto", choices=sorted(GEMM_FLAGS),
+                    help="expert GEMM kernel for bf16 prefill: the library's choice, or one forced")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -69,6 +69,11 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * word, drains the loads it issued, frees its tensor memory and returns;
  * outputs are undefined.  It exercises the timeout path without a fault. */
 #define MOE_FLAG_TEST_WAIT_TIMEOUT (1u << 7)
+/* bf16 with SM pairs: every block of an expert's token rows runs with the
+ * rows on the MMA's M side (padded to 256), instead of the default where an
+ * expert's last, short block runs swapped (rows on the N side, padded to
+ * 16).  Same results; for comparing the two (testing). */
+#define MOE_FLAG_GEMM_ROWS   (1u << 8)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the
@@ -237,6 +242,15 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg,
                       const void* W2, const float* b2, void* out, float* aux,
                       int32_t* count, int32_t* dropped, void* ws, size_t ws_bytes,
                       void* stream);
+
+/*
+ * How many kernels one moe_layer_forward with this description launches
+ * (no counterpart on the pages; it lets a caller or a benchmark account for
+ * the launches it issues).  Depends on the shape only: the path taken
+ * (one-block or multi-block dispatch, router variant) is chosen from it.
+ * Returns the count (>= 1), or a negative MOE_ERR_* for an invalid desc.
+ */
+int moe_layer_launches(const moe_desc* desc);
 
 /*
  * Stage timing for moe_layer_forward on the calling host thread (no

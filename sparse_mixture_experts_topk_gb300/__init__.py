@@ -18,10 +18,10 @@ import os
 __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU",
-    "MOE_FLAG_TEST_WAIT_TIMEOUT", "lib", "library_path", "make_desc",
+    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "lib", "library_path", "make_desc",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
-    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "workspace",
+    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "workspace",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -33,6 +33,7 @@ MOE_FLAG_GEMM_SINGLE = 1 << 4
 MOE_FLAG_GEMM_PAIR = 1 << 5
 MOE_FLAG_SWIGLU = 1 << 6
 MOE_FLAG_TEST_WAIT_TIMEOUT = 1 << 7
+MOE_FLAG_GEMM_ROWS = 1 << 8
 
 MOE_OK = 0
 
@@ -67,6 +68,7 @@ _SIGS = {
     "moe_layer_forward": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 12 + [ctypes.c_size_t, _P]),
     "moe_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_profile_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+    "moe_layer_launches": (ctypes.c_int, [ctypes.POINTER(MoeDesc)]),
 }
 
 _lib = None
@@ -185,6 +187,14 @@ def moe_layer_forward(desc, x, Wg, gate_bias, W1, b1, W2, b2, out, aux, count, d
         ctypes.byref(desc), _ptr(x), _ptr(Wg), _ptr(gate_bias), _ptr(W1), _ptr(b1), _ptr(W2),
         _ptr(b2), _ptr(out), _ptr(aux), _ptr(count), _ptr(dropped), _ptr(ws),
         ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def moe_layer_launches(desc: MoeDesc) -> int:
+    """Number of kernels one ``moe_layer_forward`` with ``desc`` launches."""
+    n = int(lib().moe_layer_launches(ctypes.byref(desc)))
+    if n < 0:
+        _check("moe_layer_launches", n)
+    return n
 
 
 def moe_get_device_error(ws, stream=None) -> int:

@@ -23,18 +23,24 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
                           void* h_perm, void* y_perm, int* err, cudaStream_t st);
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
-                               void* h_perm, void* y_perm, int* err, cudaStream_t st);
+                               void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st);
 
-// SM-pair tiles move a third less data per SM for the same MMA work but pad
-// each expert's rows to 256 instead of 128 (and N to 256).  Estimated cost
-// of each: padded tile area over its relative load efficiency.
+// SM-pair tiles move a third less data per SM for the same MMA work.  The
+// single-SM kernel pads each expert's rows to 128; the pair kernel runs its
+// GELU and plain products with the token rows on the MMA's N side, padded to
+// 16 (8 rows per expert on average), and the SwiGLU first product with rows
+// padded to 256.  Both pad the output columns to their tile width.
+// Estimated cost of each: padded tile area over its relative load
+// efficiency.
 bool use_pair_gemm(const Shape& s, int64_t rows) {
   if (s.flags & MOE_FLAG_GEMM_PAIR) return true;
   if (s.flags & MOE_FLAG_GEMM_SINGLE) return false;
   const double r = (double)rows;
   auto pad = [](int n, int t) { return (double)((n + t - 1) / t * t); };
   const double single = (r + 64.0 * s.E) * (pad(s.F, 128) + pad(s.H, 128));
-  const double paired = (r + 128.0 * s.E) * (pad(s.F, 256) + pad(s.H, 256)) / 1.5;
+  const bool m_rows = (s.flags & MOE_FLAG_GEMM_ROWS) != 0;   // token rows on the MMA's M side
+  const double first = (r + ((s.flags & MOE_FLAG_SWIGLU) || m_rows ? 128.0 : 8.0) * s.E) * pad(s.F, 256);
+  const double paired = (first + (r + (m_rows ? 128.0 : 8.0) * s.E) * pad(s.H, 256)) / 1.5;
   return paired < single;
 }
 
@@ -90,7 +96,7 @@ int sm_count() {
 
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
-                       void* h_perm, void* y_perm, int* err, cudaStream_t st) {
+                       void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
   if (s.T == 0 || max_rows == 0) return cudaSuccess;
   if (stream_ffn_eligible(s))
     return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
@@ -98,7 +104,7 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
   // unsupported shape or a missing tensor-map entry point is an error)
   if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
     if (use_pair_gemm(s, max_rows))
-      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
     return launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
   }
   return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
@@ -107,7 +113,7 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
 namespace {
 
 struct Layout {
-  size_t err, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
+  size_t err, sched, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
   size_t x_perm, h_perm, x_stage, out_stage, total;
   int64_t rows;
 };
@@ -155,7 +161,8 @@ Layout layout_of(const moe_desc& d) {
   };
   const size_t S = (size_t)s.S(), E = (size_t)s.E, es = s.esize();
   L.rows = rows_for(d);
-  L.err = take(256);
+  L.err = take(256);            // error word; the GEMM tile counters at +64
+  L.sched = L.err + 64;
   L.ids = take(S * 4);
   L.w = take(S * 4);
   L.psum_part = take((size_t)router_partials(s) * E * 4);
@@ -280,8 +287,12 @@ int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs
     return MOE_ERR_INVALID;
   const Layout L = layout_of(d);
   const Shape s = shape_of(d);
-  return cuda_status(launch_ffn(s, L.rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm,
-                                at<int>(ws, L.err), (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* sched = at<int32_t>(ws, L.sched);
+  cudaError_t e = cudaMemsetAsync(sched, 0, 2 * sizeof(int32_t), st);   // no dispatch kernel zeroed them
+  if (e == cudaSuccess)
+    e = launch_ffn(s, L.rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, at<int>(ws, L.err), sched, st);
+  return cuda_status(e);
 }
 
 int moe_combine(const moe_desc* desc, const void* y_perm, const int32_t* pos, const float* w, void* out,
@@ -300,6 +311,24 @@ int moe_aux_loss(const moe_desc* desc, const float* psum, const int32_t* count, 
   if (rc) return rc;
   if (!psum || !count || !loss) return MOE_ERR_INVALID;
   return cuda_status(launch_aux(shape_of(*desc), psum, count, loss, (cudaStream_t)stream));
+}
+
+namespace moe {
+// In the layer call the router counts its 128-token tiles' chosen experts
+// (the dispatch histogram) when the multi-block dispatch will read them.
+bool layer_fused_hist(const Shape& s) { return router_on_tensor_cores(s) && !dispatch_small(s); }
+}  // namespace moe
+
+int moe_layer_launches(const moe_desc* desc) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const Shape s = shape_of(*desc);
+  int n = 0;
+  if (s.T > 0) n += 1;                                  // router
+  if (dispatch_small(s)) n += 1;                        // one-block dispatch (also at T = 0)
+  else n += (layer_fused_hist(s) ? 0 : 1) + 3;          // histogram, scan, scatter, gather
+  if (s.T > 0) n += 2 + 1;                              // two expert products, combine
+  return n;
 }
 
 int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const float* gate_bias,
@@ -332,7 +361,7 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* w = at<float>(ws, L.w);
   float* part = at<float>(ws, L.psum_part);
-  const bool fused_hist = router_on_tensor_cores(s);
+  const bool fused_hist = layer_fused_hist(s);
   if (e == cudaSuccess)
     e = launch_router(s, xd, Wg, gate_bias, nullptr, ids, w, part, err, st,
                       fused_hist ? at<int32_t>(ws, L.blk_hist) : nullptr);
@@ -353,6 +382,7 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
     o.aux = aux;
     o.count_copy = count;
     o.dropped_copy = dropped;
+    o.sched = at<int32_t>(ws, L.sched);
     e = launch_dispatch(s, ids, xd, at<void>(ws, L.x_perm), o, err, st);
   }
   prof_mark(kMarkDispatch, st);
@@ -360,7 +390,8 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   void* h_perm = at<void>(ws, L.h_perm);
   void* y_perm = x_perm;   // x_perm is dead once the first product has run
   if (e == cudaSuccess)
-    e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err, st);
+    e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
+                   at<int32_t>(ws, L.sched), st);
   prof_mark(kMarkSecond, st);
   if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
   prof_mark(kMarkCombine, st);

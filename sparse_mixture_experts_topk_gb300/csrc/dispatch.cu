@@ -46,6 +46,72 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslo
   for (int e = threadIdx.x; e < E; e += kDispThreads) blk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
+// Thread e of a 256-thread block holds run = the number of slots routed to
+// expert e.  Cuts at the capacity and writes count, offs (exclusive prefix
+// of the kept counts, offs[E] = kept rows) and the dropped total; with
+// psum_part also the summed router probabilities and the load-balancing loss.
+__device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __restrict__ count,
+                                              int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
+                                              const float* __restrict__ psum_part, int64_t prows,
+                                              float* __restrict__ psum, float* __restrict__ aux, int64_t Tn,
+                                              int K, int32_t* __restrict__ count_copy,
+                                              int32_t* __restrict__ dropped_copy, int32_t* __restrict__ sched) {
+  __shared__ int sk[256];
+  __shared__ int sd[256];
+  __shared__ float sa[256];
+  const int e = threadIdx.x;
+  const int kept = (e < E) ? ((C > 0 && run > C) ? C : run) : 0;
+  sk[e] = kept;
+  sd[e] = (e < E) ? run - kept : 0;
+  __syncthreads();
+  // inclusive scan of kept (Hillis-Steele, 256 entries)
+  for (int o = 1; o < 256; o <<= 1) {
+    const int v = (e >= o) ? sk[e - o] : 0;
+    const int d = (e >= o) ? sd[e - o] : 0;
+    __syncthreads();
+    sk[e] += v;
+    sd[e] += d;
+    __syncthreads();
+  }
+  if (e < E) {
+    count[e] = run;
+    if (count_copy) count_copy[e] = run;
+    offs[e] = sk[e] - kept;
+    if (e == E - 1) offs[E] = sk[e];
+  }
+  if (e == 255) {
+    if (dropped) *dropped = sd[255];
+    if (dropped_copy) *dropped_copy = sd[255];
+  }
+  if (sched && e < 2) sched[e] = 0;   // the expert GEMMs that follow take tiles from these
+  if (psum_part) {
+    float p = 0.f;
+    if (e < E) {
+      // rows added in order; eight loads in flight
+      int64_t r = 0;
+      for (; r + 8 <= prows; r += 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = psum_part[(r + i) * E + e];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p += v[i];
+      }
+      for (; r < prows; ++r) p += psum_part[r * E + e];
+      if (psum) psum[e] = p;
+    }
+    if (aux) {
+      // E * sum_i (count_i / (T K)) * (psum_i / T), reduced in a fixed order
+      sa[e] = (e < E && Tn > 0) ? ((float)run / (float)(Tn * K)) * (p / (float)Tn) : 0.f;
+      __syncthreads();
+      for (int o = 128; o > 0; o >>= 1) {
+        if (e < o) sa[e] += sa[e + o];
+        __syncthreads();
+      }
+      if (e == 0) *aux = (float)E * sa[0];
+    }
+  }
+}
+
 // One block; thread e owns expert e (E <= 256).  With `staged`, the
 // [nblk, E] histogram is first copied to shared memory with coalesced loads
 // and scanned there.
@@ -55,11 +121,8 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
                      int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
                      const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
                      float* __restrict__ aux, int64_t Tn, int K, int32_t* __restrict__ count_copy,
-                     int32_t* __restrict__ dropped_copy) {
+                     int32_t* __restrict__ dropped_copy, int32_t* __restrict__ sched) {
   extern __shared__ int sh[];          // [nblk, E] when staged
-  __shared__ int sk[256];
-  __shared__ int sd[256];
-  __shared__ float sa[256];
   pdl_enter();
   const int e = threadIdx.x;
   const int64_t n = nblk * E;
@@ -95,68 +158,18 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
       run += h;
     }
   }
-  const int kept = (e < E) ? ((C > 0 && run > C) ? C : run) : 0;
-  sk[e] = kept;
-  sd[e] = (e < E) ? run - kept : 0;
-  __syncthreads();
-  // inclusive scan of kept (Hillis-Steele, 256 entries)
-  for (int o = 1; o < 256; o <<= 1) {
-    const int v = (e >= o) ? sk[e - o] : 0;
-    const int d = (e >= o) ? sd[e - o] : 0;
-    __syncthreads();
-    sk[e] += v;
-    sd[e] += d;
-    __syncthreads();
-  }
-  if (e < E) {
-    count[e] = run;
-    if (count_copy) count_copy[e] = run;
-    offs[e] = sk[e] - kept;
-    if (e == E - 1) offs[E] = sk[e];
-  }
-  if (e == 255) {
-    if (dropped) *dropped = sd[255];
-    if (dropped_copy) *dropped_copy = sd[255];
-  }
-  if (psum_part) {
-    float p = 0.f;
-    if (e < E) {
-      // rows added in order; eight loads in flight
-      int64_t r = 0;
-      for (; r + 8 <= prows; r += 8) {
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = psum_part[(r + i) * E + e];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p += v[i];
-      }
-      for (; r < prows; ++r) p += psum_part[r * E + e];
-      if (psum) psum[e] = p;
-    }
-    if (aux) {
-      // E * sum_i (count_i / (T K)) * (psum_i / T), reduced in a fixed order
-      sa[e] = (e < E && Tn > 0) ? ((float)run / (float)(Tn * K)) * (p / (float)Tn) : 0.f;
-      __syncthreads();
-      for (int o = 128; o > 0; o >>= 1) {
-        if (e < o) sa[e] += sa[e + o];
-        __syncthreads();
-      }
-      if (e == 0) *aux = (float)E * sa[0];
-    }
-  }
+  finish_counts(run, E, C, count, offs, dropped, psum_part, prows, psum, aux, Tn, K, count_copy,
+                dropped_copy, sched);
 }
 
-__global__ void __launch_bounds__(kDispThreads)
-dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
-                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offs,
-                        int32_t* __restrict__ pos, int32_t* __restrict__ src) {
+// Stable placement of slots [s0, s1): running[e] (shared) holds the rank
+// the next slot of expert e takes and is advanced past the range.  Ranks
+// within each 256-slot chunk come from a warp match plus per-warp counts.
+__device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ ids, int64_t s0, int64_t s1, int E,
+                                              int C, int* running, const int32_t* offs,
+                                              int32_t* __restrict__ pos, int32_t* __restrict__ src) {
   __shared__ int wcnt[kDispWarps][256];
-  __shared__ int running[256];
-  pdl_enter();
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int64_t s0 = (int64_t)blockIdx.x * bslots;
-  const int64_t s1 = min(S, s0 + bslots);
-  for (int e = tid; e < E; e += kDispThreads) running[e] = blk_base[(int64_t)blockIdx.x * E + e];
   for (int64_t c0 = s0; c0 < s1; c0 += kDispThreads) {
     for (int i = tid; i < kDispWarps * 256; i += kDispThreads) (&wcnt[0][0])[i] = 0;
     __syncthreads();
@@ -193,17 +206,25 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C
   }
 }
 
-// x_perm[r] = x[src[r] / K] for r < offs[E]; one warp per row.
-__global__ void __launch_bounds__(256)
-dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
-                       const int32_t* __restrict__ offs, int E, int K, int vec_per_row,
-                       uint4* __restrict__ x_perm) {
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
+                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offs,
+                        int32_t* __restrict__ pos, int32_t* __restrict__ src) {
+  __shared__ int running[256];
   pdl_enter();
-  const int64_t rows = offs[E];
+  const int64_t s0 = (int64_t)blockIdx.x * bslots;
+  const int64_t s1 = min(S, s0 + bslots);
+  for (int e = threadIdx.x; e < E; e += kDispThreads) running[e] = blk_base[(int64_t)blockIdx.x * E + e];
+  scatter_slots(ids, s0, s1, E, C, running, offs, pos, src);
+}
+
+// x_perm[r] = x[src[r] / K] for r in [0, rows), one warp per row; warps
+// w0, w0 + nw, ... of the caller's numbering.
+__device__ __forceinline__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ src,
+                                            int64_t rows, int K, int vec_per_row, uint4* __restrict__ x_perm,
+                                            int64_t w0, int64_t nw) {
   const int lane = threadIdx.x & 31;
-  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t r = warp0; r < rows; r += nwarps) {
+  for (int64_t r = w0; r < rows; r += nw) {
     const int64_t t = src[r] / K;
     const uint4* a = x + t * vec_per_row;
     uint4* b = x_perm + r * vec_per_row;
@@ -214,6 +235,49 @@ dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ 
     }
     for (; v < vec_per_row; v += 32) b[v] = a[v];
   }
+}
+
+// x_perm[r] = x[src[r] / K] for r < offs[E], over the whole grid.
+__global__ void __launch_bounds__(256)
+dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
+                       const int32_t* __restrict__ offs, int E, int K, int vec_per_row,
+                       uint4* __restrict__ x_perm) {
+  pdl_enter();
+  gather_rows(x, src, offs[E], K, vec_per_row, x_perm, ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5,
+              ((int64_t)gridDim.x * blockDim.x) >> 5);
+}
+
+// A small batch in one block: histogram, counts, stable placement and the
+// row gather, with the same arithmetic and results as the four-kernel path.
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int32_t* __restrict__ count,
+                      int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
+                      const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
+                      float* __restrict__ aux, int64_t Tn, int K, int32_t* __restrict__ count_copy,
+                      int32_t* __restrict__ dropped_copy, int32_t* __restrict__ pos, int32_t* __restrict__ src,
+                      const uint4* __restrict__ x, int vec_per_row, uint4* __restrict__ x_perm, int* err,
+                      int32_t* __restrict__ sched) {
+  __shared__ int hist[256];
+  __shared__ int s_offs[257];
+  pdl_enter();
+  const int e = threadIdx.x;
+  hist[e] = 0;
+  __syncthreads();
+  for (int64_t s = threadIdx.x; s < S; s += kDispThreads) {
+    const int v = ids[s];
+    if (v >= 0 && v < E) atomicAdd(&hist[v], 1);
+    else set_error(err, kDevBadIndex);
+  }
+  __syncthreads();
+  const int run = (e < E) ? hist[e] : 0;
+  finish_counts(run, E, C, count, offs, dropped, psum_part, prows, psum, aux, Tn, K, count_copy, dropped_copy,
+                sched);
+  __syncthreads();   // offs written by other threads of this block
+  for (int i = threadIdx.x; i <= E; i += kDispThreads) s_offs[i] = offs[i];
+  hist[e] = 0;       // reused as the running rank
+  __syncthreads();
+  scatter_slots(ids, 0, S, E, C, hist, s_offs, pos, src);
+  if (x) gather_rows(x, src, s_offs[E], K, vec_per_row, x_perm, threadIdx.x >> 5, kDispWarps);
 }
 
 }  // namespace
@@ -231,9 +295,26 @@ int64_t dispatch_blocks(const Shape& s) {
   return (s.S() + b - 1) / b;
 }
 
+bool dispatch_small(const Shape& s) {
+  // one block wins while its serial passes stay a few microseconds: up to
+  // four 256-slot chunks and 256 KB of rows for its eight warps to copy
+  return s.S() <= 4 * kDispThreads && s.S() * s.H * s.esize() <= 256 * 1024;
+}
+
 cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
                             const DispatchOut& o, int* err, cudaStream_t st) {
   const int64_t S = s.S();
+  if (dispatch_small(s)) {
+    const int vec = (int)((int64_t)s.H * s.esize() / 16);
+    const cudaError_t e =
+        launch_kernel(dispatch_small_kernel, dim3(1), dim3(kDispThreads), 0, st, 1, ids, S, s.E, s.C, o.count,
+                      o.offs, o.dropped, (const float*)o.psum_part,
+                      o.psum_part ? router_partial_rows(s) : (int64_t)0, o.psum, o.aux, s.T, s.K, o.count_copy,
+                      o.dropped_copy, o.pos, o.src, (const uint4*)(x && x_perm ? x : nullptr), vec,
+                      (uint4*)x_perm, err, o.sched);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   // blocks of slots: the router's 128-token tiles when it already counted
   // them, else blocks sized for a short scan
   const int bslots = o.hist_ready ? kRouterTileTokens * s.K : dispatch_block_slots(s);
@@ -251,7 +332,7 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
     e = launch_kernel(dispatch_scan_kernel, dim3(1), dim3(256), staged ? sm : 0, st, 1,
                       (const int32_t*)o.blk_hist, nblk, s.E, s.C, staged, o.blk_base, o.count, o.offs,
                       o.dropped, o.psum_part, o.psum_part ? router_partial_rows(s) : (int64_t)0, o.psum, o.aux,
-                      s.T, s.K, o.count_copy, o.dropped_copy);
+                      s.T, s.K, o.count_copy, o.dropped_copy, o.sched);
   if (e == cudaSuccess && nblk > 0)
     e = launch_kernel(dispatch_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
                       s.C, bslots, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos, o.src);

@@ -1,6 +1,5 @@
-// Expert FFN on CUDA cores: the fp32 layer, the bf16 fallback used to
-// cross-check the tensor-core kernel, and the weight-streaming kernel for
-// decode-sized batches.
+// Expert FFN on CUDA cores: the fp32 layer, and the bf16 path used to
+// cross-check the tensor-core kernels.
 //
 // Each expert is Linear -> GELU -> Linear (Qwen2-MoE module article, mlqm.cn,
 // section 2.2; MoE sparse-activation article, wmrh.cn, section 2.2):
@@ -114,113 +113,6 @@ grouped_gemm_simt_kernel(const T* __restrict__ A, const int32_t* __restrict__ of
   }
 }
 
-// Weight streaming for segments of at most kMaxRows rows (decode-sized
-// batches): the time is reading each used expert's weights once, so the
-// kernel is built for bytes in flight.  Block (x, y) handles kStreamRows
-// weight rows of the y-th expert that has rows (found from offs; blocks past
-// the last such expert exit).  The segment's activation rows are staged in
-// shared memory once per block; each warp takes rows of B in turn, and each
-// lane issues kUnroll independent 16-byte weight loads before any arithmetic.
-constexpr int kMaxRows = 16;
-constexpr int kStreamWarps = 8, kStreamRowsPerWarp = 2;
-constexpr int kStreamRows = kStreamWarps * kStreamRowsPerWarp;
-constexpr int kUnroll = 8;
-
-// With kEpi = kEpiSwiglu, B_e = [W1; W3] ([2N, K]) and output column n dots
-// the activation rows with gate row n and up row N + n.
-template <typename T, int kEpi>
-__global__ void __launch_bounds__(kStreamWarps * 32)
-stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int E, int mcap,
-                  const T* __restrict__ B, const float* __restrict__ bias, int N, int K,
-                  T* __restrict__ C, int* err) {
-  extern __shared__ uint4 s_act[];            // [m][K] activation rows, 16-byte vectors
-  __shared__ int s_e;
-  constexpr bool kSwi = kEpi == kEpiSwiglu;
-  pdl_enter();
-  if (threadIdx.x == 0) {
-    // the blockIdx.y-th expert with a non-empty segment
-    int found = -1, seen = 0;
-    for (int e = 0; e < E && found < 0; ++e)
-      if (offs[e + 1] > offs[e] && seen++ == (int)blockIdx.y) found = e;
-    s_e = found;
-  }
-  __syncthreads();
-  const int e = s_e;
-  if (e < 0) return;
-  const int r0 = offs[e], r1 = offs[e + 1];
-  int m = r1 - r0;
-  if (m > mcap) {                              // more rows than staged: report, compute the first mcap
-    if (threadIdx.x == 0) set_error(err, kDevBadIndex);
-    m = mcap;
-  }
-  constexpr int V = Vec<T>::N;
-  const int kv = K / V;
-  const uint4* Av = reinterpret_cast<const uint4*>(A + (int64_t)r0 * K);
-  for (int i = threadIdx.x; i < m * kv; i += blockDim.x) s_act[i] = Av[i];
-  __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const T* Be = B + (int64_t)e * N * K * (kSwi ? 2 : 1);
-  for (int q = 0; q < kStreamRowsPerWarp; ++q) {
-    const int n = blockIdx.x * kStreamRows + warp * kStreamRowsPerWarp + q;
-    if (n >= N) break;
-    const uint4* Bv = reinterpret_cast<const uint4*>(Be + (int64_t)n * K);
-    const uint4* Uv = reinterpret_cast<const uint4*>(Be + (int64_t)(N + n) * K);   // SwiGLU up row
-    float acc[kMaxRows], accu[kMaxRows];
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = accu[r] = 0.f;
-    for (int v0 = lane; v0 < kv; v0 += 32 * kUnroll) {
-      uint4 bw[kUnroll], uw[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + 32 * u;
-        if (v < kv) {
-          bw[u] = __ldcs(Bv + v);
-          if (kSwi) uw[u] = __ldcs(Uv + v);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + 32 * u;
-        if (v < kv) {
-          float b[V], bu[V];
-          Vec<T>::unpack(bw[u], b);
-          if (kSwi) Vec<T>::unpack(uw[u], bu);
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
-            if (r < m) {
-              float a[V];
-              Vec<T>::unpack(s_act[r * kv + v], a);
-#pragma unroll
-              for (int i = 0; i < V; ++i) {
-                acc[r] = fmaf(a[i], b[i], acc[r]);
-                if (kSwi) accu[r] = fmaf(a[i], bu[i], accu[r]);
-              }
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      if (r < m) {
-        float sg = acc[r], su = accu[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          sg += __shfl_xor_sync(0xffffffffu, sg, o);
-          if (kSwi) su += __shfl_xor_sync(0xffffffffu, su, o);
-        }
-        if (lane == 0) {
-          const int64_t bstride = (int64_t)N * (kSwi ? 2 : 1);
-          float v = sg + (bias ? bias[e * bstride + n] : 0.f);
-          if (kEpi == kEpiGelu) v = gelu_erf(v);
-          if (kSwi) v = silu_f(v) * (su + (bias ? bias[e * bstride + N + n] : 0.f));
-          C[(int64_t)(r0 + r) * N + n] = from_f32<T>(v);
-        }
-      }
-    }
-  }
-}
-
 template <typename T>
 cudaError_t run_simt(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                      const void* W1, const float* b1, const void* W2, const float* b2,
@@ -239,38 +131,7 @@ cudaError_t run_simt(const Shape& s, int64_t max_rows, const void* x_perm, const
                        (const T*)h_perm, offs, s.E, (const T*)W2, b2, s.H, s.F, (T*)y_perm);
 }
 
-template <typename T>
-cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
-                       const float* b1, const void* W2, const float* b2, void* h_perm, void* y_perm,
-                       int* err, cudaStream_t st) {
-  // at most T*K experts have rows; each block stages <= min(T, 16) rows
-  const int experts = (int)(s.S() < s.E ? s.S() : s.E);
-  const int mcap = (int)(s.T < kMaxRows ? s.T : kMaxRows);
-  const size_t smem1 = (size_t)mcap * s.H * s.esize();
-  const size_t smem2 = (size_t)mcap * s.F * s.esize();
-  auto k1 = (s.flags & MOE_FLAG_SWIGLU) ? stream_ffn_kernel<T, kEpiSwiglu> : stream_ffn_kernel<T, kEpiGelu>;
-  auto k2 = stream_ffn_kernel<T, kEpiPlain>;
-  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-  if (e != cudaSuccess) return e;
-  dim3 g1((s.F + kStreamRows - 1) / kStreamRows, experts);
-  e = launch_kernel(k1, g1, dim3(kStreamWarps * 32), smem1, st, 1, (const T*)x_perm, offs, s.E, mcap,
-                    (const T*)W1, b1, s.F, s.H, (T*)h_perm, err);
-  if (e != cudaSuccess) return e;
-  prof_mark(kMarkFirst, st);
-  dim3 g2((s.H + kStreamRows - 1) / kStreamRows, experts);
-  return launch_kernel(k2, g2, dim3(kStreamWarps * 32), smem2, st, 1, (const T*)h_perm, offs, s.E, mcap,
-                       (const T*)W2, b2, s.H, s.F, (T*)y_perm, err);
-}
-
 }  // namespace
-
-// decode-sized batches whose staged activation rows fit in shared memory
-bool stream_ffn_eligible(const Shape& s) {
-  if (s.T > kMaxRows || (s.flags & MOE_FLAG_NO_DECODE)) return false;
-  const int64_t widest = s.H > s.F ? s.H : s.F;
-  return s.T * widest * (int64_t)s.esize() <= 200 * 1024;
-}
 
 cudaError_t launch_ffn_simt(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                             const void* W1, const float* b1, const void* W2, const float* b2,
@@ -278,14 +139,6 @@ cudaError_t launch_ffn_simt(const Shape& s, int64_t max_rows, const void* x_perm
   if (s.dtype == MOE_BF16)
     return run_simt<bf16>(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
   return run_simt<float>(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
-}
-
-cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
-                              const float* b1, const void* W2, const float* b2, void* h_perm,
-                              void* y_perm, int* err, cudaStream_t st) {
-  if (s.dtype == MOE_BF16)
-    return run_stream<bf16>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
-  return run_stream<float>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
 }
 
 }  // namespace moe

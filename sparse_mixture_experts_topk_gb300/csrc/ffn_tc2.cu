@@ -1,6 +1,5 @@
-// Expert FFN on CTA pairs: the grouped GEMM of ffn_tc.cu with 256 x 256
-// output tiles computed by the two SMs of a 2-CTA cluster (tcgen05
-// .cta_group::2).
+// Expert FFN on CTA pairs: the grouped GEMM of ffn_tc.cu computed by the two
+// SMs of a 2-CTA cluster (tcgen05 .cta_group::2, MMA M = 256).
 //
 // Same products (Qwen2-MoE module article, mlqm.cn, section 2.2: each expert
 // is Linear -> GELU -> Linear):
@@ -9,22 +8,36 @@
 // Why pairs: with one SM per 128 x 256 tile, every k-block brings 48 KB into
 // the SM (A 16 KB + B 32 KB) for 128 x 256 x 64 multiply-adds, and the
 // measured kernel was bound by that load stream rather than by the tensor
-// cores.  A pair computes 256 x 256 per k-block while each SM loads only its
-// own 128 rows of A and its own 128 rows (N half) of B: 32 KB per SM for the
-// same work per SM.  The price is that expert segments are padded to 256
-// rows instead of 128.
+// cores.  A pair computes 256 x 256 per k-block while each SM loads 32 KB.
+//
+// Orientation, per tile.  A full 256-row block of an expert's token rows
+// runs in row orientation: MMA M = the 256 token rows (128 per CTA), N = 256
+// weight rows (output columns, 128 per CTA), and each epilogue thread owns
+// one token row of its CTA's accumulator.  An expert's last block, when it
+// holds fewer than 256 rows, runs swapped in the GELU and plain products:
+// M = 256 weight rows, N = the block's token rows rounded up to 16 and split
+// across the pair, so the block is padded to a multiple of 16 instead of to
+// 256 (20% of the MMA work at the 8192-token layer).  Each CTA then loads
+// only the 32-row boxes of token rows its half needs; the accumulator holds
+// the transposed tile (TMEM lane = output column, column = token row), and
+// each epilogue warp transposes its 32 x 32 blocks through 2 KB of shared
+// memory so that global stores stay 16-byte vectors along the row.  Full
+// blocks stay in row orientation because that transpose costs shared-memory
+// bandwidth the tensor cores need (measured: 15% slower for full tiles).
+// The SwiGLU first product keeps the row orientation for every block (N =
+// 128 gate rows in the leader and the matching 128 up rows in the peer), so
+// each CTA's accumulator holds gate | up for the same output columns.
 //
 // Roles, per CTA (192 threads), rank r = 0 (leader) or 1:
-//   warp 0     TMA producer: A rows [row0 + 128 r, +128) and B rows
-//              [n0 + 128 r, +128) of each k-block into this CTA's ring; both
-//              CTAs' loads complete on the LEADER's `full` barrier, which the
-//              leader arms for the 64 KB of the pair;
+//   warp 0     TMA producer: this CTA's share of A and B for each k-block into
+//              its ring; both CTAs' loads complete on the LEADER's `full`
+//              barrier, which the leader arms for the pair's bytes;
 //   warp 1     leader only: one thread issues tcgen05.mma.cta_group::2
-//              (M = 256, N = 256, K = 16) x 4 per stage; its commits arrive on
-//              the `empty` / `tfull` barriers of both CTAs (multicast);
-//   warps 2-5  epilogue in both CTAs: this CTA's 128 accumulator rows from its
-//              own TMEM -> bias -> GELU -> bf16 -> global; then arrive on the
-//              leader's `tempty` (256 arrivals = both CTAs).
+//              (M = 256, K = 16) x 4 per stage; its commits arrive on the
+//              `empty` / `tfull` barriers of both CTAs (multicast);
+//   warps 2-5  epilogue in both CTAs: this CTA's 128 accumulator lanes from its
+//              own TMEM -> bias -> activation -> bf16 -> global; then arrive on
+//              the leader's `tempty` (256 arrivals = both CTAs).
 // All waits are bounded (timeout -> error word + abort flag); the CTAs meet
 // in cluster barriers after set-up and before exit so neither can touch the
 // other's shared memory once it has left.
@@ -36,26 +49,40 @@ namespace moe {
 
 namespace {
 
-constexpr int kBM = 128;             // rows per CTA (the pair covers 256)
-constexpr int kBNh = 128;            // B rows per CTA (the pair covers N = 256)
+constexpr int kBM = 128;             // A rows per CTA (the pair covers M = 256)
+constexpr int kBNh = 128;            // B rows per CTA at most (the pair covers N <= 256)
 constexpr int kBK = 64;
+constexpr int kBoxB = 32;            // swapped: token rows per B box
 constexpr int kThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBNh * kBK * 2;
+constexpr int kBoxBytes = kBoxB * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kStages = 6;
 constexpr int kTmemCols = 512;       // two 256-column accumulators
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes;
+constexpr int kXposeBytes = 4 * 32 * 32 * 2;   // epilogue transpose blocks, one per warp
+constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kXposeBytes;
 constexpr uint64_t kWaitNs = 2000000000ull;
+// Tile queue: the leader's producer takes tiles from a global counter and
+// publishes them here, in both CTAs, for every other role.  No role can be
+// more than kStages + 2 tiles behind the producer (its ring and the two
+// accumulators hold it back), so 16 entries never overwrite one still unread.
+constexpr int kTQ = 16;
+static_assert(kTQ > kStages + 3, "tile queue shorter than the pipeline");
+constexpr int kTqAbort = -2;
 
-// kEpi = kEpiSwiglu: B = [W1; W3] stacked per expert ([E, 2N, K]); the
-// leader loads 128 gate rows and the peer the matching 128 up rows, so each
-// CTA's 256 accumulator columns are gate | up for 128 output columns.
+// Tensor maps: tmX = token rows [rows, K] in 128-row boxes (row-orientation
+// A), tmXs = the same rows in 32-row boxes (swapped B), tmW = weight rows
+// [E N, K] in 128-row boxes (row-orientation B, swapped A).  kEpi =
+// kEpiSwiglu: tmW covers [W1; W3] stacked per expert ([E, 2N, K]); the leader
+// loads 128 gate rows and the peer the matching 128 up rows.  swap_tail = 0
+// keeps every block in row orientation.
 template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const int32_t* __restrict__ offs, int E, int N, int K,
-                         const float* __restrict__ bias, bf16* __restrict__ C, int* err) {
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXs,
+                         const __grid_constant__ CUtensorMap tmW, const int32_t* __restrict__ offs, int E, int N,
+                         int K, int swap_tail, int* __restrict__ next_tile, const float* __restrict__ bias,
+                         bf16* __restrict__ C, int* err) {
   constexpr int S = kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_offs[257];
@@ -63,10 +90,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ __align__(8) uint64_t s_bar[2 * S + 5];
+  __shared__ __align__(8) unsigned long long s_tq[kTQ];   // (sequence + 1) << 32 | tile, tile -1 = end
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA = tc::smem_u32(smem);
   const uint32_t sB = sA + S * kABytes;
+  bf16* xpose = reinterpret_cast<bf16*>(smem + (size_t)S * kStageBytes);   // [4][32][32]
   auto full = [&](int s) { return tc::smem_u32(&s_bar[s]); };
   auto empty = [&](int s) { return tc::smem_u32(&s_bar[S + s]); };
   auto tfull = [&](int a) { return tc::smem_u32(&s_bar[2 * S + a]); };
@@ -75,16 +104,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_ctarank();          // 0 = leader
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   constexpr bool kSwi = kEpi == kEpiSwiglu;
   constexpr int kOut = kSwi ? kBNh : 2 * kBNh;   // output columns per pair tile
   const int nt = (N + kOut - 1) / kOut;
   const int nk = (K + kBK - 1) / kBK;
-  constexpr uint32_t kIdesc = tc::idesc_bf16_f32(2 * kBM, 2 * kBNh);
 
   if (warp == 0) {
     pdl_enter();   // the tile table reads offs, written by the previous kernel
-    // per-expert pair-tile counts (256-row m-tiles x n-tiles) and their prefix
+    // per-expert pair-tile counts (256-row blocks x n-tiles) and their prefix
     int loc[8];
     int sum = 0;
 #pragma unroll
@@ -125,10 +152,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       }
       tc::mbar_init(done_bar, 1);
       s_abort = 0;
+      for (int i = 0; i < kTQ; ++i) s_tq[i] = 0ull;
       tc::fence_barrier_init();
       tc::fence_proxy_async_smem();
-      tc::prefetch_tmap(&tmA);
-      tc::prefetch_tmap(&tmB);
+      tc::prefetch_tmap(&tmX);
+      tc::prefetch_tmap(&tmXs);
+      tc::prefetch_tmap(&tmW);
     }
   } else if (warp == 1) {
     tc::tmem_alloc_pair(tc::smem_u32(&s_tmem), kTmemCols);
@@ -142,18 +171,56 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   const uint32_t tmem = s_tmem;
   const int total = s_tstart[E];
 
-  auto decode = [&](int t, int& e, int& row0, int& row_end, int& n0) {
+  // the leader's producer publishes tile `t` (or -1, the end) as entry `seq`
+  auto tq_publish = [&](int seq, int t) {
+    const unsigned long long v = ((unsigned long long)(unsigned)(seq + 1) << 32) | (unsigned)t;
+    volatile unsigned long long* slot = &s_tq[seq & (kTQ - 1)];
+    *slot = v;
+    tc::st_peer_u64(tc::map_peer(tc::smem_u32(&s_tq[seq & (kTQ - 1)]), 1), v);
+  };
+  // entry `seq` of this CTA's queue: a tile, -1 at the end, kTqAbort if the
+  // kernel is aborting or the entry did not arrive in time
+  auto tq_read = [&](int seq) -> int {
+    volatile unsigned long long* slot = &s_tq[seq & (kTQ - 1)];
+    const unsigned long long want = (unsigned long long)(unsigned)(seq + 1);
+    uint64_t t0 = 0;
+    for (int i = 0;; ++i) {
+      const unsigned long long v = *slot;
+      if ((v >> 32) == want) return (int)(unsigned)(v & 0xffffffffull);
+      if (s_abort) return kTqAbort;
+      if ((i & 255) == 255) {
+        const uint64_t now = tc::globaltimer();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > kWaitNs) return kTqAbort;
+      }
+    }
+  };
+
+  // tile t -> expert e, its first token row (the pair's), the rows of that
+  // block (<= 256), the MMA N (swapped: rows rounded up to 16; else 256) and
+  // the first output column.  Tiles run expert by expert, row blocks inner.
+  struct Tile {
+    int e, row_base, nrows, row_end, mma_n, n0;
+    bool swap;
+  };
+  auto decode = [&](int t) {
+    Tile d;
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_tstart[mid] <= t) lo = mid; else hi = mid - 1;
     }
-    e = lo;
-    const int mt = (s_offs[e + 1] - s_offs[e] + 2 * kBM - 1) / (2 * kBM);
-    const int local = t - s_tstart[e];
-    row0 = s_offs[e] + (local % mt) * (2 * kBM) + (int)rank * kBM;   // this CTA's half
-    row_end = s_offs[e + 1];
-    n0 = (local / mt) * kOut;
+    d.e = lo;
+    const int rows = s_offs[d.e + 1] - s_offs[d.e];
+    const int mt = (rows + 2 * kBM - 1) / (2 * kBM);
+    const int local = t - s_tstart[d.e];
+    d.row_base = s_offs[d.e] + (local % mt) * (2 * kBM);
+    d.row_end = s_offs[d.e + 1];
+    d.nrows = min(2 * kBM, d.row_end - d.row_base);
+    d.swap = !kSwi && swap_tail && d.nrows < 2 * kBM;
+    d.mma_n = d.swap ? (d.nrows + 15) / 16 * 16 : 2 * kBNh;
+    d.n0 = (local / mt) * kOut;
+    return d;
   };
 
   uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
@@ -165,16 +232,37 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = pair; t < total && ok; t += npairs) {
-        int e, row0, row_end, n0;
-        decode(t, e, row0, row_end, n0);
+      int t_next = rank == 0 ? atomicAdd(next_tile, 1) : 0;
+      for (int seq = 0; ok; ++seq) {
+        int t;
+        if (rank == 0) {
+          t = t_next < total ? t_next : -1;
+          tq_publish(seq, t);
+          if (t >= 0) t_next = atomicAdd(next_tile, 1);   // the following tile, fetched while this one loads
+        } else {
+          t = tq_read(seq);
+          if (t == kTqAbort) { ok = false; break; }
+        }
+        if (t < 0) break;
+        const Tile d = decode(t);
+        // swapped: this CTA's token rows start half the MMA N into the block
+        const int half = d.mma_n / 2;
+        const int nbox = (half + kBoxB - 1) / kBoxB;
+        const uint32_t tx = d.swap ? 2u * (uint32_t)(kABytes + nbox * kBoxBytes) : 2u * kStageBytes;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
           const uint32_t fbar = tc::map_peer(full(stage), 0);
-          if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
-          tc::tma_load_2d_pair(sA + stage * kABytes, &tmA, fbar, kb * kBK, row0);
-          tc::tma_load_2d_pair(sB + stage * kBBytes, &tmB, fbar, kb * kBK,
-                               kSwi ? 2 * e * N + (int)rank * N + n0 : e * N + n0 + (int)rank * kBNh);
+          if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), tx);
+          if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
+            tc::tma_load_2d_pair(sA + stage * kABytes, &tmW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+            for (int i = 0; i < nbox; ++i)
+              tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, &tmXs, fbar, kb * kBK,
+                                   d.row_base + (int)rank * half + i * kBoxB);
+          } else {        // A = this CTA's 128 token rows, B = its 128 weight rows
+            tc::tma_load_2d_pair(sA + stage * kABytes, &tmX, fbar, kb * kBK, d.row_base + (int)rank * kBM);
+            tc::tma_load_2d_pair(sB + stage * kBBytes, &tmW, fbar, kb * kBK,
+                                 kSwi ? 2 * d.e * N + (int)rank * N + d.n0 : d.e * N + d.n0 + (int)rank * kBNh);
+          }
           filled |= 1u << stage;
           fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -194,7 +282,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = pair; t < total && ok; t += npairs) {
+      for (int seq = 0; ok; ++seq) {
+        const int t = tq_read(seq);
+        if (t == kTqAbort) { ok = false; break; }
+        if (t < 0) break;
+        const uint32_t idesc = tc::idesc_bf16_f32(2 * kBM, decode(t).mma_n);
         if (!tc::mbar_wait(tempty(acc), acc_phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * 2 * kBNh);
@@ -204,7 +296,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           const uint32_t a0 = sA + stage * kABytes, b0 = sB + stage * kBBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            tc::mma_bf16_pair(d, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(b0 + k * 32), kIdesc,
+            tc::mma_bf16_pair(d, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(b0 + k * 32), idesc,
                               (kb | k) != 0);
           tc::tc_commit_pair_mc(empty(stage), 0x3);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -227,50 +319,85 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
+    bf16* xb = xpose + q * 32 * 32;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = pair; t < total; t += npairs) {
-      int e, row0, row_end, n0;
-      decode(t, e, row0, row_end, n0);
+    for (int seq = 0;; ++seq) {
+      const int t = tq_read(seq);
+      if (t == kTqAbort) {
+        set_error(err, kDevTimeout);
+        s_abort = 1;
+        break;
+      }
+      if (t < 0) break;
+      const Tile d = decode(t);
       if (!tc::mbar_wait(tfull(acc), acc_phase, &s_abort, kWaitNs)) {
         set_error(err, kDevTimeout);
         s_abort = 1;
         break;
       }
       tc::tc_fence_after();
-      const int row = row0 + q * 32 + lane;
-      const bool row_ok = row < row_end;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kBNh);
-      const float* be = bias ? bias + (int64_t)e * (kSwi ? 2 * N : N) : nullptr;
+      const float* be = bias ? bias + (int64_t)d.e * (kSwi ? 2 * N : N) : nullptr;
+      if (d.swap) {
+        // lane = output column f, accumulator column j = token row row_base + j
+        const int f = d.n0 + (int)rank * kBM + q * 32 + lane;
+        const float bf = (be && f < N) ? be[f] : 0.f;
+        const int fv = d.n0 + (int)rank * kBM + q * 32 + 8 * (lane & 3);   // this lane's 8 stored columns
 #pragma unroll 1
-      for (int c = 0; c < kOut / 32; ++c) {
-        const int col0 = n0 + c * 32;
-        if (col0 >= N) break;
-        uint32_t r[32], u[kSwi ? 32 : 1];
-        tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
-        if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
-        tc::tmem_wait_ld();
-        if (row_ok) {
-          bf16* dst = C + (int64_t)row * N + col0;
+        for (int c = 0; c * 32 < d.nrows; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + g * 8 < N) {
-              float v[8];
+          for (int j = 0; j < 32; ++j) {
+            const float a = __uint_as_float(r[j]) + bf;
+            xb[j * 32 + lane] = __float2bfloat16_rn(kEpi == kEpiGelu ? gelu_erf(a) : a);
+          }
+          __syncwarp();
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float a = __uint_as_float(r[g * 8 + j]);
-                if (be) a += be[col0 + g * 8 + j];
-                if (kEpi == kEpiGelu) {
-                  v[j] = gelu_erf(a);
-                } else if (kSwi) {
-                  float b = __uint_as_float(u[(g * 8 + j) % (kSwi ? 32 : 1)]);
-                  if (be) b += be[N + col0 + g * 8 + j];
-                  v[j] = silu_f(a) * b;
-                } else {
-                  v[j] = a;
+          for (int i = 0; i < 4; ++i) {
+            const int jj = (lane >> 2) + 8 * i;
+            const int row = d.row_base + c * 32 + jj;
+            if (row < d.row_end && fv < N)
+              *reinterpret_cast<uint4*>(C + (int64_t)row * N + fv) =
+                  *reinterpret_cast<const uint4*>(xb + jj * 32 + 8 * (lane & 3));
+          }
+          __syncwarp();
+        }
+      } else {
+        const int row = d.row_base + (int)rank * kBM + q * 32 + lane;
+        const bool row_ok = row < d.row_end;
+#pragma unroll 1
+        for (int c = 0; c < kOut / 32; ++c) {
+          const int col0 = d.n0 + c * 32;
+          if (col0 >= N) break;
+          uint32_t r[32], u[kSwi ? 32 : 1];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
+          tc::tmem_wait_ld();
+          if (row_ok) {
+            bf16* dst = C + (int64_t)row * N + col0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              if (col0 + g * 8 < N) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  float a = __uint_as_float(r[g * 8 + j]);
+                  if (be) a += be[col0 + g * 8 + j];
+                  if (kEpi == kEpiGelu) {
+                    v[j] = gelu_erf(a);
+                  } else if (kSwi) {
+                    float b = __uint_as_float(u[(g * 8 + j) % (kSwi ? 32 : 1)]);
+                    if (be) b += be[N + col0 + g * 8 + j];
+                    v[j] = silu_f(a) * b;
+                  } else {
+                    v[j] = a;
+                  }
                 }
+                *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
               }
-              *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
             }
           }
         }
@@ -299,10 +426,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
 template <int kEpi>
 cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
-                     const float* bias, void* C, int* err, cudaStream_t st) {
-  CUtensorMap ma, mb;
-  if (!tma_map_bf16(&ma, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
-  if (!tma_map_bf16(&mb, B, (uint64_t)E * N * (kEpi == kEpiSwiglu ? 2 : 1), (uint64_t)K, kBNh))
+                     const float* bias, void* C, int swap_tail, int* next_tile, int* err, cudaStream_t st) {
+  CUtensorMap mx, mxs, mw;
+  if (!tma_map_bf16(&mx, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
+  if (!tma_map_bf16(&mxs, A, (uint64_t)rows, (uint64_t)K, kBoxB)) return cudaErrorNotSupported;
+  if (!tma_map_bf16(&mw, B, (uint64_t)E * N * (kEpi == kEpiSwiglu ? 2 : 1), (uint64_t)K, kBNh))
     return cudaErrorNotSupported;
   auto kern = grouped_gemm_pair_kernel<kEpi>;
   cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
@@ -323,24 +451,28 @@ cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, co
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   int fit = 0;
   if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < pairs) pairs = fit;
-  return launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmem, st, 2, ma, mb, offs, E, N, K,
-                       bias, (bf16*)C, err);
+  return launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmem, st, 2, mx, mxs, mw, offs, E, N, K,
+                       swap_tail, next_tile, bias, (bf16*)C, err);
 }
 
 }  // namespace
 
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
-                               void* h_perm, void* y_perm, int* err, cudaStream_t st) {
+                               void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
+  if (!sched) return cudaErrorInvalidValue;
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
     return cudaErrorNotSupported;
+  // each expert's last, short row block runs swapped unless all are forced to rows
+  const int swap_tail = (s.flags & MOE_FLAG_GEMM_ROWS) ? 0 : 1;
   cudaError_t r = (s.flags & MOE_FLAG_SWIGLU)
-                      ? run_pair<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st)
-                      : run_pair<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, err, st);
+                      ? run_pair<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, 0, sched, err, st)
+                      : run_pair<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, swap_tail, sched,
+                                           err, st);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
-  return run_pair<kEpiPlain>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, err, st);
+  return run_pair<kEpiPlain>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, swap_tail, sched + 1, err, st);
 }
 
 }  // namespace moe

@@ -67,6 +67,7 @@ bool tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
 // Upper bound of the rows of per-block probability partial sums the router
 // writes (workspace sizing), and the rows the chosen router writes.
 int64_t router_partials(const Shape& s);
+bool router_small(const Shape& s);   // one-cluster router for decode-sized bf16 batches
 int64_t router_partial_rows(const Shape& s);
 bool router_on_tensor_cores(const Shape& s);
 // tile_hist (nullable): [ceil(T/128), E] count of each 128-token tile's
@@ -84,6 +85,7 @@ cudaError_t launch_psum_reduce(const Shape& s, const float* psum_part, float* ps
 // ---------------------------------------------------------------- dispatch
 int64_t dispatch_blocks(const Shape& s);
 int dispatch_block_slots(const Shape& s);
+bool dispatch_small(const Shape& s);   // one-block dispatch (launch_dispatch picks it itself)
 struct DispatchOut {
   int32_t* count;      // [E]
   int32_t* offs;       // [E+1]
@@ -99,14 +101,16 @@ struct DispatchOut {
   float* aux;              // [1] or null (needs psum_part)
   int32_t* count_copy;     // [E] or null
   int32_t* dropped_copy;   // [1] or null
+  int32_t* sched;          // [2] the expert GEMMs' tile counters, zeroed here, or null
 };
 cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
                             const DispatchOut& o, int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------- expert FFN
+// sched: two zeroed ints, the tile counters of the SM-pair kernel's two products
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
-                       void* h_perm, void* y_perm, int* err, cudaStream_t st);
+                       void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine / aux
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* pos, const float* w,

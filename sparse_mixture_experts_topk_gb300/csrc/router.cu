@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -31,6 +32,79 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// One warp per token: ls holds nt rows of E fp32 scores (row pitch E + 1).
+// Lane l holds experts l + 32 i; the k largest scores are taken one at a
+// time by a warp arg-max with ties to the lower index; the token's ids and
+// weights are written, and its ls row is replaced by the full softmax (for
+// the load-balancing sums).
+__device__ __forceinline__ void finish_tokens(float* ls, int nt, int64_t t0, int E, int K, float inv_tau,
+                                              int32_t* __restrict__ ids, float* __restrict__ w, int warp0,
+                                              int nwarps) {
+  const int lane = threadIdx.x & 31;
+  for (int tt = warp0; tt < nt; tt += nwarps) {
+    float v[8];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? ls[tt * (E + 1) + e] : -INFINITY;
+      m = fmaxf(m, v[i]);
+    }
+    m = warp_max(m);
+    float zs = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) zs += expf((v[i] - m) * inv_tau);
+    }
+    zs = warp_sum(zs);
+    unsigned taken = 0;
+    int sel_id[8];
+    float sel_z[8];
+    float zsel = 0.f;
+    for (int j = 0; j < K; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float z = expf((bv - m) * inv_tau);
+      sel_id[j] = bi;
+      sel_z[j] = z;
+      zsel += z;
+    }
+    if (lane == 0) {
+      const int64_t t = t0 + tt;
+      for (int j = 0; j < K; ++j) {
+        ids[t * K + j] = sel_id[j];
+        w[t * K + j] = sel_z[j] / zsel;
+      }
+    }
+    // full-softmax probabilities for the load-balancing statistics
+    const float inv = 1.f / zs;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) ls[tt * (E + 1) + e] = expf((v[i] - m) * inv_tau) * inv;
+    }
+  }
 }
 
 // Per block: kRouterTok tokens.  Thread (warp w, lane l) accumulates the
@@ -93,69 +167,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
       logits[(t0 + r) * (int64_t)E + e] = ls[r * (E + 1) + e];
     }
   }
-  // softmax statistics and top-k; lane holds experts lane + 32 i
-  for (int tt = warp; tt < nt; tt += kRouterWarps) {
-    float v[8];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? ls[tt * (E + 1) + e] : -INFINITY;
-      m = fmaxf(m, v[i]);
-    }
-    m = warp_max(m);
-    float zs = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) zs += expf((v[i] - m) * inv_tau);
-    }
-    zs = warp_sum(zs);
-    unsigned taken = 0;
-    int sel_id[8];
-    float sel_z[8];
-    float zsel = 0.f;
-    for (int j = 0; j < K; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float z = expf((bv - m) * inv_tau);
-      sel_id[j] = bi;
-      sel_z[j] = z;
-      zsel += z;
-    }
-    if (lane == 0) {
-      const int64_t t = t0 + tt;
-      for (int j = 0; j < K; ++j) {
-        ids[t * K + j] = sel_id[j];
-        w[t * K + j] = sel_z[j] / zsel;
-      }
-    }
-    // full-softmax probabilities for the load-balancing statistics
-    const float inv = 1.f / zs;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) ls[tt * (E + 1) + e] = expf((v[i] - m) * inv_tau) * inv;
-    }
-  }
+  finish_tokens(ls, nt, t0, E, K, inv_tau, ids, w, warp, kRouterWarps);
   __syncthreads();
   if (psum_part) {
     for (int e = tid; e < E; e += kRouterThreads) {
@@ -163,6 +175,118 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
       for (int r = 0; r < nt; ++r) s += ls[r * (E + 1) + e];
       psum_part[(int64_t)blockIdx.x * E + e] = s;
     }
+  }
+}
+
+// Decode-sized batches (T <= kSmallTok, bf16): the cost is reading Wg once
+// and the latency of the few steps, so one cluster of up to 8 CTAs does it
+// all.  Warp g of the cluster owns gate rows g, g + G, ... (G = its warps);
+// each lane loads kSmallChunk 16-byte vectors of a row in one go, issued
+// before the token rows are staged in shared memory, and dots them with every
+// staged token.  The T scores of a row go straight into the leader CTA's
+// score table over distributed shared memory; after one cluster barrier the
+// leader finishes each token (bias, top-k, weights), sums the probabilities
+// per expert in token order into psum_part[0] and counts the chosen experts
+// into tile_hist[0] (the layer's single 128-token tile).
+constexpr int kSmallTok = 16;
+constexpr int kSmallChunk = 8;
+constexpr int kSmallMaxCta = 8;
+
+__global__ void __launch_bounds__(kRouterThreads)
+router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wg,
+                    const float* __restrict__ gate_bias, int Tn, int H, int E, int K, float inv_tau,
+                    float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ w,
+                    float* __restrict__ psum_part, int32_t* __restrict__ tile_hist) {
+  extern __shared__ uint4 s_x[];                       // [Tn][H] token rows, then [Tn][E+1] scores
+  __shared__ int s_hist[256];
+  constexpr int V = Vec<bf16>::N;
+  const int kv = H / V;
+  float* ls = reinterpret_cast<float*>(s_x + (size_t)Tn * kv);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t rank = tc::cluster_ctarank();
+  const int g0 = (int)rank * kRouterWarps + warp;
+  const int G = (int)gridDim.x * kRouterWarps;
+  const int nch = (kv + 32 * kSmallChunk - 1) / (32 * kSmallChunk);   // pieces per gate row
+  const int pieces = g0 < E ? ((E - 1 - g0) / G + 1) * nch : 0;
+  for (int e = threadIdx.x; e < 256; e += kRouterThreads) s_hist[e] = 0;
+  pdl_enter();
+  uint4 gw[kSmallChunk];
+  auto load_piece = [&](int p) {
+    const int e = g0 + (p / nch) * G;
+    const int c0 = (p % nch) * 32 * kSmallChunk;
+    const uint4* row = reinterpret_cast<const uint4*>(Wg + (int64_t)e * H);
+#pragma unroll
+    for (int u = 0; u < kSmallChunk; ++u) {
+      const int v = c0 + lane + 32 * u;
+      if (v < kv) gw[u] = __ldg(row + v);
+    }
+  };
+  if (pieces > 0) load_piece(0);
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  for (int i = threadIdx.x; i < Tn * kv; i += kRouterThreads) s_x[i] = xv[i];
+  __syncthreads();
+  const uint32_t ls_leader = tc::map_peer(tc::smem_u32(ls), 0);
+  float acc[kSmallTok];
+#pragma unroll
+  for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
+  for (int p = 0; p < pieces; ++p) {
+    const int e = g0 + (p / nch) * G;
+    const int c0 = (p % nch) * 32 * kSmallChunk;
+#pragma unroll
+    for (int u = 0; u < kSmallChunk; ++u) {
+      const int v = c0 + lane + 32 * u;
+      if (v < kv) {
+        float b[V];
+        Vec<bf16>::unpack(gw[u], b);
+#pragma unroll
+        for (int t = 0; t < kSmallTok; ++t) {
+          if (t < Tn) {
+            float a[V];
+            Vec<bf16>::unpack(s_x[t * kv + v], a);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[t] = fmaf(a[i], b[i], acc[t]);
+          }
+        }
+      }
+    }
+    if (p + 1 < pieces) load_piece(p + 1);
+    if (p % nch != nch - 1) continue;
+#pragma unroll
+    for (int t = 0; t < kSmallTok; ++t) {
+      if (t < Tn) {
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) tc::st_peer_f32(ls_leader + 4u * (uint32_t)(t * (E + 1) + e), v);
+      }
+      acc[t] = 0.f;
+    }
+  }
+  tc::cluster_sync();              // every score is in the leader's table
+  if (rank != 0) return;
+  for (int i = threadIdx.x; i < Tn * E; i += kRouterThreads) {
+    const int t = i / E, e = i % E;
+    float v = ls[t * (E + 1) + e] + (gate_bias ? gate_bias[e] : 0.f);
+    ls[t * (E + 1) + e] = v;
+    if (logits) logits[(int64_t)t * E + e] = v;
+  }
+  __syncthreads();
+  finish_tokens(ls, Tn, 0, E, K, inv_tau, ids, w, warp, kRouterWarps);
+  __syncthreads();
+  if (tile_hist) {
+    for (int i = threadIdx.x; i < Tn * K; i += kRouterThreads) {
+      const int id = ids[i];
+      if ((unsigned)id < (unsigned)E) atomicAdd(&s_hist[id], 1);   // no expert taken: NaN scores
+    }
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < E; e += kRouterThreads) {
+    if (psum_part) {
+      float sum = 0.f;
+      for (int t = 0; t < Tn; ++t) sum += ls[t * (E + 1) + e];
+      psum_part[e] = sum;
+    }
+    if (tile_hist) tile_hist[e] = s_hist[e];
   }
 }
 
@@ -180,7 +304,14 @@ __global__ void psum_reduce_kernel(const float* __restrict__ part, int64_t rows,
 
 int64_t router_partials(const Shape& s) { return (s.T + kRouterTok - 1) / kRouterTok; }
 
+bool router_small(const Shape& s) {
+  // the token rows and the score table fit one CTA's shared memory
+  return s.dtype == MOE_BF16 && s.T <= kSmallTok && s.E <= 256 && !(s.flags & MOE_FLAG_SIMT_ROUTER) &&
+         s.T * s.H * 2 + s.T * (s.E + 1) * 4 <= 200 * 1024;
+}
+
 int64_t router_partial_rows(const Shape& s) {
+  if (router_small(s)) return 1;
   return router_on_tensor_cores(s) ? (s.T + 127) / 128 : router_partials(s);
 }
 
@@ -188,6 +319,17 @@ cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const f
                           float* logits, int32_t* ids, float* w, float* psum_part, int* err,
                           cudaStream_t st, int32_t* tile_hist) {
   if (s.T == 0) return cudaSuccess;
+  if (router_small(s)) {
+    const int need = (s.E + kRouterWarps - 1) / kRouterWarps;
+    const int cl = need < kSmallMaxCta ? need : kSmallMaxCta;
+    const size_t smem = (size_t)s.T * s.H * sizeof(bf16) + (size_t)s.T * (s.E + 1) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(router_small_kernel, dim3((unsigned)cl), dim3(kRouterThreads), smem, st, (unsigned)cl,
+                         (const bf16*)x, (const bf16*)Wg, gate_bias, (int)s.T, s.H, s.E, s.K, s.inv_tau, logits,
+                         ids, w, psum_part, tile_hist);
+  }
   if (router_on_tensor_cores(s))
     return launch_router_tc(s, x, Wg, gate_bias, logits, ids, w, psum_part, tile_hist, err, st);
   const size_t smem = sizeof(float) * (kRouterTok * (kRouterKC + 1) + s.E * (kRouterKC + 1) +

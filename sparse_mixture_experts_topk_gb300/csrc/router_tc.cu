@@ -281,7 +281,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       if (j < K) {
         ids[t * K + j] = ti[j];
         w[t * K + j] = z[j] / zsel;
-        atomicAdd(&s_hist[ti[j]], 1);
+        if ((unsigned)ti[j] < (unsigned)E) atomicAdd(&s_hist[ti[j]], 1);   // no expert taken: NaN scores
       }
     }
   } else {

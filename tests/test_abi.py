@@ -59,6 +59,22 @@ def test_workspace_size_grows_with_shape(lib):
     assert b >= 16384 * (3584 + 2560) * 2
 
 
+def test_layer_launch_count(lib):
+    """The kernels one layer call issues, from the shape: router, dispatch
+    (one block for a small batch; else scan, scatter, gather, plus a
+    histogram pass when the router does not count its tiles), two expert
+    products, combine."""
+    prefill = moe.make_desc(8192, 3584, 32, 2, 2560)
+    assert moe.moe_layer_launches(prefill) == 1 + 3 + 2 + 1
+    f32 = moe.make_desc(4096, 256, 8, 2, 512, dtype=moe.MOE_F32)      # CUDA-core router: own histogram
+    assert moe.moe_layer_launches(f32) == 1 + 4 + 2 + 1
+    decode = moe.make_desc(8, 3584, 32, 2, 2560)
+    assert moe.moe_layer_launches(decode) == 1 + 1 + 2 + 1
+    assert moe.moe_layer_launches(moe.make_desc(0, 3584, 32, 2, 2560)) == 1
+    with pytest.raises(moe.MoeError):
+        moe.moe_layer_launches(moe.make_desc(8, 3584, 32, 9, 2560))
+
+
 @pytest.mark.parametrize("bad", [
     dict(K=0), dict(K=9), dict(E=1, K=2), dict(E=257), dict(H=12), dict(F=4), dict(T=-1),
     dict(dtype=7), dict(T=1 << 30, K=4), dict(temperature=float("nan")), dict(temperature=float("inf")),

@@ -239,16 +239,18 @@ def test_heavily_tied_scores_route_like_the_oracle():
         assert (srt[:, :-1] == srt[:, 1:]).any(axis=1).mean() > 0.9   # ties everywhere
 
 
-@pytest.mark.parametrize("kind", ["single", "pair"])
+@pytest.mark.parametrize("kind", ["single", "pair", "pair_rows"])
 @pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "ffn_bias", "cap_zipf_k4", "e256_k3", "one_token",
                                   "swiglu_ragged"])
 def test_expert_gemm_kernels_match_oracle(name, kind):
-    """Both tensor-core GEMM kernels (128x256 tiles per SM, 256x256 tiles per
-    SM pair) against the oracle, product by product, and the layer output."""
+    """The tensor-core GEMM kernels (128x256 tiles per SM; SM pairs with the
+    token rows on the MMA's N side, the default, or on its M side) against
+    the oracle, product by product, and the layer output."""
     w = SMALL[name]
     inp = W.generate(w)
     dev = Dev(inp)
-    flag = moe.MOE_FLAG_GEMM_SINGLE if kind == "single" else moe.MOE_FLAG_GEMM_PAIR
+    flag = {"single": moe.MOE_FLAG_GEMM_SINGLE, "pair": moe.MOE_FLAG_GEMM_PAIR,
+            "pair_rows": moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_GEMM_ROWS}[kind]
     flags = flag | moe.MOE_FLAG_NO_DECODE
     r = run_stages(dev, flags=flags)
     assert r["device_error"] == 0
