@@ -50,12 +50,16 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslo
 // expert e.  Cuts at the capacity and writes count, offs (exclusive prefix
 // of the kept counts, offs[E] = kept rows) and the dropped total; with
 // psum_part also the summed router probabilities and the load-balancing loss.
+// s_offs (nullable): also receives offs[0..E] in shared memory.  p_pre >= 0
+// (with psum_part set): this thread's probability sum, already added up in
+// row order by the caller.
 __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __restrict__ count,
                                               int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
                                               const float* __restrict__ psum_part, int64_t prows,
                                               float* __restrict__ psum, float* __restrict__ aux, int64_t Tn,
                                               int K, int32_t* __restrict__ count_copy,
-                                              int32_t* __restrict__ dropped_copy, int32_t* __restrict__ sched) {
+                                              int32_t* __restrict__ dropped_copy, int32_t* __restrict__ sched,
+                                              int* s_offs = nullptr, float p_pre = -1.f) {
   __shared__ int sk[256];
   __shared__ int sd[256];
   __shared__ float sa[256];
@@ -78,6 +82,10 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
     if (count_copy) count_copy[e] = run;
     offs[e] = sk[e] - kept;
     if (e == E - 1) offs[E] = sk[e];
+    if (s_offs) {
+      s_offs[e] = sk[e] - kept;
+      if (e == E - 1) s_offs[E] = sk[e];
+    }
   }
   if (e == 255) {
     if (dropped) *dropped = sd[255];
@@ -85,8 +93,9 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
   }
   if (sched && e < 2) sched[e] = 0;   // the expert GEMMs that follow take tiles from these
   if (psum_part) {
-    float p = 0.f;
-    if (e < E) {
+    float p = p_pre;
+    if (e < E && p_pre < 0.f) {
+      p = 0.f;
       // rows added in order; eight loads in flight
       int64_t r = 0;
       for (; r + 8 <= prows; r += 8) {
@@ -97,8 +106,8 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
         for (int i = 0; i < 8; ++i) p += v[i];
       }
       for (; r < prows; ++r) p += psum_part[r * E + e];
-      if (psum) psum[e] = p;
     }
+    if (e < E && psum) psum[e] = p;
     if (aux) {
       // E * sum_i (count_i / (T K)) * (psum_i / T), reduced in a fixed order
       sa[e] = (e < E && Tn > 0) ? ((float)run / (float)(Tn * K)) * (p / (float)Tn) : 0.f;
@@ -114,22 +123,40 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
 
 // One block; thread e owns expert e (E <= 256).  With `staged`, the
 // [nblk, E] histogram is first copied to shared memory with coalesced loads
-// and scanned there.
+// and scanned there; with `staged_p`, the [prows, E] probability partials
+// are copied in the same pass (so their loads overlap) and summed there.
 __global__ void __launch_bounds__(256)
 dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, int C, int staged,
-                     int32_t* __restrict__ blk_base, int32_t* __restrict__ count,
+                     int staged_p, int32_t* __restrict__ blk_base, int32_t* __restrict__ count,
                      int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
                      const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
                      float* __restrict__ aux, int64_t Tn, int K, int32_t* __restrict__ count_copy,
                      int32_t* __restrict__ dropped_copy, int32_t* __restrict__ sched) {
-  extern __shared__ int sh[];          // [nblk, E] when staged
+  extern __shared__ int sh[];          // [nblk, E] when staged, then [prows, E] floats when staged_p
   pdl_enter();
   const int e = threadIdx.x;
   const int64_t n = nblk * E;
+  const int64_t np = staged_p ? prows * E : 0;
+  float* sp = reinterpret_cast<float*>(sh + (staged ? n : 0));
+  if (staged || staged_p) {
+    const int64_t m = (staged ? n : 0) > np ? (staged ? n : 0) : np;
+    for (int64_t i = threadIdx.x; i < m; i += 256) {
+      int h = 0;
+      float q = 0.f;
+      if (staged && i < n) h = blk_hist[i];
+      if (i < np) q = psum_part[i];
+      if (staged && i < n) sh[i] = h;
+      if (i < np) sp[i] = q;
+    }
+    __syncthreads();
+  }
+  float p_pre = -1.f;
+  if (staged_p && e < E) {
+    p_pre = 0.f;
+    for (int64_t r = 0; r < prows; ++r) p_pre += sp[r * E + e];   // rows in order
+  }
   int run = 0;
   if (staged) {
-    for (int64_t i = threadIdx.x; i < n; i += 256) sh[i] = blk_hist[i];
-    __syncthreads();
     if (e < E) {
       for (int64_t b = 0; b < nblk; ++b) {
         const int h = sh[b * E + e];
@@ -159,50 +186,60 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
     }
   }
   finish_counts(run, E, C, count, offs, dropped, psum_part, prows, psum, aux, Tn, K, count_copy,
-                dropped_copy, sched);
+                dropped_copy, sched, nullptr, p_pre);
 }
 
-// Stable placement of slots [s0, s1): running[e] (shared) holds the rank
-// the next slot of expert e takes and is advanced past the range.  Ranks
-// within each 256-slot chunk come from a warp match plus per-warp counts.
+// One 256-slot chunk of the stable placement: this thread holds slot s
+// (valid or not) routed to expert e (-1: none or out of range).
+// running[e] (shared) is the rank the chunk's first slot of expert e takes
+// and is advanced past the chunk; ranks within the chunk come from a warp
+// match plus per-warp counts.  s_src (nullable) gets a shared copy of src.
+__device__ __forceinline__ void scatter_chunk(int e, int64_t s, bool valid, int E, int C, int (*wcnt)[256],
+                                              int* running, const int32_t* offs, int32_t* __restrict__ pos,
+                                              int32_t* __restrict__ src, int* s_src) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < kDispWarps * 256; i += kDispThreads) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const unsigned below = peers & lanemask_lt();
+  if (e >= 0 && below == 0) wcnt[warp][e] = __popc(peers);
+  __syncthreads();
+  if (valid) {
+    int p = -1;
+    if (e >= 0) {
+      int r = running[e] + __popc(below);
+      for (int w2 = 0; w2 < warp; ++w2) r += wcnt[w2][e];
+      if (C <= 0 || r < C) {
+        p = offs[e] + r;
+        src[p] = (int32_t)s;
+        if (s_src) s_src[p] = (int)s;
+      }
+    }
+    pos[s] = p;
+  }
+  __syncthreads();
+  for (int e2 = tid; e2 < E; e2 += kDispThreads) {
+    int add = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kDispWarps; ++w2) add += wcnt[w2][e2];
+    running[e2] += add;
+  }
+  __syncthreads();
+}
+
+// Stable placement of slots [s0, s1), their expert ids read from ids.
 __device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ ids, int64_t s0, int64_t s1, int E,
                                               int C, int* running, const int32_t* offs,
                                               int32_t* __restrict__ pos, int32_t* __restrict__ src) {
   __shared__ int wcnt[kDispWarps][256];
-  const int tid = threadIdx.x, warp = tid >> 5;
   for (int64_t c0 = s0; c0 < s1; c0 += kDispThreads) {
-    for (int i = tid; i < kDispWarps * 256; i += kDispThreads) (&wcnt[0][0])[i] = 0;
-    __syncthreads();
-    const int64_t s = c0 + tid;
+    const int64_t s = c0 + threadIdx.x;
     int e = -1;
     if (s < s1) {
       e = ids[s];
       if (e < 0 || e >= E) e = -1;   // reported by the histogram pass
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const unsigned below = peers & lanemask_lt();
-    if (e >= 0 && below == 0) wcnt[warp][e] = __popc(peers);
-    __syncthreads();
-    if (s < s1) {
-      int p = -1;
-      if (e >= 0) {
-        int r = running[e] + __popc(below);
-        for (int w2 = 0; w2 < warp; ++w2) r += wcnt[w2][e];
-        if (C <= 0 || r < C) {
-          p = offs[e] + r;
-          src[p] = (int32_t)s;
-        }
-      }
-      pos[s] = p;
-    }
-    __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += kDispThreads) {
-      int add = 0;
-#pragma unroll
-      for (int w2 = 0; w2 < kDispWarps; ++w2) add += wcnt[w2][e2];
-      running[e2] += add;
-    }
-    __syncthreads();
+    scatter_chunk(e, s, s < s1, E, C, wcnt, running, offs, pos, src, nullptr);
   }
 }
 
@@ -219,7 +256,9 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C
 }
 
 // x_perm[r] = x[src[r] / K] for r in [0, rows), one warp per row; warps
-// w0, w0 + nw, ... of the caller's numbering.
+// w0, w0 + nw, ... of the caller's numbering.  x_perm is stored evict-first:
+// it is larger than what the first expert product could find in L2 anyway,
+// and x (read once per slot) then stays there for its second read.
 __device__ __forceinline__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ src,
                                             int64_t rows, int K, int vec_per_row, uint4* __restrict__ x_perm,
                                             int64_t w0, int64_t nw) {
@@ -231,9 +270,9 @@ __device__ __forceinline__ void gather_rows(const uint4* __restrict__ x, const i
     int v = lane;
     for (; v + 96 < vec_per_row; v += 128) {
       const uint4 u0 = a[v], u1 = a[v + 32], u2 = a[v + 64], u3 = a[v + 96];
-      b[v] = u0; b[v + 32] = u1; b[v + 64] = u2; b[v + 96] = u3;
+      __stcs(b + v, u0); __stcs(b + v + 32, u1); __stcs(b + v + 64, u2); __stcs(b + v + 96, u3);
     }
-    for (; v < vec_per_row; v += 32) b[v] = a[v];
+    for (; v < vec_per_row; v += 32) __stcs(b + v, a[v]);
   }
 }
 
@@ -249,6 +288,12 @@ dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ 
 
 // A small batch in one block: histogram, counts, stable placement and the
 // row gather, with the same arithmetic and results as the four-kernel path.
+// Each thread reads its (at most 4) slots' expert ids and its expert's
+// probability partials once, up front; offsets and src stay in shared
+// memory, so the only dependent global reads are those and the x rows.
+constexpr int kSmallChunks = 4;
+constexpr int kSmallSlots = kSmallChunks * kDispThreads;
+
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int32_t* __restrict__ count,
                       int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
@@ -259,25 +304,58 @@ dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, 
                       int32_t* __restrict__ sched) {
   __shared__ int hist[256];
   __shared__ int s_offs[257];
+  __shared__ int s_src[kSmallSlots];
+  __shared__ int wcnt[kDispWarps][256];
   pdl_enter();
   const int e = threadIdx.x;
   hist[e] = 0;
+  int my[kSmallChunks];
+#pragma unroll
+  for (int c = 0; c < kSmallChunks; ++c) {
+    const int64_t s = (int64_t)c * kDispThreads + threadIdx.x;
+    my[c] = s < S ? ids[s] : -1;
+  }
+  float p = -1.f;
+  if (psum_part && e < E) {
+    p = 0.f;
+    for (int64_t r = 0; r < prows; ++r) p += psum_part[r * E + e];
+  }
   __syncthreads();
-  for (int64_t s = threadIdx.x; s < S; s += kDispThreads) {
-    const int v = ids[s];
-    if (v >= 0 && v < E) atomicAdd(&hist[v], 1);
-    else set_error(err, kDevBadIndex);
+#pragma unroll
+  for (int c = 0; c < kSmallChunks; ++c) {
+    const int64_t s = (int64_t)c * kDispThreads + threadIdx.x;
+    if (s < S) {
+      if (my[c] >= 0 && my[c] < E) atomicAdd(&hist[my[c]], 1);
+      else set_error(err, kDevBadIndex);
+    }
+    if (my[c] < 0 || my[c] >= E) my[c] = -1;
   }
   __syncthreads();
   const int run = (e < E) ? hist[e] : 0;
   finish_counts(run, E, C, count, offs, dropped, psum_part, prows, psum, aux, Tn, K, count_copy, dropped_copy,
-                sched);
-  __syncthreads();   // offs written by other threads of this block
-  for (int i = threadIdx.x; i <= E; i += kDispThreads) s_offs[i] = offs[i];
+                sched, s_offs, p);
   hist[e] = 0;       // reused as the running rank
   __syncthreads();
-  scatter_slots(ids, 0, S, E, C, hist, s_offs, pos, src);
-  if (x) gather_rows(x, src, s_offs[E], K, vec_per_row, x_perm, threadIdx.x >> 5, kDispWarps);
+#pragma unroll
+  for (int c = 0; c < kSmallChunks; ++c) {
+    const int64_t s0 = (int64_t)c * kDispThreads;
+    if (s0 < S) scatter_chunk(my[c], s0 + threadIdx.x, s0 + threadIdx.x < S, E, C, wcnt, hist, s_offs, pos, src,
+                              s_src);
+  }
+  if (x) {
+    const int rows = s_offs[E];
+    const int lane = threadIdx.x & 31;
+    for (int r = threadIdx.x >> 5; r < rows; r += kDispWarps) {
+      const uint4* a = x + (int64_t)(s_src[r] / K) * vec_per_row;
+      uint4* b = x_perm + (int64_t)r * vec_per_row;
+      int v = lane;
+      for (; v + 96 < vec_per_row; v += 128) {
+        const uint4 u0 = a[v], u1 = a[v + 32], u2 = a[v + 64], u3 = a[v + 96];
+        b[v] = u0; b[v + 32] = u1; b[v + 64] = u2; b[v + 96] = u3;
+      }
+      for (; v < vec_per_row; v += 32) b[v] = a[v];
+    }
+  }
 }
 
 }  // namespace
@@ -298,7 +376,7 @@ int64_t dispatch_blocks(const Shape& s) {
 bool dispatch_small(const Shape& s) {
   // one block wins while its serial passes stay a few microseconds: up to
   // four 256-slot chunks and 256 KB of rows for its eight warps to copy
-  return s.S() <= 4 * kDispThreads && s.S() * s.H * s.esize() <= 256 * 1024;
+  return s.S() <= kSmallSlots && s.S() * s.H * s.esize() <= 256 * 1024;
 }
 
 cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
@@ -325,14 +403,17 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
     e = launch_kernel(dispatch_hist_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
                       bslots, o.blk_hist, err);
   const size_t sm = (size_t)nblk * s.E * sizeof(int);
+  const int64_t prows = o.psum_part ? router_partial_rows(s) : (int64_t)0;
+  const size_t smp = (size_t)prows * s.E * sizeof(float);
   const int staged = sm <= 96 * 1024 ? 1 : 0;
-  if (e == cudaSuccess && staged && sm > 48 * 1024)
-    e = cudaFuncSetAttribute(dispatch_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  const int staged_p = (o.psum_part && (staged ? sm : 0) + smp <= 192 * 1024) ? 1 : 0;
+  const size_t smem = (staged ? sm : 0) + (staged_p ? smp : 0);
+  if (e == cudaSuccess && smem > 48 * 1024)
+    e = cudaFuncSetAttribute(dispatch_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
-    e = launch_kernel(dispatch_scan_kernel, dim3(1), dim3(256), staged ? sm : 0, st, 1,
-                      (const int32_t*)o.blk_hist, nblk, s.E, s.C, staged, o.blk_base, o.count, o.offs,
-                      o.dropped, o.psum_part, o.psum_part ? router_partial_rows(s) : (int64_t)0, o.psum, o.aux,
-                      s.T, s.K, o.count_copy, o.dropped_copy, o.sched);
+    e = launch_kernel(dispatch_scan_kernel, dim3(1), dim3(256), smem, st, 1, (const int32_t*)o.blk_hist, nblk,
+                      s.E, s.C, staged, staged_p, o.blk_base, o.count, o.offs, o.dropped, o.psum_part, prows,
+                      o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy, o.sched);
   if (e == cudaSuccess && nblk > 0)
     e = launch_kernel(dispatch_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
                       s.C, bslots, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos, o.src);

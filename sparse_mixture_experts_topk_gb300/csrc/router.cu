@@ -39,9 +39,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 // time by a warp arg-max with ties to the lower index; the token's ids and
 // weights are written, and its ls row is replaced by the full softmax (for
 // the load-balancing sums).
+// s_hist (nullable, shared): counts of the chosen experts.
 __device__ __forceinline__ void finish_tokens(float* ls, int nt, int64_t t0, int E, int K, float inv_tau,
                                               int32_t* __restrict__ ids, float* __restrict__ w, int warp0,
-                                              int nwarps) {
+                                              int nwarps, int* s_hist = nullptr) {
   const int lane = threadIdx.x & 31;
   for (int tt = warp0; tt < nt; tt += nwarps) {
     float v[8];
@@ -95,6 +96,7 @@ __device__ __forceinline__ void finish_tokens(float* ls, int nt, int64_t t0, int
       for (int j = 0; j < K; ++j) {
         ids[t * K + j] = sel_id[j];
         w[t * K + j] = sel_z[j] / zsel;
+        if (s_hist && (unsigned)sel_id[j] < (unsigned)E) atomicAdd(&s_hist[sel_id[j]], 1);   // NaN scores: none
       }
     }
     // full-softmax probabilities for the load-balancing statistics
@@ -183,14 +185,40 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
 // all.  Warp g of the cluster owns gate rows g, g + G, ... (G = its warps);
 // each lane loads kSmallChunk 16-byte vectors of a row in one go, issued
 // before the token rows are staged in shared memory, and dots them with every
-// staged token.  The T scores of a row go straight into the leader CTA's
-// score table over distributed shared memory; after one cluster barrier the
-// leader finishes each token (bias, top-k, weights), sums the probabilities
-// per expert in token order into psum_part[0] and counts the chosen experts
-// into tile_hist[0] (the layer's single 128-token tile).
+// staged token (a body sized for the batch, so the hot loop stays small).  The T scores of a row go straight
+// into the leader CTA's score table over distributed shared memory; after one
+// cluster barrier the leader finishes each token (bias, top-k, weights),
+// counts the chosen experts as it picks them into tile_hist[0] (the layer's
+// single 128-token tile) and sums the probabilities per expert in token order
+// into psum_part[0].
 constexpr int kSmallTok = 16;
 constexpr int kSmallChunk = 8;
 constexpr int kSmallMaxCta = 8;
+
+// acc[t] += gate piece (gw, vectors c0 + lane + 32 u) . token row t, t < Tn <= MR
+template <int MR>
+__device__ __forceinline__ void small_dot(const uint4 (&gw)[kSmallChunk], const uint4* s_x, int kv, int c0,
+                                          int Tn, float (&acc)[kSmallTok]) {
+  constexpr int V = Vec<bf16>::N;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < kSmallChunk; ++u) {
+    const int v = c0 + lane + 32 * u;
+    if (v < kv) {
+      float b[V];
+      Vec<bf16>::unpack(gw[u], b);
+#pragma unroll
+      for (int t = 0; t < MR; ++t) {
+        if (t < Tn) {
+          float a[V];
+          Vec<bf16>::unpack(s_x[t * kv + v], a);
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[t] = fmaf(a[i], b[i], acc[t]);
+        }
+      }
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kRouterThreads)
 router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wg,
@@ -232,23 +260,11 @@ router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wg,
   for (int p = 0; p < pieces; ++p) {
     const int e = g0 + (p / nch) * G;
     const int c0 = (p % nch) * 32 * kSmallChunk;
-#pragma unroll
-    for (int u = 0; u < kSmallChunk; ++u) {
-      const int v = c0 + lane + 32 * u;
-      if (v < kv) {
-        float b[V];
-        Vec<bf16>::unpack(gw[u], b);
-#pragma unroll
-        for (int t = 0; t < kSmallTok; ++t) {
-          if (t < Tn) {
-            float a[V];
-            Vec<bf16>::unpack(s_x[t * kv + v], a);
-#pragma unroll
-            for (int i = 0; i < V; ++i) acc[t] = fmaf(a[i], b[i], acc[t]);
-          }
-        }
-      }
-    }
+    if (Tn <= 1) small_dot<1>(gw, s_x, kv, c0, Tn, acc);
+    else if (Tn <= 2) small_dot<2>(gw, s_x, kv, c0, Tn, acc);
+    else if (Tn <= 4) small_dot<4>(gw, s_x, kv, c0, Tn, acc);
+    else if (Tn <= 8) small_dot<8>(gw, s_x, kv, c0, Tn, acc);
+    else small_dot<kSmallTok>(gw, s_x, kv, c0, Tn, acc);
     if (p + 1 < pieces) load_piece(p + 1);
     if (p % nch != nch - 1) continue;
 #pragma unroll
@@ -271,15 +287,8 @@ router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wg,
     if (logits) logits[(int64_t)t * E + e] = v;
   }
   __syncthreads();
-  finish_tokens(ls, Tn, 0, E, K, inv_tau, ids, w, warp, kRouterWarps);
+  finish_tokens(ls, Tn, 0, E, K, inv_tau, ids, w, warp, kRouterWarps, s_hist);
   __syncthreads();
-  if (tile_hist) {
-    for (int i = threadIdx.x; i < Tn * K; i += kRouterThreads) {
-      const int id = ids[i];
-      if ((unsigned)id < (unsigned)E) atomicAdd(&s_hist[id], 1);   // no expert taken: NaN scores
-    }
-    __syncthreads();
-  }
   for (int e = threadIdx.x; e < E; e += kRouterThreads) {
     if (psum_part) {
       float sum = 0.f;

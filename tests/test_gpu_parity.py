@@ -45,6 +45,16 @@ SMALL = {
     # distinct-expert construction scales x by 64, and SiLU(g) * u would square
     # that into outputs whose bf16 storage alone exceeds the 2e-2 bound
     "swiglu_decode": W.small("swiglu_decode", T=4, H=512, E=16, K=2, F=200, act="swiglu"),
+    # one-block dispatch: capacity drops; exactly its slot limit (1024 slots,
+    # 256 KB of rows); one slot pair past it (multi-block path)
+    "small_cap": W.small("small_cap", T=100, H=128, E=8, K=2, F=64,
+                         capacity=W.capacity_ceil(100, 8, 2) // 2, gate_bias="zipf"),
+    "slots_1024": W.small("slots_1024", T=512, H=128, E=8, K=2, F=64),
+    "slots_1026": W.small("slots_1026", T=513, H=128, E=8, K=2, F=64),
+    # small-batch router with the widest cluster (8 CTAs, 4 gate rows a warp)
+    "tiny_e256_k8": W.small("tiny_e256_k8", T=5, H=64, E=256, K=8, F=64),
+    # every token picks both experts: 16-row segments, the largest streaming body
+    "decode16_all": W.small("decode16_all", T=16, H=256, E=2, K=2, F=128),
 }
 
 
