@@ -251,7 +251,7 @@ def run_ours(args, w: W.Workload):
     aux = torch.empty(1, device="cuda")
     count = torch.empty(w.E, dtype=torch.int32, device="cuda")
     dropped = torch.empty(1, dtype=torch.int32, device="cuda")
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -262,7 +262,7 @@ def run_ours(args, w: W.Workload):
     t_w = time.time()
     i = 0
     while i < args.warmup or time.time() - t_w < args.min_warmup_s:
-        flush.zero_()
+        flush()
         step()
         i += 1
         if i % 20 == 0:
@@ -286,12 +286,12 @@ def run_ours(args, w: W.Workload):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
-        flush.zero_()                     # L2 flushed between timed steps
+        flush()                           # L2 flushed between timed steps
         ev_a[k][0].record()
         step()
         ev_a[k][1].record()
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         moe.moe_profile_events(evs[k])
         step()
     moe.moe_profile_events(None)
@@ -359,7 +359,8 @@ def run_ours(args, w: W.Workload):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
         "data": "synthetic",
         "config": {"workload": describe(w), "global_batch_tokens": world * w.T,
-                   "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write)",
+                   "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write, then "
+                         f"{FLUSH_BYTES >> 20} MB read so the written lines are back in DRAM)",
                    "parallelism": f"replicas x{world}", "kept_rows": rows, "used_experts": used,
                    "gemm": args.gemm},
         "roofline": roof,
@@ -379,6 +380,21 @@ def run_ours(args, w: W.Workload):
         dist.destroy_process_group()
 
 
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2, which evicts the
+    layer's data, then read a second one, so that the written lines reach
+    DRAM before the next step instead of being written back while the
+    step's first kernels run."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(FLUSH_BYTES // 8, dtype=torch.int64, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
+
 def run_e2e(args, moe, torch, w, d, x, Wg, gb, W1, W2, aux, flush, stream, world, dist):
     dh = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity, d.dtype, d.flags | moe.MOE_FLAG_HOST_IO,
                        w.temperature)
@@ -391,7 +407,7 @@ def run_e2e(args, moe, torch, w, d, x, Wg, gb, W1, W2, aux, flush, stream, world
     n = max(3, min(args.steps, 50))
     tot = 0.0
     for _ in range(n):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         a = time.perf_counter()
         moe.moe_layer_forward(dh, xh, Wg, gb, W1, None, W2, None, outh, aux, None, None, wsh)
