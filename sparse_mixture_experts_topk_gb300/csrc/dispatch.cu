@@ -139,21 +139,44 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
   const int64_t np = staged_p ? prows * E : 0;
   float* sp = reinterpret_cast<float*>(sh + (staged ? n : 0));
   if (staged || staged_p) {
-    const int64_t m = (staged ? n : 0) > np ? (staged ? n : 0) : np;
-    for (int64_t i = threadIdx.x; i < m; i += 256) {
-      int h = 0;
-      float q = 0.f;
-      if (staged && i < n) h = blk_hist[i];
-      if (i < np) q = psum_part[i];
-      if (staged && i < n) sh[i] = h;
-      if (i < np) sp[i] = q;
+    // eight loads of each kind in flight per thread before any store
+    const int64_t nh = staged ? n : 0;
+    const int64_t m = nh > np ? nh : np;
+    for (int64_t i0 = threadIdx.x; i0 < m; i0 += 256 * 8) {
+      int h[8];
+      float q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + 256 * u;
+        h[u] = i < nh ? blk_hist[i] : 0;
+        q[u] = i < np ? psum_part[i] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + 256 * u;
+        if (i < nh) sh[i] = h[u];
+        if (i < np) sp[i] = q[u];
+      }
     }
     __syncthreads();
   }
+  // probability sums: G = 256 / E thread groups each add every G-th row (in
+  // row order), then thread e adds the G group sums in group order
+  __shared__ float s_pg[256];
   float p_pre = -1.f;
-  if (staged_p && e < E) {
-    p_pre = 0.f;
-    for (int64_t r = 0; r < prows; ++r) p_pre += sp[r * E + e];   // rows in order
+  if (staged_p) {
+    const int G = 256 / E;
+    const int g = threadIdx.x / E, ee = threadIdx.x % E;
+    if (g < G) {
+      float a = 0.f;
+      for (int64_t r = g; r < prows; r += G) a += sp[r * E + ee];
+      s_pg[g * E + ee] = a;
+    }
+    __syncthreads();
+    if (e < E) {
+      p_pre = 0.f;
+      for (int gg = 0; gg < G; ++gg) p_pre += s_pg[gg * E + e];
+    }
   }
   int run = 0;
   if (staged) {

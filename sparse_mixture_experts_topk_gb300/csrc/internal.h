@@ -70,6 +70,7 @@ int64_t router_partials(const Shape& s);
 bool router_small(const Shape& s);   // one-cluster router for decode-sized bf16 batches
 int64_t router_partial_rows(const Shape& s);
 bool router_on_tensor_cores(const Shape& s);
+int router_tc_split(const Shape& s);   // CTAs the tensor-core router splits the hidden dimension over (1 or 2)
 // tile_hist (nullable): [ceil(T/128), E] count of each 128-token tile's
 // chosen experts, in slot order blocks of 128*K slots.
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,

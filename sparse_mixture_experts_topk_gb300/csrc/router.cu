@@ -321,7 +321,7 @@ bool router_small(const Shape& s) {
 
 int64_t router_partial_rows(const Shape& s) {
   if (router_small(s)) return 1;
-  return router_on_tensor_cores(s) ? (s.T + 127) / 128 : router_partials(s);
+  return router_on_tensor_cores(s) ? (s.T + 127) / 128 * router_tc_split(s) : router_partials(s);
 }
 
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,

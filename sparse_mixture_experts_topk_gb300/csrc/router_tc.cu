@@ -16,15 +16,18 @@
 //   * one thread issues tcgen05.mma M=128, N=E rounded up to 16, K=16 into
 //     TMEM (fp32);
 //   * when the tiles fill less than half the GPU, the hidden dimension is
-//     split over a CTA pair (a 2-CTA cluster); each CTA copies its partial scores
-//     TMEM -> shared memory, and CTA rank 0 adds the others' partials over
-//     distributed shared memory in rank order (deterministic);
-//   * rank 0 then finishes each token in one thread: bias, top-k by a
-//     branch-free insertion into k registers, softmax statistics, weights; the probabilities of the
-//     tile are summed per expert in token order into psum_part[tile], and the
-//     tile's chosen experts are counted into tile_hist[tile] (the dispatch
-//     histogram of the tile's 128*k slots, so the layer needs no separate
-//     histogram pass).
+//     split over a CTA pair (a 2-CTA cluster); each CTA copies its partial
+//     scores TMEM -> shared memory (a sum of two partials does not depend on
+//     their order, so either CTA may add them);
+//   * each CTA of the pair then finishes half of the tile's tokens, one
+//     thread per token: the two partial scores added (over distributed
+//     shared memory), bias, top-k by a branch-free insertion into k
+//     registers, softmax statistics, weights; its tokens' probabilities are
+//     summed per expert in token order into psum_part[tile * ks + rank], and
+//     the tile's chosen experts are counted into tile_hist[tile] (the
+//     dispatch histogram of the tile's 128*k slots, so the layer needs no
+//     separate histogram pass; the peer's counts reach the leader by a
+//     distributed shared-memory reduction).
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the error word, skips the remaining work, still meets both cluster
 // barriers, frees TMEM and returns.
@@ -197,43 +200,42 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, tmem_cols);
   }
+  // this CTA finishes the tile's rows [h0, h1); with a pair, each of the two
+  // adds the other's partial scores of its rows (ks <= 2: the sum of two
+  // partials is the same in either order)
+  const int h0 = (int)rank * (kTok / ks), h1 = h0 + kTok / ks;
+  const bool mine_row = row >= h0 && row < h1;
   if (ks > 1) {
-    tc::cluster_sync();            // every rank's partial is in its shared memory
-    if (rank == 0) {
-      // own + rank 1 + rank 2 + ... per score, in that order; 16 remote loads in flight
-      const uint32_t mine = tc::smem_u32(part + row * ld);
-      for (int r = 1; r < ks; ++r) {
-        const uint32_t peer = tc::map_peer(mine, (uint32_t)r);
-        for (int e0 = 0; e0 < E; e0 += 16) {
-          float v[16];
+    tc::cluster_sync();            // both partials are in shared memory
+    if (mine_row) {
+      const uint32_t peer = tc::map_peer(tc::smem_u32(part + row * ld), rank ^ 1u);
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        float v[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = (e0 + j < E) ? tc::ld_peer_f32(peer + 4u * (e0 + j)) : 0.f;
+        for (int j = 0; j < 32; ++j) v[j] = (e0 + j < E) ? tc::ld_peer_f32(peer + 4u * (e0 + j)) : 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (e0 + j < E) part[row * ld + e0 + j] += v[j];
-        }
+        for (int j = 0; j < 32; ++j)
+          if (e0 + j < E) part[row * ld + e0 + j] += v[j];
       }
     }
-    tc::cluster_sync();            // peers keep their shared memory until rank 0 has read it
   }
-  if (rank != 0) return;
 
   // ------------------------------------------------------------ per token
   const int64_t t = t0 + row;
   float* lr = part + row * ld;
-  if (t < Tn) {
+  const bool live = mine_row && t < Tn;
+  if (live) {
     for (int e = 0; e < E; ++e) lr[e] += gate_bias ? gate_bias[e] : 0.f;
   }
   __syncthreads();
   if (logits) {
     const int64_t nt = (Tn - t0) < kTok ? (Tn - t0) : kTok;
-    for (int i = threadIdx.x; i < nt * E; i += kThreads) {
-      const int rr = i / E, e = i % E;
-      logits[(t0 + rr) * E + e] = part[rr * ld + e];
+    for (int i = threadIdx.x; i < (h1 - h0) * E; i += kThreads) {
+      const int rr = h0 + i / E, e = i % E;
+      if (rr < nt) logits[(t0 + rr) * E + e] = part[rr * ld + e];
     }
   }
-  __syncthreads();
-  if (t < Tn) {
+  if (live) {
     // the k largest so far in (score descending, index ascending) order; a
     // candidate bubbles down the list and swaps with every held entry it
     // precedes in that order (empty slots hold -inf and the largest index).
@@ -284,21 +286,34 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         if ((unsigned)ti[j] < (unsigned)E) atomicAdd(&s_hist[ti[j]], 1);   // no expert taken: NaN scores
       }
     }
-  } else {
+  } else if (mine_row) {
     for (int e = 0; e < E; ++e) lr[e] = 0.f;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kThreads) {
     if (psum_part) {
-      float s = 0.f;
-      for (int rr = 0; rr < kTok; ++rr) s += part[rr * ld + e];
-      psum_part[tile * E + e] = s;
+      float sum = 0.f;
+      for (int rr = h0; rr < h1; ++rr) sum += part[rr * ld + e];
+      psum_part[(tile * ks + rank) * E + e] = sum;
     }
-    if (tile_hist) tile_hist[tile * E + e] = s_hist[e];
+    if (tile_hist && rank != 0)
+      tc::red_peer_add_u32(tc::map_peer(tc::smem_u32(&s_hist[e]), 0), (uint32_t)s_hist[e]);
   }
+  if (ks > 1) tc::cluster_sync();  // the peer's counts have reached the leader; neither leaves early
+  if (tile_hist && rank == 0)
+    for (int e = threadIdx.x; e < E; e += kThreads) tile_hist[tile * E + e] = s_hist[e];
 }
 
 }  // namespace
+
+// The hidden dimension is split over a CTA pair when that still fits one
+// wave (wider splits measured slower: cluster scheduling and the reduction;
+// the pair epilogue also relies on at most two partials).
+int router_tc_split(const Shape& s) {
+  const int64_t tiles = (s.T + kTok - 1) / kTok;
+  const int nk = (s.H + kBK - 1) / kBK;
+  return (tiles * 2 <= sm_count() && nk >= 2) ? 2 : 1;
+}
 
 bool router_on_tensor_cores(const Shape& s) {
   return s.dtype == MOE_BF16 && s.H >= kBK && s.E <= 256 && !(s.flags & MOE_FLAG_SIMT_ROUTER);
@@ -308,11 +323,8 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, cons
                              float* logits, int32_t* ids, float* w, float* psum_part,
                              int32_t* tile_hist, int* err, cudaStream_t st) {
   const int64_t tiles = (s.T + kTok - 1) / kTok;
-  const int nk = (s.H + kBK - 1) / kBK;
   const int sms = sm_count();
-  // split the hidden dimension over a CTA pair when that still fits one wave
-  // (wider splits measured slower: cluster scheduling and the reduction)
-  const int ks = (tiles * 2 <= sms && nk >= 2) ? 2 : 1;
+  const int ks = router_tc_split(s);
   const int per_sm = (int)((tiles * ks + sms - 1) / sms);
   const RouterCfg c = router_cfg(s.E, per_sm);
   CUtensorMap mx, mg;

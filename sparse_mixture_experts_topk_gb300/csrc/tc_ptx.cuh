@@ -207,6 +207,11 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
 __device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+// Atomic add into a cluster peer's shared memory (relaxed; visible to it
+// after the next cluster barrier).
+__device__ __forceinline__ void red_peer_add_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_peer_u64(uint32_t addr, unsigned long long v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
