@@ -45,12 +45,17 @@ STAGES = ["router", "dispatch", "ffn_first", "ffn_second", "combine"]
 
 
 def peaks():
+    """HBM copy GB/s, bf16 TFLOP/s burst and sustained, and where they come
+    from.  The expert GEMMs run inside a loop of layer steps held under load
+    for seconds (the power cap active), so their roofline uses the sustained
+    bf16 figure; the burst fraction is reported beside it."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        burst = float(d["bf16_tflops"])
+        return float(d["hbm_gbs"]), burst, float(d.get("bf16_tflops_sustained", burst)), "measured"
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 def describe(w: W.Workload) -> str:
@@ -322,7 +327,7 @@ def run_ours(args, w: W.Workload):
             dist.destroy_process_group()
         return
 
-    hbm, tflops, src = peaks()
+    hbm, tflops_burst, tflops, src = peaks()
     work = work_counts(w, rows, used)
     value = world * w.T * args.steps / (total_ms / 1e3)
     f1, f2 = stage_ms["ffn_first"], stage_ms["ffn_second"]
@@ -340,8 +345,9 @@ def run_ours(args, w: W.Workload):
         traffic = ncu_traffic(w.name)
         roof = {"kernel": f"expert grouped GEMM ({dom})", "bound": "tensor", "achieved": achieved,
                 "peak": tflops, "unit": "TFLOP/s", "frac": achieved / tflops,
-                "peak_source": f"{src} bf16 (burst)", "traffic": traffic.get(dom) if traffic else None,
-                "algorithmic_flops_per_launch": flops[dom]}
+                "peak_source": f"{src} bf16 (sustained: timed inside a seconds-long loop of layer steps)",
+                "frac_of_burst_peak": achieved / tflops_burst, "burst_peak": tflops_burst,
+                "traffic": traffic.get(dom) if traffic else None, "algorithmic_flops_per_launch": flops[dom]}
     stages = {}
     for name in STAGES:
         ms = stage_ms[name]

@@ -17,7 +17,8 @@
 //   3. scatter: per block, the stable rank of each slot among the block's
 //               slots of the same expert (warp match + per-warp counts), so
 //               rank = block base + in-block rank; kept iff rank < capacity;
-//   4. gather:  x_perm[r] = x[src[r] / K], one warp per row, 16-byte vectors.
+//   4. gather:  x_perm[pos[t K + j]] = x[t], one warp per token: each x row
+//               is read once and written to its kept slots' rows.
 #include "common.cuh"
 #include "internal.h"
 
@@ -278,35 +279,46 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C
   scatter_slots(ids, s0, s1, E, C, running, offs, pos, src);
 }
 
-// x_perm[r] = x[src[r] / K] for r in [0, rows), one warp per row; warps
-// w0, w0 + nw, ... of the caller's numbering.  x_perm is stored evict-first:
-// it is larger than what the first expert product could find in L2 anyway,
-// and x (read once per slot) then stays there for its second read.
-__device__ __forceinline__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ src,
-                                            int64_t rows, int K, int vec_per_row, uint4* __restrict__ x_perm,
-                                            int64_t w0, int64_t nw) {
+// x_perm[pos[t K + j]] = x[t] for every kept slot j of token t: each x row
+// is read once and written to its (at most K) rows, one warp per token, 4
+// vectors a lane in flight.  (Every kept row of x_perm is the image of
+// exactly one slot, so each is written once.)  x_perm is stored evict-first:
+// the first expert product streams it from DRAM either way.  KP: K rounded
+// up to 2, 4 or 8.
+template <int KP>
+__global__ void __launch_bounds__(256)
+dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ pos, int64_t Tn, int K,
+                       int vec_per_row, uint4* __restrict__ x_perm) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
-  for (int64_t r = w0; r < rows; r += nw) {
-    const int64_t t = src[r] / K;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = warp0; t < Tn; t += nwarps) {
+    int64_t dst[KP];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      const int p = j < K ? pos[t * K + j] : -1;
+      dst[j] = p >= 0 ? (int64_t)p * vec_per_row : -1;
+    }
     const uint4* a = x + t * vec_per_row;
-    uint4* b = x_perm + r * vec_per_row;
     int v = lane;
     for (; v + 96 < vec_per_row; v += 128) {
       const uint4 u0 = a[v], u1 = a[v + 32], u2 = a[v + 64], u3 = a[v + 96];
-      __stcs(b + v, u0); __stcs(b + v + 32, u1); __stcs(b + v + 64, u2); __stcs(b + v + 96, u3);
+#pragma unroll
+      for (int j = 0; j < KP; ++j) {
+        if (dst[j] >= 0) {
+          uint4* b = x_perm + dst[j];
+          __stcs(b + v, u0); __stcs(b + v + 32, u1); __stcs(b + v + 64, u2); __stcs(b + v + 96, u3);
+        }
+      }
     }
-    for (; v < vec_per_row; v += 32) __stcs(b + v, a[v]);
+    for (; v < vec_per_row; v += 32) {
+      const uint4 u = a[v];
+#pragma unroll
+      for (int j = 0; j < KP; ++j)
+        if (dst[j] >= 0) __stcs(x_perm + dst[j] + v, u);
+    }
   }
-}
-
-// x_perm[r] = x[src[r] / K] for r < offs[E], over the whole grid.
-__global__ void __launch_bounds__(256)
-dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
-                       const int32_t* __restrict__ offs, int E, int K, int vec_per_row,
-                       uint4* __restrict__ x_perm) {
-  pdl_enter();
-  gather_rows(x, src, offs[E], K, vec_per_row, x_perm, ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5,
-              ((int64_t)gridDim.x * blockDim.x) >> 5);
 }
 
 // A small batch in one block: histogram, counts, stable placement and the
@@ -442,8 +454,11 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
                       s.C, bslots, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos, o.src);
   if (e == cudaSuccess && x && x_perm && S > 0) {
     const int vec = (int)((int64_t)s.H * s.esize() / 16);
-    e = launch_kernel(dispatch_gather_kernel, dim3(sm_count() * 8), dim3(256), 0, st, 1, (const uint4*)x,
-                      (const int32_t*)o.src, (const int32_t*)o.offs, s.E, s.K, vec, (uint4*)x_perm);
+    auto kern = s.K <= 2 ? dispatch_gather_kernel<2> : s.K <= 4 ? dispatch_gather_kernel<4> : dispatch_gather_kernel<8>;
+    int64_t grid = (s.T + 7) / 8;                      // 8 warps (tokens) a block
+    if (grid > (int64_t)sm_count() * 8) grid = (int64_t)sm_count() * 8;
+    e = launch_kernel(kern, dim3((unsigned)grid), dim3(256), 0, st, 1, (const uint4*)x, (const int32_t*)o.pos, s.T,
+                      s.K, vec, (uint4*)x_perm);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

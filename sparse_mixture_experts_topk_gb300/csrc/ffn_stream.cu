@@ -114,23 +114,27 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int
   }
   pdl_enter();
   if (warp == 0) {
-    // the experts with rows: how many (na), and the (blockIdx.x mod na)-th
+    // the experts with rows: how many (na), and the (blockIdx.x mod na)-th;
+    // all of offs is read in one round (E <= 256: 8 chunks of 32)
+    unsigned bal[8];
     int na = 0;
-    for (int c = 0; c < E; c += 32) {
-      const int e = c + lane;
-      na += __popc(__ballot_sync(0xffffffffu, e < E && offs[e + 1] > offs[e]));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int e = c * 32 + lane;
+      bal[c] = __ballot_sync(0xffffffffu, e < E && offs[e + 1] > offs[e]);
+      na += __popc(bal[c]);
     }
     int found = -1;
     if (na > 0) {
-      int seen = 0;
-      const int want = (int)(blockIdx.x % (unsigned)na);
-      for (int c = 0; c < E && found < 0; c += 32) {
-        const int e = c + lane;
-        const bool ne = e < E && offs[e + 1] > offs[e];
-        const unsigned bal = __ballot_sync(0xffffffffu, ne);
-        const unsigned hit = __ballot_sync(0xffffffffu, ne && __popc(bal & lanemask_lt()) == want - seen);
-        if (hit) found = c + __ffs(hit) - 1;
-        seen += __popc(bal);
+      int want = (int)(blockIdx.x % (unsigned)na);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int cnt = __popc(bal[c]);
+        if (found < 0 && want < cnt) {
+          const bool mine = ((bal[c] >> lane) & 1u) && __popc(bal[c] & lanemask_lt()) == want;
+          found = c * 32 + __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+        }
+        if (found < 0) want -= cnt;
       }
     }
     if (lane == 0) {
