@@ -325,8 +325,7 @@ int moe_layer_launches(const moe_desc* desc) {
   const Shape s = shape_of(*desc);
   int n = 0;
   if (s.T > 0) n += 1;                                  // router
-  if (dispatch_small(s)) n += 1;                        // one-block dispatch (also at T = 0)
-  else n += (layer_fused_hist(s) ? 0 : 1) + 3;          // histogram, scan, scatter, gather
+  n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
   if (s.T > 0) n += 2 + 1;                              // two expert products, combine
   return n;
 }

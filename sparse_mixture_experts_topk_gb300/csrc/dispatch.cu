@@ -51,6 +51,7 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslo
 // expert e.  Cuts at the capacity and writes count, offs (exclusive prefix
 // of the kept counts, offs[E] = kept rows) and the dropped total; with
 // psum_part also the summed router probabilities and the load-balancing loss.
+// Every output pointer may be null (that output is not written).
 // s_offs (nullable): also receives offs[0..E] in shared memory.  p_pre >= 0
 // (with psum_part set): this thread's probability sum, already added up in
 // row order by the caller.
@@ -79,10 +80,12 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
     __syncthreads();
   }
   if (e < E) {
-    count[e] = run;
+    if (count) count[e] = run;
     if (count_copy) count_copy[e] = run;
-    offs[e] = sk[e] - kept;
-    if (e == E - 1) offs[E] = sk[e];
+    if (offs) {
+      offs[e] = sk[e] - kept;
+      if (e == E - 1) offs[E] = sk[e];
+    }
     if (s_offs) {
       s_offs[e] = sk[e] - kept;
       if (e == E - 1) s_offs[E] = sk[e];
@@ -321,6 +324,82 @@ dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ 
   }
 }
 
+// Scan and scatter in one kernel, when the router has counted its 128-token
+// tiles: every block reads the whole [nblk, E] table of tile counts (eight
+// loads in flight per thread), takes its rank base (the counts of the tiles
+// before it) and the experts' totals and offsets, and places its tile's
+// slots.  Block 0 also writes the counts, offsets, dropped slots,
+// probability sums (added up exactly as the scan kernel does) and the loss.
+__global__ void __launch_bounds__(kDispThreads)
+dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
+                             const int32_t* __restrict__ blk_hist, int64_t nblk, int32_t* __restrict__ count,
+                             int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
+                             const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
+                             float* __restrict__ aux, int64_t Tn, int K, int32_t* __restrict__ count_copy,
+                             int32_t* __restrict__ dropped_copy, int32_t* __restrict__ sched,
+                             int32_t* __restrict__ pos, int32_t* __restrict__ src) {
+  extern __shared__ int sh[];          // [nblk, E] tile counts
+  __shared__ int running[256];
+  __shared__ int s_offs[257];
+  __shared__ int wcnt[kDispWarps][256];
+  __shared__ float s_pg[256];
+  pdl_enter();
+  const int e = threadIdx.x;
+  const bool leader = blockIdx.x == 0;
+  const int64_t n = nblk * E;
+  for (int64_t i0 = threadIdx.x; i0 < n; i0 += 256 * 8) {
+    int h[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) h[u] = i0 + 256 * u < n ? blk_hist[i0 + 256 * u] : 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + 256 * u < n) sh[i0 + 256 * u] = h[u];
+  }
+  float p_pre = -1.f;
+  if (leader && psum_part) {
+    // G = 256 / E thread groups each add every G-th row in row order, then
+    // thread e adds the G group sums in group order
+    const int G = 256 / E;
+    const int g = threadIdx.x / E, ee = threadIdx.x % E;
+    if (g < G) {
+      float a = 0.f;
+      for (int64_t r = g; r < prows; r += G) a += psum_part[r * E + ee];
+      s_pg[g * E + ee] = a;
+    }
+    __syncthreads();
+    if (e < E) {
+      p_pre = 0.f;
+      for (int gg = 0; gg < G; ++gg) p_pre += s_pg[gg * E + e];
+    }
+  }
+  __syncthreads();
+  int base = 0, total = 0;
+  if (e < E) {
+    for (int64_t b = 0; b < nblk; ++b) {
+      const int h = sh[b * E + e];
+      if (b < (int64_t)blockIdx.x) base += h;
+      total += h;
+    }
+  }
+  running[e] = base;
+  finish_counts(total, E, C, leader ? count : nullptr, leader ? offs : nullptr, leader ? dropped : nullptr,
+                leader ? psum_part : nullptr, prows, leader ? psum : nullptr, leader ? aux : nullptr, Tn, K,
+                leader ? count_copy : nullptr, leader ? dropped_copy : nullptr, leader ? sched : nullptr, s_offs,
+                p_pre);
+  __syncthreads();
+  const int64_t s0 = (int64_t)blockIdx.x * bslots;
+  const int64_t s1 = min(S, s0 + bslots);
+  for (int64_t c0 = s0; c0 < s1; c0 += kDispThreads) {
+    const int64_t sl = c0 + threadIdx.x;
+    int ex = -1;
+    if (sl < s1) {
+      ex = ids[sl];
+      if (ex < 0 || ex >= E) ex = -1;   // the router writes only ids in range (NaN scores: none taken)
+    }
+    scatter_chunk(ex, sl, sl < s1, E, C, wcnt, running, s_offs, pos, src, nullptr);
+  }
+}
+
 // A small batch in one block: histogram, counts, stable placement and the
 // row gather, with the same arithmetic and results as the four-kernel path.
 // Each thread reads its (at most 4) slots' expert ids and its expert's
@@ -408,6 +487,27 @@ int64_t dispatch_blocks(const Shape& s) {
   return (s.S() + b - 1) / b;
 }
 
+namespace {
+// the fused scan + scatter keeps the whole table of tile counts in shared memory
+constexpr size_t kFusedScanTable = 96 * 1024;
+
+cudaError_t launch_gather(const Shape& s, const void* x, const int32_t* pos, void* x_perm, cudaStream_t st) {
+  const int vec = (int)((int64_t)s.H * s.esize() / 16);
+  auto kern = s.K <= 2 ? dispatch_gather_kernel<2> : s.K <= 4 ? dispatch_gather_kernel<4> : dispatch_gather_kernel<8>;
+  int64_t grid = (s.T + 7) / 8;                      // 8 warps (tokens) a block
+  if (grid > (int64_t)sm_count() * 8) grid = (int64_t)sm_count() * 8;
+  return launch_kernel(kern, dim3((unsigned)grid), dim3(256), 0, st, 1, (const uint4*)x, pos, s.T, s.K, vec,
+                       (uint4*)x_perm);
+}
+}  // namespace
+
+int dispatch_launches(const Shape& s, bool hist_ready) {
+  if (dispatch_small(s)) return 1;
+  const int64_t nblk = hist_ready ? (s.T + kRouterTileTokens - 1) / kRouterTileTokens : dispatch_blocks(s);
+  if (hist_ready && (size_t)nblk * s.E * sizeof(int) <= kFusedScanTable) return 2;   // scan+scatter, gather
+  return (hist_ready ? 0 : 1) + 3;                                                   // (hist,) scan, scatter, gather
+}
+
 bool dispatch_small(const Shape& s) {
   // one block wins while its serial passes stay a few microseconds: up to
   // four 256-slot chunks and 256 KB of rows for its eight warps to copy
@@ -434,6 +534,21 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
   const int64_t nblk = o.hist_ready ? (s.T + kRouterTileTokens - 1) / kRouterTileTokens
                                     : dispatch_blocks(s);
   cudaError_t e = cudaSuccess;
+  const size_t table = (size_t)nblk * s.E * sizeof(int);
+  if (o.hist_ready && nblk > 0 && table <= kFusedScanTable) {
+    if (table > 48 * 1024)
+      e = cudaFuncSetAttribute(dispatch_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)table);
+    const int64_t prows = o.psum_part ? router_partial_rows(s) : (int64_t)0;
+    if (e == cudaSuccess)
+      e = launch_kernel(dispatch_scan_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), table, st, 1, ids,
+                        S, s.E, s.C, bslots, (const int32_t*)o.blk_hist, nblk, o.count, o.offs, o.dropped,
+                        o.psum_part, prows, o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy, o.sched,
+                        o.pos, o.src);
+    if (e == cudaSuccess && x && x_perm && S > 0) e = launch_gather(s, x, o.pos, x_perm, st);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   if (nblk > 0 && !o.hist_ready)
     e = launch_kernel(dispatch_hist_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
                       bslots, o.blk_hist, err);
@@ -452,14 +567,7 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
   if (e == cudaSuccess && nblk > 0)
     e = launch_kernel(dispatch_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
                       s.C, bslots, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos, o.src);
-  if (e == cudaSuccess && x && x_perm && S > 0) {
-    const int vec = (int)((int64_t)s.H * s.esize() / 16);
-    auto kern = s.K <= 2 ? dispatch_gather_kernel<2> : s.K <= 4 ? dispatch_gather_kernel<4> : dispatch_gather_kernel<8>;
-    int64_t grid = (s.T + 7) / 8;                      // 8 warps (tokens) a block
-    if (grid > (int64_t)sm_count() * 8) grid = (int64_t)sm_count() * 8;
-    e = launch_kernel(kern, dim3((unsigned)grid), dim3(256), 0, st, 1, (const uint4*)x, (const int32_t*)o.pos, s.T,
-                      s.K, vec, (uint4*)x_perm);
-  }
+  if (e == cudaSuccess && x && x_perm && S > 0) e = launch_gather(s, x, o.pos, x_perm, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

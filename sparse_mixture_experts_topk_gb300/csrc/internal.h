@@ -86,7 +86,8 @@ cudaError_t launch_psum_reduce(const Shape& s, const float* psum_part, float* ps
 // ---------------------------------------------------------------- dispatch
 int64_t dispatch_blocks(const Shape& s);
 int dispatch_block_slots(const Shape& s);
-bool dispatch_small(const Shape& s);   // one-block dispatch (launch_dispatch picks it itself)
+bool dispatch_small(const Shape& s);
+int dispatch_launches(const Shape& s, bool hist_ready);   // kernels launch_dispatch issues (S > 0)   // one-block dispatch (launch_dispatch picks it itself)
 struct DispatchOut {
   int32_t* count;      // [E]
   int32_t* offs;       // [E+1]

@@ -61,11 +61,11 @@ def test_workspace_size_grows_with_shape(lib):
 
 def test_layer_launch_count(lib):
     """The kernels one layer call issues, from the shape: router, dispatch
-    (one block for a small batch; else scan, scatter, gather, plus a
-    histogram pass when the router does not count its tiles), two expert
+    (one block for a small batch; scan+scatter and gather when the router
+    counted its tiles; else histogram, scan, scatter, gather), two expert
     products, combine."""
     prefill = moe.make_desc(8192, 3584, 32, 2, 2560)
-    assert moe.moe_layer_launches(prefill) == 1 + 3 + 2 + 1
+    assert moe.moe_layer_launches(prefill) == 1 + 2 + 2 + 1
     f32 = moe.make_desc(4096, 256, 8, 2, 512, dtype=moe.MOE_F32)      # CUDA-core router: own histogram
     assert moe.moe_layer_launches(f32) == 1 + 4 + 2 + 1
     decode = moe.make_desc(8, 3584, 32, 2, 2560)
