@@ -126,13 +126,20 @@ def gen_gate_bias(w: Workload):
     """Optional per-expert gate bias (fp32 ``[E]``) or None.
 
     ``zipf``: ``b_e = ln(p_e)`` with ``p_e`` proportional to ``(e+1)^-s``, so
-    that the softmax prior over experts is Zipf(s)."""
+    that the softmax prior over experts is Zipf(s).
+    ``hot``: +20 on the first K experts and 0 elsewhere, so that every token
+    picks experts 0..K-1 (the most unbalanced routing: K long segments, the
+    other experts empty)."""
     if w.gate_bias == "none":
         return None
     if w.gate_bias == "zipf":
         p = (np.arange(1, w.E + 1, dtype=np.float64)) ** (-w.zipf_s)
         p /= p.sum()
         return np.log(p).astype(np.float32)
+    if w.gate_bias == "hot":
+        b = np.zeros(w.E, dtype=np.float32)
+        b[:w.K] = 20.0
+        return b
     raise ValueError(w.gate_bias)
 
 

@@ -55,6 +55,11 @@ SMALL = {
     "tiny_e256_k8": W.small("tiny_e256_k8", T=5, H=64, E=256, K=8, F=64),
     # every token picks both experts: 16-row segments, the largest streaming body
     "decode16_all": W.small("decode16_all", T=16, H=256, E=2, K=2, F=128),
+    # every token to experts 0 and 1: long segments (three 256-row blocks, the
+    # last one short), six empty experts
+    "hot2": W.small("hot2", T=700, H=256, E=8, K=2, F=384, gate_bias="hot"),
+    "hot2_cap": W.small("hot2_cap", T=700, H=256, E=8, K=2, F=384, gate_bias="hot",
+                        capacity=W.capacity_ceil(700, 8, 2)),
     # fp32 decode-sized batches: the CUDA-core router and the fp32 streaming kernel
     "decode_f32": W.small("decode_f32", T=3, H=96, E=6, K=2, F=64, dtype=W.F32, ffn_bias=True),
     "swiglu_decode_f32": W.small("swiglu_decode_f32", T=6, H=128, E=8, K=3, F=72, dtype=W.F32, act="swiglu"),

@@ -56,3 +56,12 @@ def test_zipf_gate_bias_is_log_zipf():
     p = np.exp(b)
     assert p.sum() == pytest.approx(1.0, rel=1e-6)
     np.testing.assert_allclose(p[0] / p[1:], np.arange(2, 33) ** 1.2, rtol=1e-5)
+
+
+def test_hot_gate_bias_sends_every_token_to_the_first_k_experts():
+    from oracle import moe_oracle as O
+    w = W.small("hot", T=50, H=64, E=8, K=2, F=64, gate_bias="hot")
+    inp = W.generate(w)
+    l = O.gate_logits(O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype), inp.gate_bias)
+    ids, _, _ = O.route(l, w.K)
+    assert set(np.unique(ids)) == {0, 1}
