@@ -204,14 +204,21 @@ def moe_get_device_error(ws, stream=None) -> int:
     return int(code.value)
 
 
+_prof_events = None
+
+
 def moe_profile_events(events) -> None:
     """Record the 6 given ``torch.cuda.Event`` objects at the stage boundaries of
     every later ``moe_layer_forward`` on this thread; ``None`` switches it off."""
+    global _prof_events
     if not events:
         _check("moe_profile_events", lib().moe_profile_events(None, 0))
+        _prof_events = None
         return
+    events = list(events)
     for ev in events:            # torch creates the CUDA event on first record
         if not ev.cuda_event:
             ev.record()
     arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
     _check("moe_profile_events", lib().moe_profile_events(arr, len(events)))
+    _prof_events = events        # the library records these handles until switched off
