@@ -23,11 +23,6 @@ constexpr int kRouterKC = 32;    // hidden elements staged per step
 constexpr int kRouterThreads = 256;
 constexpr int kRouterWarps = kRouterThreads / 32;
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -35,44 +30,33 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // One warp per token: ls holds nt rows of E fp32 scores (row pitch E + 1).
-// Lane l holds experts l + 32 i; the k largest scores are taken one at a
-// time by a warp arg-max with ties to the lower index; the token's ids and
-// weights are written, and its ls row is replaced by the full softmax (for
-// the load-balancing sums).
+// Lane l reads experts l, l + 32, ...  Pick j is a warp arg-max over the
+// entries ranked after pick j - 1 in (score descending, index ascending)
+// order, so no entry is taken twice; lane j keeps pick j.  The token's ids
+// and weights are written, and its ls row is replaced by the full softmax
+// (for the load-balancing sums).  Loops are kept rolled: the routers run
+// once per layer with their code cold, and straight-line code costs more to
+// fetch than the loop overhead it saves.
 // s_hist (nullable, shared): counts of the chosen experts.
 __device__ __forceinline__ void finish_tokens(float* ls, int nt, int64_t t0, int E, int K, float inv_tau,
                                               int32_t* __restrict__ ids, float* __restrict__ w, int warp0,
                                               int nwarps, int* s_hist = nullptr) {
   const int lane = threadIdx.x & 31;
+#pragma unroll 1
   for (int tt = warp0; tt < nt; tt += nwarps) {
-    float v[8];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? ls[tt * (E + 1) + e] : -INFINITY;
-      m = fmaxf(m, v[i]);
-    }
-    m = warp_max(m);
-    float zs = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) zs += expf((v[i] - m) * inv_tau);
-    }
-    zs = warp_sum(zs);
-    unsigned taken = 0;
-    int sel_id[8];
-    float sel_z[8];
-    float zsel = 0.f;
+    float* row = ls + tt * (E + 1);
+    float prev_v = INFINITY, my_v = -INFINITY;
+    int prev_i = -1, my_id = 0x7fffffff;
+#pragma unroll 1
     for (int j = 0; j < K; ++j) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
+#pragma unroll 1
+      for (int e = lane; e < E; e += 32) {
+        const float v = row[e];
+        const bool after = v < prev_v || (v == prev_v && e > prev_i);
+        if (after && (v > bv || (v == bv && e < bi))) {
+          bv = v;
           bi = e;
         }
       }
@@ -85,26 +69,34 @@ __device__ __forceinline__ void finish_tokens(float* ls, int nt, int64_t t0, int
           bi = oi;
         }
       }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float z = expf((bv - m) * inv_tau);
-      sel_id[j] = bi;
-      sel_z[j] = z;
-      zsel += z;
-    }
-    if (lane == 0) {
-      const int64_t t = t0 + tt;
-      for (int j = 0; j < K; ++j) {
-        ids[t * K + j] = sel_id[j];
-        w[t * K + j] = sel_z[j] / zsel;
-        if (s_hist && (unsigned)sel_id[j] < (unsigned)E) atomicAdd(&s_hist[sel_id[j]], 1);   // NaN scores: none
+      if (lane == j) {
+        my_v = bv;
+        my_id = bi;
       }
+      prev_v = bv;
+      prev_i = bi;
     }
-    // full-softmax probabilities for the load-balancing statistics
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);   // the first pick is the largest score
+    float zs = 0.f;
+#pragma unroll 1
+    for (int e = lane; e < E; e += 32) {
+      const float z = expf((row[e] - m) * inv_tau);
+      row[e] = z;
+      zs += z;
+    }
+    zs = warp_sum(zs);
     const float inv = 1.f / zs;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) ls[tt * (E + 1) + e] = expf((v[i] - m) * inv_tau) * inv;
+#pragma unroll 1
+    for (int e = lane; e < E; e += 32) row[e] *= inv;
+    const float z = lane < K ? expf((my_v - m) * inv_tau) : 0.f;
+    float zsel = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < K; ++j) zsel += __shfl_sync(0xffffffffu, z, j);
+    if (lane < K) {
+      const int64_t t = t0 + tt;
+      ids[t * K + lane] = my_id;
+      w[t * K + lane] = z / zsel;
+      if (s_hist && (unsigned)my_id < (unsigned)E) atomicAdd(&s_hist[my_id], 1);   // NaN scores: none
     }
   }
 }
@@ -182,25 +174,43 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
 
 // Decode-sized batches (T <= kSmallTok, bf16): the cost is reading Wg once
 // and the latency of the few steps, so one cluster of up to 8 CTAs does it
-// all.  Warp g of the cluster owns gate rows g, g + G, ... (G = its warps);
-// each lane loads kSmallChunk 16-byte vectors of a row in one go, issued
-// before the token rows are staged in shared memory, and dots them with every
-// staged token (a body sized for the batch, so the hot loop stays small).  The T scores of a row go straight
-// into the leader CTA's score table over distributed shared memory; after one
-// cluster barrier the leader finishes each token (bias, top-k, weights),
-// counts the chosen experts as it picks them into tile_hist[0] (the layer's
-// single 128-token tile) and sums the probabilities per expert in token order
-// into psum_part[0].
+// all.  A gate row is cut into pieces of 32 * kSmallChunk 16-byte vectors,
+// and warp g of the cluster owns the (row, piece) units g, g + G, ... (G =
+// its warps), so that with E * pieces <= G the whole of Wg is requested in
+// one round; each lane loads its kSmallChunk vectors of a unit in one go
+// (the first before the token rows are staged in shared memory) and dots
+// them with every staged token (a body sized for the batch, so the hot loop
+// stays small).  A unit's T partial scores go straight into the leader CTA's
+// piece table over distributed shared memory; after one cluster barrier the
+// leader adds each score's pieces in piece order, adds the bias, finishes
+// each token (top-k, weights), counts the chosen experts as it picks them
+// into tile_hist[0] (the layer's single 128-token tile) and sums the
+// probabilities per expert in token order into psum_part[0].
 constexpr int kSmallTok = 16;
 constexpr int kSmallChunk = 8;
 constexpr int kSmallMaxCta = 8;
 
-// acc[t] += gate piece (gw, vectors c0 + lane + 32 u) . token row t, t < Tn <= MR
+// pieces of 32 * kSmallChunk 16-byte vectors per gate row of H bf16
+__host__ __device__ inline int small_pieces(int H) { return (H / 8 + 32 * kSmallChunk - 1) / (32 * kSmallChunk); }
+
+// shared memory of the small router: token rows, score table, piece table
+inline size_t small_smem(int64_t T, int H, int E) {
+  return (size_t)T * H * sizeof(bf16) + (size_t)T * (E + 1) * sizeof(float) +
+         (size_t)small_pieces(H) * T * E * sizeof(float);
+}
+
+// One (gate row e, piece c) unit: the piece (gw, vectors c0 + lane + 32 u)
+// dotted with each staged token row t < Tn <= MR, summed over the warp, and
+// stored by lane 0 at dst + 4 t E (the leader's piece table).  MR fixes the
+// body's size, so a small batch runs (and fetches) a small body.
 template <int MR>
-__device__ __forceinline__ void small_dot(const uint4 (&gw)[kSmallChunk], const uint4* s_x, int kv, int c0,
-                                          int Tn, float (&acc)[kSmallTok]) {
+__device__ __forceinline__ void small_unit(const uint4 (&gw)[kSmallChunk], const uint4* s_x, int kv, int c0,
+                                           int Tn, int E, uint32_t dst) {
   constexpr int V = Vec<bf16>::N;
   const int lane = threadIdx.x & 31;
+  float acc[MR];
+#pragma unroll
+  for (int t = 0; t < MR; ++t) acc[t] = 0.f;
 #pragma unroll
   for (int u = 0; u < kSmallChunk; ++u) {
     const int v = c0 + lane + 32 * u;
@@ -218,6 +228,15 @@ __device__ __forceinline__ void small_dot(const uint4 (&gw)[kSmallChunk], const 
       }
     }
   }
+#pragma unroll
+  for (int t = 0; t < MR; ++t) {
+    if (t < Tn) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) tc::st_peer_f32(dst + 4u * (uint32_t)(t * E), v);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kRouterThreads)
@@ -225,64 +244,64 @@ router_small_kernel(const bf16* __restrict__ x, const bf16* __restrict__ Wg,
                     const float* __restrict__ gate_bias, int Tn, int H, int E, int K, float inv_tau,
                     float* __restrict__ logits, int32_t* __restrict__ ids, float* __restrict__ w,
                     float* __restrict__ psum_part, int32_t* __restrict__ tile_hist) {
-  extern __shared__ uint4 s_x[];                       // [Tn][H] token rows, then [Tn][E+1] scores
+  // [Tn][H] token rows, then [Tn][E+1] scores, then [pieces][Tn][E] partial scores
+  extern __shared__ uint4 s_x[];
   __shared__ int s_hist[256];
   constexpr int V = Vec<bf16>::N;
   const int kv = H / V;
+  const int nch = small_pieces(H);                                     // pieces per gate row
   float* ls = reinterpret_cast<float*>(s_x + (size_t)Tn * kv);
+  float* lp = ls + Tn * (E + 1);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t rank = tc::cluster_ctarank();
   const int g0 = (int)rank * kRouterWarps + warp;
   const int G = (int)gridDim.x * kRouterWarps;
-  const int nch = (kv + 32 * kSmallChunk - 1) / (32 * kSmallChunk);   // pieces per gate row
-  const int pieces = g0 < E ? ((E - 1 - g0) / G + 1) * nch : 0;
+  const int units = E * nch;
+  const int mine = g0 < units ? (units - 1 - g0) / G + 1 : 0;
   for (int e = threadIdx.x; e < 256; e += kRouterThreads) s_hist[e] = 0;
   pdl_enter();
   uint4 gw[kSmallChunk];
-  auto load_piece = [&](int p) {
-    const int e = g0 + (p / nch) * G;
-    const int c0 = (p % nch) * 32 * kSmallChunk;
+  auto load_unit = [&](int p) {
+    const int u = g0 + p * G;
+    const int e = u / nch;
+    const int c0 = (u % nch) * 32 * kSmallChunk;
     const uint4* row = reinterpret_cast<const uint4*>(Wg + (int64_t)e * H);
 #pragma unroll
-    for (int u = 0; u < kSmallChunk; ++u) {
-      const int v = c0 + lane + 32 * u;
-      if (v < kv) gw[u] = __ldg(row + v);
+    for (int i = 0; i < kSmallChunk; ++i) {
+      const int v = c0 + lane + 32 * i;
+      if (v < kv) gw[i] = __ldg(row + v);
     }
   };
-  if (pieces > 0) load_piece(0);
+  if (mine > 0) load_unit(0);
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   for (int i = threadIdx.x; i < Tn * kv; i += kRouterThreads) s_x[i] = xv[i];
   __syncthreads();
-  const uint32_t ls_leader = tc::map_peer(tc::smem_u32(ls), 0);
-  float acc[kSmallTok];
+  const uint32_t lp_leader = tc::map_peer(tc::smem_u32(lp), 0);
+#pragma unroll 1
+  for (int p = 0; p < mine; ++p) {
+    const int u = g0 + p * G;
+    const int e = u / nch, c = u % nch;
+    const int c0 = c * 32 * kSmallChunk;
+    const uint32_t dst = lp_leader + 4u * (uint32_t)(c * Tn * E + e);
+    uint4 cur[kSmallChunk];
 #pragma unroll
-  for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
-  for (int p = 0; p < pieces; ++p) {
-    const int e = g0 + (p / nch) * G;
-    const int c0 = (p % nch) * 32 * kSmallChunk;
-    if (Tn <= 1) small_dot<1>(gw, s_x, kv, c0, Tn, acc);
-    else if (Tn <= 2) small_dot<2>(gw, s_x, kv, c0, Tn, acc);
-    else if (Tn <= 4) small_dot<4>(gw, s_x, kv, c0, Tn, acc);
-    else if (Tn <= 8) small_dot<8>(gw, s_x, kv, c0, Tn, acc);
-    else small_dot<kSmallTok>(gw, s_x, kv, c0, Tn, acc);
-    if (p + 1 < pieces) load_piece(p + 1);
-    if (p % nch != nch - 1) continue;
-#pragma unroll
-    for (int t = 0; t < kSmallTok; ++t) {
-      if (t < Tn) {
-        float v = acc[t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) tc::st_peer_f32(ls_leader + 4u * (uint32_t)(t * (E + 1) + e), v);
-      }
-      acc[t] = 0.f;
-    }
+    for (int i = 0; i < kSmallChunk; ++i) cur[i] = gw[i];
+    if (p + 1 < mine) load_unit(p + 1);   // the next unit's loads fly during this one
+    if (Tn <= 1) small_unit<1>(cur, s_x, kv, c0, Tn, E, dst);
+    else if (Tn <= 2) small_unit<2>(cur, s_x, kv, c0, Tn, E, dst);
+    else if (Tn <= 4) small_unit<4>(cur, s_x, kv, c0, Tn, E, dst);
+    else if (Tn <= 8) small_unit<8>(cur, s_x, kv, c0, Tn, E, dst);
+    else small_unit<kSmallTok>(cur, s_x, kv, c0, Tn, E, dst);
   }
-  tc::cluster_sync();              // every score is in the leader's table
+  tc::cluster_sync();              // every partial score is in the leader's piece table
   if (rank != 0) return;
+#pragma unroll 1
   for (int i = threadIdx.x; i < Tn * E; i += kRouterThreads) {
     const int t = i / E, e = i % E;
-    float v = ls[t * (E + 1) + e] + (gate_bias ? gate_bias[e] : 0.f);
+    float v = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) v += lp[(c * Tn + t) * E + e];
+    if (gate_bias) v += gate_bias[e];
     ls[t * (E + 1) + e] = v;
     if (logits) logits[(int64_t)t * E + e] = v;
   }
@@ -316,7 +335,7 @@ int64_t router_partials(const Shape& s) { return (s.T + kRouterTok - 1) / kRoute
 bool router_small(const Shape& s) {
   // the token rows and the score table fit one CTA's shared memory
   return s.dtype == MOE_BF16 && s.T <= kSmallTok && s.E <= 256 && !(s.flags & MOE_FLAG_SIMT_ROUTER) &&
-         s.T * s.H * 2 + s.T * (s.E + 1) * 4 <= 200 * 1024;
+         small_smem(s.T, s.H, s.E) <= 200 * 1024;
 }
 
 int64_t router_partial_rows(const Shape& s) {
@@ -329,9 +348,9 @@ cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const f
                           cudaStream_t st, int32_t* tile_hist) {
   if (s.T == 0) return cudaSuccess;
   if (router_small(s)) {
-    const int need = (s.E + kRouterWarps - 1) / kRouterWarps;
+    const int need = (s.E * small_pieces(s.H) + kRouterWarps - 1) / kRouterWarps;
     const int cl = need < kSmallMaxCta ? need : kSmallMaxCta;
-    const size_t smem = (size_t)s.T * s.H * sizeof(bf16) + (size_t)s.T * (s.E + 1) * sizeof(float);
+    const size_t smem = small_smem(s.T, s.H, s.E);
     cudaError_t e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

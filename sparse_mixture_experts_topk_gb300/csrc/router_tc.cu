@@ -325,7 +325,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       if (j < K) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-#pragma unroll 1
+#pragma unroll 4
         for (int i = 0; i < nv; ++i) {
           const int e = sub + G * i;
           const float v = lr[e];
@@ -354,7 +354,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     // total in every lane of the group
     const float m = sel_v[0];
     float zs = 0.f;
-#pragma unroll 1
+#pragma unroll 4
     for (int i = 0; i < nv; ++i) {
       const int e = sub + G * i;
       const float z = expf((lr[e] - m) * inv_tau);
@@ -363,7 +363,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     }
     for (int o = 1; o < G; o <<= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
     const float inv = 1.f / zs;
-#pragma unroll 1
+#pragma unroll 4
     for (int i = 0; i < nv; ++i) {
       const int e = sub + G * i;
       lr[e] = live ? lr[e] * inv : 0.f;
