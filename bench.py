@@ -39,8 +39,9 @@ METRIC = "MoE layer tokens/s at 1 GB300; % of bf16 tensor peak (GEMM) and HBM BW
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 # --gemm: the library's choice, or one expert GEMM kernel forced (descriptor
 # flags: single-SM tiles; SM pairs; SM pairs with token rows on the MMA's M
-# side for every product)
-GEMM_FLAGS = {"auto": 0, "single": 1 << 4, "pair": 1 << 5, "pair-rows": (1 << 5) | (1 << 8)}
+# side for every product; SM pairs with one launch per product)
+GEMM_FLAGS = {"auto": 0, "single": 1 << 4, "pair": 1 << 5, "pair-rows": (1 << 5) | (1 << 8),
+              "pair-split": (1 << 5) | (1 << 9)}
 STAGES = ["router", "dispatch", "ffn_first", "ffn_second", "combine"]
 
 
@@ -251,6 +252,8 @@ def run_ours(args, w: W.Workload):
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                       moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
     launches_per_step = moe.moe_layer_launches(d)
+    ffn_kind = moe.moe_ffn_kernel(d)
+    fused = ffn_kind == moe.MOE_FFN_TC_FUSED
     ws = moe.workspace(d)
     out = torch.empty((w.T, w.H), dtype=dt, device="cuda")
     aux = torch.empty(1, device="cuda")
@@ -331,10 +334,17 @@ def run_ours(args, w: W.Workload):
     work = work_counts(w, rows, used)
     value = world * w.T * args.steps / (total_ms / 1e3)
     f1, f2 = stage_ms["ffn_first"], stage_ms["ffn_second"]
-    dom, dom_ms = ("ffn_first", f1) if f1 >= f2 else ("ffn_second", f2)
+    flops = {"ffn_first": work["ffn_flops_first"], "ffn_second": work["ffn_flops_second"],
+             "ffn": work["ffn_flops_first"] + work["ffn_flops_second"]}
+    work["ffn_bytes"] = work["ffn_first_bytes"] + work["ffn_second_bytes"]
+    if fused:
+        # one launch runs both products: its time is the whole span between the
+        # dispatch and the combine marks (the second mark follows it directly)
+        dom, dom_ms = "ffn", f1 + f2
+    else:
+        dom, dom_ms = ("ffn_first", f1) if f1 >= f2 else ("ffn_second", f2)
     # decode-sized batches run the weight-streaming kernel: bound by HBM
-    streaming = w.T <= 16
-    flops = {"ffn_first": work["ffn_flops_first"], "ffn_second": work["ffn_flops_second"]}
+    streaming = ffn_kind == moe.MOE_FFN_STREAM
     if streaming:
         achieved = work[dom + "_bytes"] / (dom_ms / 1e3) / 1e9
         roof = {"kernel": f"weight-streaming expert kernel ({dom})", "bound": "hbm", "achieved": achieved,
@@ -343,13 +353,17 @@ def run_ours(args, w: W.Workload):
     else:
         achieved = flops[dom] / (dom_ms / 1e3) / 1e12
         traffic = ncu_traffic(w.name)
-        roof = {"kernel": f"expert grouped GEMM ({dom})", "bound": "tensor", "achieved": achieved,
+        roof = {"kernel": "expert grouped GEMM (both products, one launch)" if fused
+                else f"expert grouped GEMM ({dom})", "bound": "tensor", "achieved": achieved,
                 "peak": tflops, "unit": "TFLOP/s", "frac": achieved / tflops,
                 "peak_source": f"{src} bf16 (sustained: timed inside a seconds-long loop of layer steps)",
                 "frac_of_burst_peak": achieved / tflops_burst, "burst_peak": tflops_burst,
                 "traffic": traffic.get(dom) if traffic else None, "algorithmic_flops_per_launch": flops[dom]}
     stages = {}
-    for name in STAGES:
+    stage_names = ["router", "dispatch", "ffn", "combine"] if fused else STAGES
+    if fused:
+        stage_ms = dict(stage_ms, ffn=f1 + f2)
+    for name in stage_names:
         ms = stage_ms[name]
         if name.startswith("ffn"):
             tf = flops[name] / (ms / 1e3) / 1e12

@@ -74,6 +74,12 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * expert's last, short block runs swapped (rows on the N side, padded to
  * 16).  Same results; for comparing the two (testing). */
 #define MOE_FLAG_GEMM_ROWS   (1u << 8)
+/* bf16 with SM pairs: run the two expert products as two launches.  By
+ * default one persistent launch runs both: a tile of the second product
+ * starts as soon as the first product has written every hidden column of
+ * its 256-row block, so the second product's tiles fill the first one's
+ * tail.  Same results; for comparing the two (testing). */
+#define MOE_FLAG_FFN_SPLIT   (1u << 9)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the
@@ -251,6 +257,20 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg,
  * Returns the count (>= 1), or a negative MOE_ERR_* for an invalid desc.
  */
 int moe_layer_launches(const moe_desc* desc);
+
+/*
+ * Which expert-FFN kernel moe_expert_ffn and moe_layer_forward run for this
+ * description (no counterpart on the pages; it lets a caller or a benchmark
+ * account for the launches and attribute time).  Depends on the shape and
+ * flags only.  Returns one of MOE_FFN_*, or a negative MOE_ERR_* for an
+ * invalid desc.
+ */
+#define MOE_FFN_STREAM    0 /* weight streaming for decode-sized batches: 2 launches */
+#define MOE_FFN_SIMT      1 /* CUDA cores (f32, or forced): 2 launches */
+#define MOE_FFN_TC_SINGLE 2 /* tensor cores, 128x256 tiles per SM: 2 launches */
+#define MOE_FFN_TC_PAIRS  3 /* tensor cores on SM pairs, one launch per product: 2 launches */
+#define MOE_FFN_TC_FUSED  4 /* tensor cores on SM pairs, both products in 1 launch */
+int moe_ffn_kernel(const moe_desc* desc);
 
 /*
  * Stage timing for moe_layer_forward on the calling host thread (no

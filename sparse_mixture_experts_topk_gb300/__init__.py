@@ -18,10 +18,11 @@ import os
 __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU",
-    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "lib", "library_path", "make_desc",
+    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "lib", "library_path", "make_desc",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
-    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "workspace",
+    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "moe_ffn_kernel",
+    "MOE_FFN_STREAM", "MOE_FFN_SIMT", "MOE_FFN_TC_SINGLE", "MOE_FFN_TC_PAIRS", "MOE_FFN_TC_FUSED", "workspace",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -34,6 +35,9 @@ MOE_FLAG_GEMM_PAIR = 1 << 5
 MOE_FLAG_SWIGLU = 1 << 6
 MOE_FLAG_TEST_WAIT_TIMEOUT = 1 << 7
 MOE_FLAG_GEMM_ROWS = 1 << 8
+MOE_FLAG_FFN_SPLIT = 1 << 9
+# moe_ffn_kernel results
+MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED = 0, 1, 2, 3, 4
 
 MOE_OK = 0
 
@@ -69,6 +73,7 @@ _SIGS = {
     "moe_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_profile_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     "moe_layer_launches": (ctypes.c_int, [ctypes.POINTER(MoeDesc)]),
+    "moe_ffn_kernel": (ctypes.c_int, [ctypes.POINTER(MoeDesc)]),
 }
 
 _lib = None
@@ -195,6 +200,14 @@ def moe_layer_launches(desc: MoeDesc) -> int:
     if n < 0:
         _check("moe_layer_launches", n)
     return n
+
+
+def moe_ffn_kernel(desc: MoeDesc) -> int:
+    """Which expert-FFN kernel (``MOE_FFN_*``) a call with ``desc`` runs."""
+    k = int(lib().moe_ffn_kernel(ctypes.byref(desc)))
+    if k < 0:
+        _check("moe_ffn_kernel", k)
+    return k
 
 
 def moe_get_device_error(ws, stream=None) -> int:

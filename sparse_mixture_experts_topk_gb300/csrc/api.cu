@@ -94,6 +94,16 @@ int sm_count() {
   return cached[dev];
 }
 
+// The kernel launch_ffn runs (MOE_FFN_*); the same tests in the same order.
+int ffn_kernel(const Shape& s, int64_t max_rows) {
+  if (stream_ffn_eligible(s)) return MOE_FFN_STREAM;
+  if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
+    if (use_pair_gemm(s, max_rows)) return (s.flags & MOE_FLAG_FFN_SPLIT) ? MOE_FFN_TC_PAIRS : MOE_FFN_TC_FUSED;
+    return MOE_FFN_TC_SINGLE;
+  }
+  return MOE_FFN_SIMT;
+}
+
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
@@ -161,8 +171,8 @@ Layout layout_of(const moe_desc& d) {
   };
   const size_t S = (size_t)s.S(), E = (size_t)s.E, es = s.esize();
   L.rows = rows_for(d);
-  L.err = take(256);            // error word; the GEMM tile counters at +64
-  L.sched = L.err + 64;
+  L.err = take(256);            // error word
+  L.sched = take((size_t)sched_words(L.rows, s.E) * 4);   // the GEMMs' tile and row-block counters
   L.ids = take(S * 4);
   L.w = take(S * 4);
   L.psum_part = take((size_t)router_partials(s) * E * 4);
@@ -289,7 +299,8 @@ int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs
   const Shape s = shape_of(d);
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* sched = at<int32_t>(ws, L.sched);
-  cudaError_t e = cudaMemsetAsync(sched, 0, 2 * sizeof(int32_t), st);   // no dispatch kernel zeroed them
+  // no dispatch kernel zeroed them
+  cudaError_t e = cudaMemsetAsync(sched, 0, (size_t)sched_words(L.rows, s.E) * sizeof(int32_t), st);
   if (e == cudaSuccess)
     e = launch_ffn(s, L.rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, at<int>(ws, L.err), sched, st);
   return cuda_status(e);
@@ -326,8 +337,14 @@ int moe_layer_launches(const moe_desc* desc) {
   int n = 0;
   if (s.T > 0) n += 1;                                  // router
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
-  if (s.T > 0) n += 2 + 1;                              // two expert products, combine
+  if (s.T > 0) n += (ffn_kernel(s, rows_for(*desc)) == MOE_FFN_TC_FUSED ? 1 : 2) + 1;   // expert FFN, combine
   return n;
+}
+
+int moe_ffn_kernel(const moe_desc* desc) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  return ffn_kernel(shape_of(*desc), rows_for(*desc));
 }
 
 int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const float* gate_bias,

@@ -95,7 +95,12 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
     if (dropped) *dropped = sd[255];
     if (dropped_copy) *dropped_copy = sd[255];
   }
-  if (sched && e < 2) sched[e] = 0;   // the expert GEMMs that follow take tiles from these
+  if (sched) {
+    // the expert GEMMs that follow take tiles from sched[0..1] and count the
+    // finished hidden columns of each 256-row block of the kept rows in the rest
+    const int words = 2 + (sk[255] >> 8) + E + 1;
+    for (int i = e; i < words; i += 256) sched[i] = 0;
+  }
   if (psum_part) {
     float p = p_pre;
     if (e < E && p_pre < 0.f) {

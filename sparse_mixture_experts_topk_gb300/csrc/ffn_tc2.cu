@@ -28,6 +28,15 @@
 // 128 gate rows in the leader and the matching 128 up rows in the peer), so
 // each CTA's accumulator holds gate | up for the same output columns.
 //
+// One launch, both products.  The persistent pairs take the first
+// product's tiles and then the second's from one queue.  A second-product
+// tile needs every hidden column of its 256-row block, so its producers wait
+// on that block's counter, which each epilogue warp of the block's
+// first-product tiles advances once its stores are visible GPU-wide.  The
+// pairs that finish the first product early thus start on the second instead
+// of idling until the last first-product tile is done (with one launch per
+// product they idled 10 us on average at the 8192-token layer).
+//
 // Roles, per CTA (192 threads), rank r = 0 (leader) or 1:
 //   warp 0     TMA producer: this CTA's share of A and B for each k-block into
 //              its ring; both CTAs' loads complete on the LEADER's `full`
@@ -54,6 +63,7 @@ constexpr int kBNh = 128;            // B rows per CTA at most (the pair covers 
 constexpr int kBK = 64;
 constexpr int kBoxB = 32;            // swapped: token rows per B box
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;         // epilogue warps per pair (4 per CTA)
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBNh * kBK * 2;
 constexpr int kBoxBytes = kBoxB * kBK * 2;
@@ -71,22 +81,143 @@ constexpr int kTQ = 16;
 static_assert(kTQ > kStages + 3, "tile queue shorter than the pipeline");
 constexpr int kTqAbort = -2;
 
-// Tensor maps: tmX = token rows [rows, K] in 128-row boxes (row-orientation
-// A), tmXs = the same rows in 32-row boxes (swapped B), tmW = weight rows
-// [E N, K] in 128-row boxes (row-orientation B, swapped A).  kEpi =
-// kEpiSwiglu: tmW covers [W1; W3] stacked per expert ([E, 2N, K]); the leader
-// loads 128 gate rows and the peer the matching 128 up rows.  swap_tail = 0
-// keeps every block in row orientation.
+// One product of a launch: output columns N, reduction length K, the
+// nullable per-expert bias and the output rows C [rows, N].
+struct PairProduct {
+  int N, K;
+  const float* bias;
+  bf16* C;
+};
+
+// Wait (bounded) until the counter reaches `need`, with acquire semantics at
+// GPU scope; then order those observed writes before this thread's later
+// tensor copies (a proxy fence: the copies read global memory through the
+// async proxy).  False on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int* p, int need, const volatile int* abort) {
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= need) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (*abort) return false;
+    if ((i & 63) == 63) {
+      const uint64_t now = tc::globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitNs) return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// One tile's epilogue: this warp's 32 accumulator lanes (TMEM lane quarter
+// q) -> bias -> activation -> bf16 -> global.  Swapped tiles hold the
+// transposed block (lane = output column, column = token row) and go through
+// the warp's 2 KB transpose buffer so stores stay 16-byte vectors along rows.
 template <int kEpi>
+__device__ __forceinline__ void tile_epilogue(uint32_t tbase, bool swap, int e, int row_base, int nrows, int row_end,
+                                              int n0, uint32_t rank, int q, int lane, bf16* xb,
+                                              const PairProduct& P) {
+  constexpr bool kSwi = kEpi == kEpiSwiglu;
+  constexpr int kOut = kSwi ? kBNh : 2 * kBNh;
+  const int N = P.N;
+  bf16* C = P.C;
+  const float* be = P.bias ? P.bias + (int64_t)e * (kSwi ? 2 * N : N) : nullptr;
+  if (swap) {
+    // lane = output column f, accumulator column j = token row row_base + j
+    const int f = n0 + (int)rank * kBM + q * 32 + lane;
+    const float bf = (be && f < N) ? be[f] : 0.f;
+    const int fv = n0 + (int)rank * kBM + q * 32 + 8 * (lane & 3);   // this lane's 8 stored columns
+#pragma unroll 1
+    for (int c = 0; c * 32 < nrows; ++c) {
+      uint32_t r[32];
+      tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a = __uint_as_float(r[j]) + bf;
+        xb[j * 32 + lane] = __float2bfloat16_rn(kEpi == kEpiGelu ? gelu_erf(a) : a);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int jj = (lane >> 2) + 8 * i;
+        const int row = row_base + c * 32 + jj;
+        if (row < row_end && fv < N)
+          *reinterpret_cast<uint4*>(C + (int64_t)row * N + fv) =
+              *reinterpret_cast<const uint4*>(xb + jj * 32 + 8 * (lane & 3));
+      }
+      __syncwarp();
+    }
+  } else {
+    const int row = row_base + (int)rank * kBM + q * 32 + lane;
+    const bool row_ok = row < row_end;
+#pragma unroll 1
+    for (int c = 0; c < kOut / 32; ++c) {
+      const int col0 = n0 + c * 32;
+      if (col0 >= N) break;
+      uint32_t r[32], u[kSwi ? 32 : 1];
+      tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+      if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
+      tc::tmem_wait_ld();
+      if (row_ok) {
+        bf16* dst = C + (int64_t)row * N + col0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          if (col0 + g * 8 < N) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float a = __uint_as_float(r[g * 8 + j]);
+              if (be) a += be[col0 + g * 8 + j];
+              if (kEpi == kEpiGelu) {
+                v[j] = gelu_erf(a);
+              } else if (kSwi) {
+                float b = __uint_as_float(u[(g * 8 + j) % (kSwi ? 32 : 1)]);
+                if (be) b += be[N + col0 + g * 8 + j];
+                v[j] = silu_f(a) * b;
+              } else {
+                v[j] = a;
+              }
+            }
+            *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
+          }
+        }
+      }
+    }
+  }
+}
+
+// One launch runs one product, or both (nphase = 2): the tiles of the first
+// product (activation kEpiA), then those of the second (plain), from one
+// tile queue.  A second-product tile reads the hidden rows of one 256-row
+// block, which all first-product tiles of that block write; each epilogue
+// warp of such a tile adds 1 to ready[block] once its stores are visible, and
+// both producers of a second-product tile wait until ready[block] = 8 x
+// (first-product tiles per block).  First-product tiles never wait and every
+// one of them is handed out before any second-product tile, so every wait
+// ends.  The block index is (offs[e] >> 8) + e + (row block within e), which
+// is unique and below rows / 256 + E + 1.
+//
+// Tensor maps, per product p: tmX = token rows [rows, K] in 128-row boxes
+// (row-orientation A), tmXs = the same rows in 32-row boxes (swapped B), tmW
+// = weight rows [E N, K] in 128-row boxes (row-orientation B, swapped A).
+// kEpiA = kEpiSwiglu: tmW0 covers [W1; W3] stacked per expert ([E, 2N, K]);
+// the leader loads 128 gate rows and the peer the matching 128 up rows.
+// swap_tail = 0 keeps every block in row orientation.
+template <int kEpiA>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXs,
-                         const __grid_constant__ CUtensorMap tmW, const int32_t* __restrict__ offs, int E, int N,
-                         int K, int swap_tail, int* __restrict__ next_tile, const float* __restrict__ bias,
-                         bf16* __restrict__ C, int* err) {
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmXs0,
+                         const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmX1,
+                         const __grid_constant__ CUtensorMap tmXs1, const __grid_constant__ CUtensorMap tmW1,
+                         const int32_t* __restrict__ offs, int E, PairProduct P0, PairProduct P1, int nphase,
+                         int swap_tail, int* __restrict__ next_tile, int* __restrict__ ready, int* err) {
   constexpr int S = kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_offs[257];
-  __shared__ int s_tstart[257];
+  __shared__ int s_tstart[2][257];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ __align__(8) uint64_t s_bar[2 * S + 5];
@@ -104,43 +235,59 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_ctarank();          // 0 = leader
-  constexpr bool kSwi = kEpi == kEpiSwiglu;
-  constexpr int kOut = kSwi ? kBNh : 2 * kBNh;   // output columns per pair tile
-  const int nt = (N + kOut - 1) / kOut;
-  const int nk = (K + kBK - 1) / kBK;
+  constexpr bool kSwiA = kEpiA == kEpiSwiglu;
+  constexpr int kOutA = kSwiA ? kBNh : 2 * kBNh;   // output columns per pair tile, first product
+  constexpr int kOutB = 2 * kBNh;                  // second product
+  const int nt0 = (P0.N + kOutA - 1) / kOutA;
+  const int nt1 = (P1.N + kOutB - 1) / kOutB;
+  const int nk0 = (P0.K + kBK - 1) / kBK;
+  const int nk1 = (P1.K + kBK - 1) / kBK;
 
   if (warp == 0) {
     pdl_enter();   // the tile table reads offs, written by the previous kernel
-    // per-expert pair-tile counts (256-row blocks x n-tiles) and their prefix
-    int loc[8];
-    int sum = 0;
+    // per-expert pair-tile counts (256-row blocks x n-tiles) of both products and their prefixes
+    int loc0[8], loc1[8];
+    int sum0 = 0, sum1 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      int v = 0;
+      int mt = 0;
       if (e < E) {
         const int o0 = offs[e], o1 = offs[e + 1];
-        v = ((o1 - o0 + 2 * kBM - 1) / (2 * kBM)) * nt;
+        mt = (o1 - o0 + 2 * kBM - 1) / (2 * kBM);
         s_offs[e] = o0;
         if (e == E - 1) s_offs[E] = o1;
       }
-      loc[i] = v;
-      sum += v;
+      loc0[i] = mt * nt0;
+      loc1[i] = nphase > 1 ? mt * nt1 : 0;
+      sum0 += loc0[i];
+      sum1 += loc1[i];
     }
-    int incl = sum;
+    int incl0 = sum0, incl1 = sum1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      const int t0 = __shfl_up_sync(0xffffffffu, incl0, o);
+      const int t1 = __shfl_up_sync(0xffffffffu, incl1, o);
+      if (lane >= o) {
+        incl0 += t0;
+        incl1 += t1;
+      }
     }
-    int run = incl - sum;
+    int run0 = incl0 - sum0, run1 = incl1 - sum1;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      if (e < E) s_tstart[e] = run;
-      run += loc[i];
+      if (e < E) {
+        s_tstart[0][e] = run0;
+        s_tstart[1][e] = run1;
+      }
+      run0 += loc0[i];
+      run1 += loc1[i];
     }
-    if (lane == 31) s_tstart[E] = incl;
+    if (lane == 31) {
+      s_tstart[0][E] = incl0;
+      s_tstart[1][E] = incl1;
+    }
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
         tc::mbar_init(full(s), 1);       // used in the leader: its arm + both CTAs' bytes
@@ -155,9 +302,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
       for (int i = 0; i < kTQ; ++i) s_tq[i] = 0ull;
       tc::fence_barrier_init();
       tc::fence_proxy_async_smem();
-      tc::prefetch_tmap(&tmX);
-      tc::prefetch_tmap(&tmXs);
-      tc::prefetch_tmap(&tmW);
+      tc::prefetch_tmap(&tmX0);
+      tc::prefetch_tmap(&tmXs0);
+      tc::prefetch_tmap(&tmW0);
+      if (nphase > 1) {
+        tc::prefetch_tmap(&tmX1);
+        tc::prefetch_tmap(&tmXs1);
+        tc::prefetch_tmap(&tmW1);
+      }
     }
   } else if (warp == 1) {
     tc::tmem_alloc_pair(tc::smem_u32(&s_tmem), kTmemCols);
@@ -169,7 +321,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
   tc::tc_fence_after();
   if (warp != 0) pdl_wait();
   const uint32_t tmem = s_tmem;
-  const int total = s_tstart[E];
+  const int total0 = s_tstart[0][E];
+  const int total = total0 + s_tstart[1][E];
 
   // the leader's producer publishes tile `t` (or -1, the end) as entry `seq`
   auto tq_publish = [&](int seq, int t) {
@@ -196,30 +349,36 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     }
   };
 
-  // tile t -> expert e, its first token row (the pair's), the rows of that
-  // block (<= 256), the MMA N (swapped: rows rounded up to 16; else 256) and
-  // the first output column.  Tiles run expert by expert, row blocks inner.
+  // tile t -> product p, expert e, its first token row (the pair's), the
+  // rows of that block (<= 256), the MMA N (swapped: rows rounded up to 16;
+  // else 256), the first output column and the block's ready counter.  Tiles
+  // run product by product, expert by expert, row blocks inner.
   struct Tile {
-    int e, row_base, nrows, row_end, mma_n, n0;
+    int p, e, row_base, nrows, row_end, mma_n, n0, block;
     bool swap;
   };
   auto decode = [&](int t) {
     Tile d;
+    d.p = t >= total0 ? 1 : 0;
+    const int tl = t - (d.p ? total0 : 0);
+    const int* ts = s_tstart[d.p];
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_tstart[mid] <= t) lo = mid; else hi = mid - 1;
+      if (ts[mid] <= tl) lo = mid; else hi = mid - 1;
     }
     d.e = lo;
     const int rows = s_offs[d.e + 1] - s_offs[d.e];
     const int mt = (rows + 2 * kBM - 1) / (2 * kBM);
-    const int local = t - s_tstart[d.e];
-    d.row_base = s_offs[d.e] + (local % mt) * (2 * kBM);
+    const int local = tl - ts[d.e];
+    const int rb = local % mt;
+    d.row_base = s_offs[d.e] + rb * (2 * kBM);
     d.row_end = s_offs[d.e + 1];
     d.nrows = min(2 * kBM, d.row_end - d.row_base);
-    d.swap = !kSwi && swap_tail && d.nrows < 2 * kBM;
+    d.swap = !(d.p == 0 && kSwiA) && swap_tail && d.nrows < 2 * kBM;
     d.mma_n = d.swap ? (d.nrows + 15) / 16 * 16 : 2 * kBNh;
-    d.n0 = (local / mt) * kOut;
+    d.n0 = (local / mt) * (d.p ? kOutB : kOutA);
+    d.block = (s_offs[d.e] >> 8) + d.e + rb;
     return d;
   };
 
@@ -245,6 +404,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         }
         if (t < 0) break;
         const Tile d = decode(t);
+        // a second-product tile reads hidden rows that other SMs write
+        if (d.p == 1 && !wait_count(ready + d.block, kEpiWarps * nt0, &s_abort)) { ok = false; break; }
+        const CUtensorMap* mX = d.p ? &tmX1 : &tmX0;
+        const CUtensorMap* mXs = d.p ? &tmXs1 : &tmXs0;
+        const CUtensorMap* mW = d.p ? &tmW1 : &tmW0;
+        const int N = d.p ? P1.N : P0.N;
+        const int nk = d.p ? nk1 : nk0;
         // swapped: this CTA's token rows start half the MMA N into the block
         const int half = d.mma_n / 2;
         const int nbox = (half + kBoxB - 1) / kBoxB;
@@ -254,14 +420,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
           const uint32_t fbar = tc::map_peer(full(stage), 0);
           if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), tx);
           if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
-            tc::tma_load_2d_pair(sA + stage * kABytes, &tmW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+            tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
             for (int i = 0; i < nbox; ++i)
-              tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, &tmXs, fbar, kb * kBK,
+              tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, mXs, fbar, kb * kBK,
                                    d.row_base + (int)rank * half + i * kBoxB);
           } else {        // A = this CTA's 128 token rows, B = its 128 weight rows
-            tc::tma_load_2d_pair(sA + stage * kABytes, &tmX, fbar, kb * kBK, d.row_base + (int)rank * kBM);
-            tc::tma_load_2d_pair(sB + stage * kBBytes, &tmW, fbar, kb * kBK,
-                                 kSwi ? 2 * d.e * N + (int)rank * N + d.n0 : d.e * N + d.n0 + (int)rank * kBNh);
+            tc::tma_load_2d_pair(sA + stage * kABytes, mX, fbar, kb * kBK, d.row_base + (int)rank * kBM);
+            tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
+                                 (d.p == 0 && kSwiA) ? 2 * d.e * N + (int)rank * N + d.n0
+                                                     : d.e * N + d.n0 + (int)rank * kBNh);
           }
           filled |= 1u << stage;
           fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
@@ -286,7 +453,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         const int t = tq_read(seq);
         if (t == kTqAbort) { ok = false; break; }
         if (t < 0) break;
-        const uint32_t idesc = tc::idesc_bf16_f32(2 * kBM, decode(t).mma_n);
+        const Tile dt = decode(t);
+        const uint32_t idesc = tc::idesc_bf16_f32(2 * kBM, dt.mma_n);
+        const int nk = dt.p ? nk1 : nk0;
         if (!tc::mbar_wait(tempty(acc), acc_phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * 2 * kBNh);
@@ -338,69 +507,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
       }
       tc::tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kBNh);
-      const float* be = bias ? bias + (int64_t)d.e * (kSwi ? 2 * N : N) : nullptr;
-      if (d.swap) {
-        // lane = output column f, accumulator column j = token row row_base + j
-        const int f = d.n0 + (int)rank * kBM + q * 32 + lane;
-        const float bf = (be && f < N) ? be[f] : 0.f;
-        const int fv = d.n0 + (int)rank * kBM + q * 32 + 8 * (lane & 3);   // this lane's 8 stored columns
-#pragma unroll 1
-        for (int c = 0; c * 32 < d.nrows; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float a = __uint_as_float(r[j]) + bf;
-            xb[j * 32 + lane] = __float2bfloat16_rn(kEpi == kEpiGelu ? gelu_erf(a) : a);
-          }
+      if (d.p == 0) {
+        tile_epilogue<kEpiA>(tbase, d.swap, d.e, d.row_base, d.nrows, d.row_end, d.n0, rank, q, lane, xb, P0);
+        if (nphase > 1) {
+          // this warp's stores are visible GPU-wide before the block's counter moves
+          __threadfence();
           __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int jj = (lane >> 2) + 8 * i;
-            const int row = d.row_base + c * 32 + jj;
-            if (row < d.row_end && fv < N)
-              *reinterpret_cast<uint4*>(C + (int64_t)row * N + fv) =
-                  *reinterpret_cast<const uint4*>(xb + jj * 32 + 8 * (lane & 3));
-          }
-          __syncwarp();
+          if (lane == 0) atomicAdd(ready + d.block, 1);
         }
       } else {
-        const int row = d.row_base + (int)rank * kBM + q * 32 + lane;
-        const bool row_ok = row < d.row_end;
-#pragma unroll 1
-        for (int c = 0; c < kOut / 32; ++c) {
-          const int col0 = d.n0 + c * 32;
-          if (col0 >= N) break;
-          uint32_t r[32], u[kSwi ? 32 : 1];
-          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
-          if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
-          tc::tmem_wait_ld();
-          if (row_ok) {
-            bf16* dst = C + (int64_t)row * N + col0;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              if (col0 + g * 8 < N) {
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  float a = __uint_as_float(r[g * 8 + j]);
-                  if (be) a += be[col0 + g * 8 + j];
-                  if (kEpi == kEpiGelu) {
-                    v[j] = gelu_erf(a);
-                  } else if (kSwi) {
-                    float b = __uint_as_float(u[(g * 8 + j) % (kSwi ? 32 : 1)]);
-                    if (be) b += be[N + col0 + g * 8 + j];
-                    v[j] = silu_f(a) * b;
-                  } else {
-                    v[j] = a;
-                  }
-                }
-                *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
-              }
-            }
-          }
-        }
+        tile_epilogue<kEpiPlain>(tbase, d.swap, d.e, d.row_base, d.nrows, d.row_end, d.n0, rank, q, lane, xb, P1);
       }
       tc::tc_fence_before();
       if (rank == 0) tc::mbar_arrive(tempty(acc));
@@ -424,18 +540,24 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
   }
 }
 
-template <int kEpi>
-cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, const void* B, int N, int K,
-                     const float* bias, void* C, int swap_tail, int* next_tile, int* err, cudaStream_t st) {
-  CUtensorMap mx, mxs, mw;
-  if (!tma_map_bf16(&mx, A, (uint64_t)rows, (uint64_t)K, kBM)) return cudaErrorNotSupported;
-  if (!tma_map_bf16(&mxs, A, (uint64_t)rows, (uint64_t)K, kBoxB)) return cudaErrorNotSupported;
-  if (!tma_map_bf16(&mw, B, (uint64_t)E * N * (kEpi == kEpiSwiglu ? 2 : 1), (uint64_t)K, kBNh))
-    return cudaErrorNotSupported;
-  auto kern = grouped_gemm_pair_kernel<kEpi>;
+// The three tensor maps of one product: token rows A [rows, K] in 128- and
+// 32-row boxes, weight rows [wrows, K] in 128-row boxes.
+bool pair_maps(CUtensorMap* mx, CUtensorMap* mxs, CUtensorMap* mw, const void* A, int64_t rows, const void* B,
+               int64_t wrows, int K) {
+  return tma_map_bf16(mx, A, (uint64_t)rows, (uint64_t)K, kBM) &&
+         tma_map_bf16(mxs, A, (uint64_t)rows, (uint64_t)K, kBoxB) &&
+         tma_map_bf16(mw, B, (uint64_t)wrows, (uint64_t)K, kBNh);
+}
+
+// One persistent launch: one resident pair per two SMs, never more pairs
+// than fit at once.
+template <int kEpiA>
+cudaError_t launch_pair(const CUtensorMap (&m)[6], const int32_t* offs, int E, const PairProduct& P0,
+                        const PairProduct& P1, int nphase, int swap_tail, int* next_tile, int* ready, int* err,
+                        cudaStream_t st) {
+  auto kern = grouped_gemm_pair_kernel<kEpiA>;
   cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (r != cudaSuccess) return r;
-  // one resident pair per two SMs (persistent); never more pairs than fit at once
   int pairs = sm_count() / 2;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -451,12 +573,14 @@ cudaError_t run_pair(const void* A, int64_t rows, const int32_t* offs, int E, co
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   int fit = 0;
   if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < pairs) pairs = fit;
-  return launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmem, st, 2, mx, mxs, mw, offs, E, N, K,
-                       swap_tail, next_tile, bias, (bf16*)C, err);
+  return launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmem, st, 2, m[0], m[1], m[2], m[3], m[4],
+                       m[5], offs, E, P0, P1, nphase, swap_tail, next_tile, ready, err);
 }
 
 }  // namespace
 
+// sched[0], sched[1]: tile counters; sched[2 ..]: the row blocks' ready
+// counters (rows / 256 + E + 1 of them), all zero on entry.
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
                                void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
@@ -464,15 +588,31 @@ cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_p
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
     return cudaErrorNotSupported;
+  const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
   // each expert's last, short row block runs swapped unless all are forced to rows
   const int swap_tail = (s.flags & MOE_FLAG_GEMM_ROWS) ? 0 : 1;
-  cudaError_t r = (s.flags & MOE_FLAG_SWIGLU)
-                      ? run_pair<kEpiSwiglu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, 0, sched, err, st)
-                      : run_pair<kEpiGelu>(x_perm, max_rows, offs, s.E, W1, s.F, s.H, b1, h_perm, swap_tail, sched,
-                                           err, st);
+  CUtensorMap m1[6], m2[6];
+  if (!pair_maps(&m1[0], &m1[1], &m1[2], x_perm, max_rows, W1, (int64_t)s.E * s.F * (swi ? 2 : 1), s.H) ||
+      !pair_maps(&m2[0], &m2[1], &m2[2], h_perm, max_rows, W2, (int64_t)s.E * s.H, s.F))
+    return cudaErrorNotSupported;
+  const PairProduct P1{s.F, s.H, b1, (bf16*)h_perm};
+  const PairProduct P2{s.H, s.F, b2, (bf16*)y_perm};
+  if (!(s.flags & MOE_FLAG_FFN_SPLIT)) {
+    // both products in one launch: the second's tiles start on row blocks the first has finished
+    const CUtensorMap m[6] = {m1[0], m1[1], m1[2], m2[0], m2[1], m2[2]};
+    cudaError_t r = swi ? launch_pair<kEpiSwiglu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st)
+                        : launch_pair<kEpiGelu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st);
+    if (r != cudaSuccess) return r;
+    prof_mark(kMarkFirst, st);
+    return cudaSuccess;
+  }
+  const CUtensorMap ma[6] = {m1[0], m1[1], m1[2], m1[0], m1[1], m1[2]};
+  cudaError_t r = swi ? launch_pair<kEpiSwiglu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st)
+                      : launch_pair<kEpiGelu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
-  return run_pair<kEpiPlain>(h_perm, max_rows, offs, s.E, W2, s.H, s.F, b2, y_perm, swap_tail, sched + 1, err, st);
+  const CUtensorMap mb[6] = {m2[0], m2[1], m2[2], m2[0], m2[1], m2[2]};
+  return launch_pair<kEpiPlain>(mb, offs, s.E, P2, P2, 1, swap_tail, sched + 1, nullptr, err, st);
 }
 
 }  // namespace moe

@@ -103,13 +103,16 @@ struct DispatchOut {
   float* aux;              // [1] or null (needs psum_part)
   int32_t* count_copy;     // [E] or null
   int32_t* dropped_copy;   // [1] or null
-  int32_t* sched;          // [2] the expert GEMMs' tile counters, zeroed here, or null
+  int32_t* sched;          // [sched_words] the expert GEMMs' counters, zeroed here, or null
 };
 cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
                             const DispatchOut& o, int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------- expert FFN
-// sched: two zeroed ints, the tile counters of the SM-pair kernel's two products
+// The SM-pair expert GEMMs' counters: two tile counters, then one ready
+// counter per 256-row block of the kept rows (at most rows / 256 + E + 1).
+inline int64_t sched_words(int64_t rows, int E) { return 2 + rows / 256 + E + 1; }
+// sched: sched_words(max_rows, E) zeroed ints (the SM-pair kernel's counters)
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st);

@@ -62,17 +62,27 @@ def test_workspace_size_grows_with_shape(lib):
 def test_layer_launch_count(lib):
     """The kernels one layer call issues, from the shape: router, dispatch
     (one block for a small batch; scan+scatter and gather when the router
-    counted its tiles; else histogram, scan, scatter, gather), two expert
-    products, combine."""
+    counted its tiles; else histogram, scan, scatter, gather), the expert
+    products (one launch on SM pairs, else one per product), combine."""
     prefill = moe.make_desc(8192, 3584, 32, 2, 2560)
-    assert moe.moe_layer_launches(prefill) == 1 + 2 + 2 + 1
+    assert moe.moe_ffn_kernel(prefill) == moe.MOE_FFN_TC_FUSED
+    assert moe.moe_layer_launches(prefill) == 1 + 2 + 1 + 1
+    split = moe.make_desc(8192, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_FFN_SPLIT)
+    assert moe.moe_ffn_kernel(split) == moe.MOE_FFN_TC_PAIRS
+    assert moe.moe_layer_launches(split) == 1 + 2 + 2 + 1
+    single = moe.make_desc(8192, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_GEMM_SINGLE)
+    assert moe.moe_ffn_kernel(single) == moe.MOE_FFN_TC_SINGLE
     f32 = moe.make_desc(4096, 256, 8, 2, 512, dtype=moe.MOE_F32)      # CUDA-core router: own histogram
+    assert moe.moe_ffn_kernel(f32) == moe.MOE_FFN_SIMT
     assert moe.moe_layer_launches(f32) == 1 + 4 + 2 + 1
     decode = moe.make_desc(8, 3584, 32, 2, 2560)
+    assert moe.moe_ffn_kernel(decode) == moe.MOE_FFN_STREAM
     assert moe.moe_layer_launches(decode) == 1 + 1 + 2 + 1
     assert moe.moe_layer_launches(moe.make_desc(0, 3584, 32, 2, 2560)) == 1
     with pytest.raises(moe.MoeError):
         moe.moe_layer_launches(moe.make_desc(8, 3584, 32, 9, 2560))
+    with pytest.raises(moe.MoeError):
+        moe.moe_ffn_kernel(moe.make_desc(8, 3584, 32, 9, 2560))
 
 
 @pytest.mark.parametrize("bad", [

@@ -257,18 +257,20 @@ def test_heavily_tied_scores_route_like_the_oracle():
         assert (srt[:, :-1] == srt[:, 1:]).any(axis=1).mean() > 0.9   # ties everywhere
 
 
-@pytest.mark.parametrize("kind", ["single", "pair", "pair_rows"])
+@pytest.mark.parametrize("kind", ["single", "pair", "pair_rows", "pair_split"])
 @pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "ffn_bias", "cap_zipf_k4", "e256_k3", "one_token",
                                   "swiglu_ragged"])
 def test_expert_gemm_kernels_match_oracle(name, kind):
     """The tensor-core GEMM kernels (128x256 tiles per SM; SM pairs with the
-    token rows on the MMA's N side, the default, or on its M side) against
-    the oracle, product by product, and the layer output."""
+    token rows on the MMA's N side, the default, or on its M side; SM pairs
+    with both products in one launch, the default, or one launch each)
+    against the oracle, product by product, and the layer output."""
     w = SMALL[name]
     inp = W.generate(w)
     dev = Dev(inp)
     flag = {"single": moe.MOE_FLAG_GEMM_SINGLE, "pair": moe.MOE_FLAG_GEMM_PAIR,
-            "pair_rows": moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_GEMM_ROWS}[kind]
+            "pair_rows": moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_GEMM_ROWS,
+            "pair_split": moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_FFN_SPLIT}[kind]
     flags = flag | moe.MOE_FLAG_NO_DECODE
     r = run_stages(dev, flags=flags)
     assert r["device_error"] == 0
@@ -298,3 +300,21 @@ def test_expert_gemm_kernels_match_oracle(name, kind):
                           bf16=True, logits=gl, act=w.act)
     mx, rel = out_errors(as_f64(L["out"]), ref["out"])
     assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
+
+
+@pytest.mark.parametrize("name", ["ragged_bf16", "cap_zipf_k4", "swiglu_ragged", "hot2", "hot2_cap", "e64_k8"])
+def test_fused_pair_products_equal_split_launches(name):
+    """One launch for both SM-pair products (second-product tiles wait on
+    their row block's counter) gives the same bits as one launch per
+    product: every tile computes the same sums in the same order; only when
+    they run changes."""
+    w = SMALL[name]
+    dev = Dev(W.generate(w))
+    base = moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_NO_DECODE
+    fused = run_stages(dev, flags=base)
+    split = run_stages(dev, flags=base | moe.MOE_FLAG_FFN_SPLIT)
+    assert fused["device_error"] == 0 and split["device_error"] == 0
+    R = int(to_np(fused["offs"])[-1])
+    for key in ("h_perm", "y_perm"):
+        np.testing.assert_array_equal(to_np(fused[key])[:R], to_np(split[key])[:R], err_msg=key)
+    np.testing.assert_array_equal(to_np(fused["out"]), to_np(split["out"]))
