@@ -47,8 +47,9 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* po
                            void* out, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
   const int vec = (int)((int64_t)s.H * s.esize() / 16);
-  const int64_t cap = (int64_t)sm_count() * 8;    // blocks of 8 warps
-  const int chunk = combine_chunk(s.T, vec, cap * 8);
+  // persistent: as many blocks of 8 warps as the SMs hold at once (3 each)
+  const int64_t cap = (int64_t)sm_count() * 3;
+  const int chunk = combine_chunk();
   const int64_t items = s.T * ((vec + chunk - 1) / chunk);
   int64_t grid = (items + 7) / 8;
   if (grid > cap) grid = cap;

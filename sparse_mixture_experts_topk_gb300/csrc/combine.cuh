@@ -1,4 +1,4 @@
-// Combine body shared by the combine kernel and the fused decode kernel.
+// Combine body of the combine kernel.
 //
 // out[t] = sum_j w[t, j] * y_perm[pos[t, j]] for the K slots of token t
 // (a dropped slot, pos < 0, adds nothing), summed in fp32 in slot order j =
@@ -73,12 +73,11 @@ __device__ __forceinline__ void combine_items(const uint4* __restrict__ y_perm, 
   }
 }
 
-// Vectors per work item: whole rows for a large batch (each warp reads a
-// token's pos and w once); kCombineChunk for a batch with fewer items than
-// `warps`, so that it still spreads over many warps.
-__host__ __device__ inline int combine_chunk(int64_t T, int vec_per_row, int64_t warps) {
-  const int64_t small_items = T * ((vec_per_row + kCombineChunk - 1) / kCombineChunk);
-  return small_items <= warps ? kCombineChunk : (vec_per_row + kCombineChunk - 1) / kCombineChunk * kCombineChunk;
-}
+// Vectors per work item: a quarter of a 3584-wide bf16 row (kCombineChunk).
+// Items this small keep every warp of a persistent grid busy to the end
+// (8192 tokens make 32768 items for 3648 warps, nine rounds), where whole-row
+// items left the last of 2.25 waves a quarter full; re-reading a token's pos
+// and w per item costs 16 bytes.
+__host__ __device__ inline int combine_chunk() { return kCombineChunk; }
 
 }  // namespace moe
