@@ -14,8 +14,8 @@ bool stream_ffn_eligible(const Shape& s);
 cudaError_t launch_ffn_simt(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                             const void* W1, const float* b1, const void* W2, const float* b2,
                             void* h_perm, void* y_perm, cudaStream_t st);
-cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const int32_t* ids,
-                              const void* W1, const float* b1, const void* W2, const float* b2, void* h_perm,
+cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
+                              const float* b1, const void* W2, const float* b2, void* h_perm,
                               void* y_perm, int* err, cudaStream_t st);
 // Tensor-core paths; return cudaErrorNotSupported when they do not apply.
 cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
@@ -105,11 +105,11 @@ int ffn_kernel(const Shape& s, int64_t max_rows) {
 }
 
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
-                       const int32_t* ids, const void* W1, const float* b1, const void* W2, const float* b2,
+                       const void* W1, const float* b1, const void* W2, const float* b2,
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
   if (s.T == 0 || max_rows == 0) return cudaSuccess;
   if (stream_ffn_eligible(s))
-    return launch_ffn_stream(s, x_perm, offs, ids, W1, b1, W2, b2, h_perm, y_perm, err, st);
+    return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
   // bf16 runs on the tensor cores; there is no silent fallback (an
   // unsupported shape or a missing tensor-map entry point is an error)
   if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
@@ -302,8 +302,7 @@ int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs
   // no dispatch kernel zeroed them
   cudaError_t e = cudaMemsetAsync(sched, 0, (size_t)sched_words(L.rows, s.E) * sizeof(int32_t), st);
   if (e == cudaSuccess)
-    e = launch_ffn(s, L.rows, x_perm, offs, nullptr, W1, b1, W2, b2, h_perm, y_perm, at<int>(ws, L.err), sched,
-                   st);
+    e = launch_ffn(s, L.rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, at<int>(ws, L.err), sched, st);
   return cuda_status(e);
 }
 
@@ -407,8 +406,8 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   void* h_perm = at<void>(ws, L.h_perm);
   void* y_perm = x_perm;   // x_perm is dead once the first product has run
   if (e == cudaSuccess)
-    e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), at<int32_t>(ws, L.ids), W1, b1, W2, b2, h_perm,
-                   y_perm, err, at<int32_t>(ws, L.sched), st);
+    e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
+                   at<int32_t>(ws, L.sched), st);
   prof_mark(kMarkSecond, st);
   if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
   prof_mark(kMarkCombine, st);

@@ -55,6 +55,7 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslo
 // s_offs (nullable): also receives offs[0..E] in shared memory.  p_pre >= 0
 // (with psum_part set): this thread's probability sum, already added up in
 // row order by the caller.
+template <bool kRolled = false>
 __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __restrict__ count,
                                               int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
                                               const float* __restrict__ psum_part, int64_t prows,
@@ -71,6 +72,7 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
   sd[e] = (e < E) ? run - kept : 0;
   __syncthreads();
   // inclusive scan of kept (Hillis-Steele, 256 entries)
+#pragma unroll(kRolled ? 1 : 8)
   for (int o = 1; o < 256; o <<= 1) {
     const int v = (e >= o) ? sk[e - o] : 0;
     const int d = (e >= o) ? sd[e - o] : 0;
@@ -121,6 +123,7 @@ __device__ __forceinline__ void finish_counts(int run, int E, int C, int32_t* __
       // E * sum_i (count_i / (T K)) * (psum_i / T), reduced in a fixed order
       sa[e] = (e < E && Tn > 0) ? ((float)run / (float)(Tn * K)) * (p / (float)Tn) : 0.f;
       __syncthreads();
+#pragma unroll(kRolled ? 1 : 8)
       for (int o = 128; o > 0; o >>= 1) {
         if (e < o) sa[e] += sa[e + o];
         __syncthreads();
@@ -226,6 +229,7 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_hist, int64_t nblk, int E, 
 // running[e] (shared) is the rank the chunk's first slot of expert e takes
 // and is advanced past the chunk; ranks within the chunk come from a warp
 // match plus per-warp counts.  s_src (nullable) gets a shared copy of src.
+template <bool kRolled = false>
 __device__ __forceinline__ void scatter_chunk(int e, int64_t s, bool valid, int E, int C, int (*wcnt)[256],
                                               int* running, const int32_t* offs, int32_t* __restrict__ pos,
                                               int32_t* __restrict__ src, int* s_src) {
@@ -240,6 +244,7 @@ __device__ __forceinline__ void scatter_chunk(int e, int64_t s, bool valid, int 
     int p = -1;
     if (e >= 0) {
       int r = running[e] + __popc(below);
+#pragma unroll(kRolled ? 1 : 4)
       for (int w2 = 0; w2 < warp; ++w2) r += wcnt[w2][e];
       if (C <= 0 || r < C) {
         p = offs[e] + r;
@@ -252,7 +257,7 @@ __device__ __forceinline__ void scatter_chunk(int e, int64_t s, bool valid, int 
   __syncthreads();
   for (int e2 = tid; e2 < E; e2 += kDispThreads) {
     int add = 0;
-#pragma unroll
+#pragma unroll(kRolled ? 1 : kDispWarps)
     for (int w2 = 0; w2 < kDispWarps; ++w2) add += wcnt[w2][e2];
     running[e2] += add;
   }
@@ -451,14 +456,14 @@ dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, 
   }
   __syncthreads();
   const int run = (e < E) ? hist[e] : 0;
-  finish_counts(run, E, C, count, offs, dropped, psum_part, prows, psum, aux, Tn, K, count_copy, dropped_copy,
-                sched, s_offs, p);
+  finish_counts<true>(run, E, C, count, offs, dropped, psum_part, prows, psum, aux, Tn, K, count_copy,
+                      dropped_copy, sched, s_offs, p);
   hist[e] = 0;       // reused as the running rank
   __syncthreads();
 #pragma unroll
   for (int c = 0; c < kSmallChunks; ++c) {
     const int64_t s0 = (int64_t)c * kDispThreads;
-    if (s0 < S) scatter_chunk(my[c], s0 + threadIdx.x, s0 + threadIdx.x < S, E, C, wcnt, hist, s_offs, pos, src,
+    if (s0 < S) scatter_chunk<true>(my[c], s0 + threadIdx.x, s0 + threadIdx.x < S, E, C, wcnt, hist, s_offs, pos, src,
                               s_src);
   }
   if (x) {

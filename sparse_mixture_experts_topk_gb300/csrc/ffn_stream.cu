@@ -5,10 +5,8 @@
 // most 16 rows.  The time is reading every used expert's weights once, so
 // the kernel is built around bytes in flight rather than arithmetic:
 //   * one CTA per SM; CTA b serves the (b mod A)-th of the A experts that
-//     have rows (found from offs with a warp ballot, or, in the layer call's
-//     first product, from the routing ids, so that its first weight stage
-//     goes out while the dispatch still runs), and the CTAs of one expert
-//     split its output columns into contiguous ranges;
+//     have rows (found from offs with a warp ballot), and the CTAs of one
+//     expert split its output columns into contiguous ranges;
 //   * a producer thread moves the expert's activation rows and then, stage
 //     after stage, `rps` consecutive weight rows (one untiled bulk copy per
 //     stage; SwiGLU: a second copy for the matching up rows) into a ring of
@@ -32,10 +30,6 @@ constexpr int kConsumers = 8;                    // consumer warps; a stage hold
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
 constexpr int kMaxStages = 4;
 constexpr size_t kSmemBudget = 220 * 1024;
-// weight stages the first product issues before its dependency wait (one
-// measured best: decode steps 48.5 us at T=1 against 48.7 with 2-4 and 50.7
-// with none; more stages delay the activation rows queued behind them)
-constexpr int kEarlyStages = 1;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __host__ __device__ inline size_t act_bytes(int mcap, int K, int esize) { return ((size_t)mcap * K * esize + 127) / 128 * 128; }
@@ -90,21 +84,13 @@ __device__ __forceinline__ void dot_rows(const uint4* w, const uint4* u, const u
   }
 }
 
-// ids (nullable): the layer's routing ids [nids], complete before this
-// kernel is launched (they come from the kernel before the dispatch).  With
-// them a CTA finds its expert without the dispatch's offsets, so its weight
-// stages start streaming while the previous kernel still runs; only the
-// activation rows and their offsets wait for it.  early_stages: how many
-// weight stages go out before that wait (at most the ring's depth); the
-// activation rows queue behind them.
 template <typename T, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
-stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, const int32_t* __restrict__ ids,
-                  int nids, int E, int mcap, const T* __restrict__ B, const float* __restrict__ bias, int N, int K,
-                  int rps, int stages, int early_stages, T* __restrict__ C, int* err) {
+stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int E, int mcap,
+                  const T* __restrict__ B, const float* __restrict__ bias, int N, int K, int rps, int stages,
+                  T* __restrict__ C, int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_e, s_na, s_abort;
-  __shared__ unsigned s_mask[8];   // experts with rows, one bit each
   __shared__ __align__(8) uint64_t s_bar[2 * kMaxStages + 1];
   constexpr bool kSwi = kEpi == kEpiSwiglu;
   constexpr int V = Vec<T>::N;
@@ -126,36 +112,18 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, con
     s_abort = 0;
     tc::fence_barrier_init();
   }
-  pdl_trigger();
-  const bool early = ids != nullptr;
-  if (!early) pdl_wait();
+  pdl_enter();
   if (warp == 0) {
-    // the experts with rows: how many (na), and the (blockIdx.x mod na)-th.
-    // From offs (all of it read in one round, E <= 256: 8 chunks of 32), or
-    // from the routing ids: every chosen expert keeps at least one row,
-    // since a capacity is at least 1.
-    if (lane < 8) s_mask[lane] = 0u;
-    __syncwarp();
-    if (early) {
-      for (int i = lane; i < nids; i += 32) {
-        const int e = __ldcg(ids + i);
-        if ((unsigned)e < (unsigned)E) atomicOr(&s_mask[e >> 5], 1u << (e & 31));
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int e = c * 32 + lane;
-        const unsigned b = __ballot_sync(0xffffffffu, e < E && offs[e + 1] > offs[e]);
-        if (lane == 0) s_mask[c] = b;
-      }
-    }
-    __syncwarp();
+    // the experts with rows: how many (na), and the (blockIdx.x mod na)-th;
+    // all of offs is read in one round (E <= 256: 8 chunks of 32)
     unsigned bal[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) bal[c] = s_mask[c];
     int na = 0;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) na += __popc(bal[c]);
+    for (int c = 0; c < 8; ++c) {
+      const int e = c * 32 + lane;
+      bal[c] = __ballot_sync(0xffffffffu, e < E && offs[e + 1] > offs[e]);
+      na += __popc(bal[c]);
+    }
     int found = -1;
     if (na > 0) {
       int want = (int)(blockIdx.x % (unsigned)na);
@@ -177,6 +145,12 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, con
   __syncthreads();
   const int e = s_e, na = s_na;
   if (e < 0) return;
+  const int r0 = offs[e];
+  int m = offs[e + 1] - r0;
+  if (m > mcap) {                               // more rows than staged: report, compute the first mcap
+    if (threadIdx.x == 0) set_error(err, kDevBadIndex);
+    m = mcap;
+  }
   // this CTA's contiguous range of output columns of expert e
   const int a = (int)(blockIdx.x % (unsigned)na);
   const int nblk = ((int)gridDim.x - 1 - a) / na + 1;
@@ -192,22 +166,10 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, con
     // ------------------------------------------------------------ producer
     if (tc::elect_one()) {
       producer = true;
+      tc::mbar_arrive_expect_tx(act_bar, (uint32_t)m * row_bytes);
+      tc::bulk_load(s_act, A + (int64_t)r0 * K, (uint32_t)m * row_bytes, act_bar);
       bool ok = true;
-      // the ring starts empty: its first stages need no wait, and (with the
-      // ids) nothing from the previous kernel, so they go out before the
-      // activation rows, which do
-      const int first = early ? min(groups, min(stages, early_stages)) : 0;
-      bool act_issued = false;
-      for (int g = 0; g < groups || !act_issued; ++g) {
-        if (g == first && !act_issued) {
-          pdl_wait();
-          const int r0 = offs[e];
-          const int m = max(0, min(offs[e + 1] - r0, mcap));   // 0 only if the ids and offs disagree
-          tc::mbar_arrive_expect_tx(act_bar, (uint32_t)m * row_bytes);
-          if (m > 0) tc::bulk_load(s_act, A + (int64_t)r0 * K, (uint32_t)m * row_bytes, act_bar);
-          act_issued = true;
-        }
-        if (g >= groups) break;
+      for (int g = 0; g < groups; ++g) {
         const int s = g % stages;
         const uint32_t ph = (uint32_t)(g / stages) & 1u;
         if (!tc::mbar_wait(empty(s), ph ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
@@ -228,13 +190,6 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, con
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers
-    pdl_wait();
-    const int r0 = offs[e];
-    int m = offs[e + 1] - r0;
-    if (m > mcap || m <= 0) {   // more rows than staged, or none: report, compute what was staged
-      if (threadIdx.x == 0) set_error(err, kDevBadIndex);
-      m = max(0, min(m, mcap));
-    }
     const int kv = K / V;
     const uint4* act = reinterpret_cast<const uint4*>(smem);
     bool ok = tc::mbar_wait(act_bar, 0, &s_abort, kWaitNs);
@@ -299,9 +254,9 @@ StreamCfg stream_cfg(int mcap, int K, int esize, bool swi) {
 }
 
 template <typename T>
-cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, const int32_t* ids,
-                       const void* W1, const float* b1, const void* W2, const float* b2, void* h_perm,
-                       void* y_perm, int* err, cudaStream_t st) {
+cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
+                       const float* b1, const void* W2, const float* b2, void* h_perm, void* y_perm,
+                       int* err, cudaStream_t st) {
   const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
   const int64_t experts = s.S() < s.E ? s.S() : s.E;   // at most T*K experts have rows
   const int mcap = (int)(s.T < kMaxRows ? s.T : kMaxRows);
@@ -320,17 +275,12 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
     if (g > most) g = most;
     return dim3((unsigned)(g > 0 ? g : 1));
   };
-  // the first product starts streaming while the dispatch runs; the second
-  // cannot start before the first's CTAs leave, when its dependency is all
-  // but met, so it waits first and loads its activation rows first
-  const int nids = ids ? (int)s.S() : 0;
-  e = launch_kernel(k1, grid(s.F, c1.rps), dim3(kThreads), c1.smem, st, 1, (const T*)x_perm, offs, ids, nids, s.E,
-                    mcap, (const T*)W1, b1, s.F, s.H, c1.rps, c1.stages, kEarlyStages, (T*)h_perm, err);
+  e = launch_kernel(k1, grid(s.F, c1.rps), dim3(kThreads), c1.smem, st, 1, (const T*)x_perm, offs, s.E, mcap,
+                    (const T*)W1, b1, s.F, s.H, c1.rps, c1.stages, (T*)h_perm, err);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
-  return launch_kernel(k2, grid(s.H, c2.rps), dim3(kThreads), c2.smem, st, 1, (const T*)h_perm, offs,
-                       (const int32_t*)nullptr, 0, s.E, mcap, (const T*)W2, b2, s.H, s.F, c2.rps, c2.stages, 0,
-                       (T*)y_perm, err);
+  return launch_kernel(k2, grid(s.H, c2.rps), dim3(kThreads), c2.smem, st, 1, (const T*)h_perm, offs, s.E, mcap,
+                       (const T*)W2, b2, s.H, s.F, c2.rps, c2.stages, (T*)y_perm, err);
 }
 
 }  // namespace
@@ -346,12 +296,12 @@ bool stream_ffn_eligible(const Shape& s) {
   return stream_cfg(mcap, s.H, s.esize(), swi).stages >= 2 && stream_cfg(mcap, s.F, s.esize(), false).stages >= 2;
 }
 
-cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const int32_t* ids,
-                              const void* W1, const float* b1, const void* W2, const float* b2, void* h_perm,
+cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
+                              const float* b1, const void* W2, const float* b2, void* h_perm,
                               void* y_perm, int* err, cudaStream_t st) {
   if (s.dtype == MOE_BF16)
-    return run_stream<bf16>(s, x_perm, offs, ids, W1, b1, W2, b2, h_perm, y_perm, err, st);
-  return run_stream<float>(s, x_perm, offs, ids, W1, b1, W2, b2, h_perm, y_perm, err, st);
+    return run_stream<bf16>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+  return run_stream<float>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
 }
 
 }  // namespace moe

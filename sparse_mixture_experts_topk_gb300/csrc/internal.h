@@ -112,12 +112,9 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
 // The SM-pair expert GEMMs' counters: two tile counters, then one ready
 // counter per 256-row block of the kept rows (at most rows / 256 + E + 1).
 inline int64_t sched_words(int64_t rows, int E) { return 2 + rows / 256 + E + 1; }
-// sched: sched_words(max_rows, E) zeroed ints (the SM-pair kernel's counters).
-// ids (nullable): the layer's routing ids, complete before the expert kernels
-// launch; the weight-streaming kernels use them to start before the dispatch
-// has finished.
+// sched: sched_words(max_rows, E) zeroed ints (the SM-pair kernel's counters)
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
-                       const int32_t* ids, const void* W1, const float* b1, const void* W2, const float* b2,
+                       const void* W1, const float* b1, const void* W2, const float* b2,
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine / aux
