@@ -39,9 +39,10 @@ METRIC = "MoE layer tokens/s at 1 GB300; % of bf16 tensor peak (GEMM) and HBM BW
 FLUSH_BYTES = 512 << 20          # > 129 MB L2
 # --gemm: the library's choice, or one expert GEMM kernel forced (descriptor
 # flags: single-SM tiles; SM pairs; SM pairs with token rows on the MMA's M
-# side for every product; SM pairs with one launch per product)
+# side for every product; SM pairs with one launch per product; the library's
+# choice with one launch per product)
 GEMM_FLAGS = {"auto": 0, "single": 1 << 4, "pair": 1 << 5, "pair-rows": (1 << 5) | (1 << 8),
-              "pair-split": (1 << 5) | (1 << 9)}
+              "pair-split": (1 << 5) | (1 << 9), "split": 1 << 9}
 STAGES = ["router", "dispatch", "ffn_first", "ffn_second", "combine"]
 
 
@@ -253,7 +254,7 @@ def run_ours(args, w: W.Workload):
                       moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
     launches_per_step = moe.moe_layer_launches(d)
     ffn_kind = moe.moe_ffn_kernel(d)
-    fused = ffn_kind == moe.MOE_FFN_TC_FUSED
+    fused = ffn_kind in (moe.MOE_FFN_TC_FUSED, moe.MOE_FFN_STREAM)   # both products in one launch
     ws = moe.workspace(d)
     out = torch.empty((w.T, w.H), dtype=dt, device="cuda")
     aux = torch.empty(1, device="cuda")
@@ -344,10 +345,11 @@ def run_ours(args, w: W.Workload):
     else:
         dom, dom_ms = ("ffn_first", f1) if f1 >= f2 else ("ffn_second", f2)
     # decode-sized batches run the weight-streaming kernel: bound by HBM
-    streaming = ffn_kind == moe.MOE_FFN_STREAM
+    streaming = ffn_kind in (moe.MOE_FFN_STREAM, moe.MOE_FFN_STREAM_SPLIT)
     if streaming:
         achieved = work[dom + "_bytes"] / (dom_ms / 1e3) / 1e9
-        roof = {"kernel": f"weight-streaming expert kernel ({dom})", "bound": "hbm", "achieved": achieved,
+        roof = {"kernel": "weight-streaming expert kernel (both products, one launch)" if fused
+                else f"weight-streaming expert kernel ({dom})", "bound": "hbm", "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{src} HBM copy",
                 "traffic": None, "algorithmic_bytes_per_launch": work[dom + "_bytes"]}
     else:

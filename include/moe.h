@@ -74,11 +74,14 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * expert's last, short block runs swapped (rows on the N side, padded to
  * 16).  Same results; for comparing the two (testing). */
 #define MOE_FLAG_GEMM_ROWS   (1u << 8)
-/* bf16 with SM pairs: run the two expert products as two launches.  By
- * default one persistent launch runs both: a tile of the second product
- * starts as soon as the first product has written every hidden column of
- * its 256-row block, so the second product's tiles fill the first one's
- * tail.  Same results; for comparing the two (testing). */
+/* Run the two expert products as two launches.  By default one persistent
+ * launch runs both.  On SM pairs a tile of the second product starts as
+ * soon as the first product has written every hidden column of its 256-row
+ * block, so the second product's tiles fill the first one's tail; in the
+ * weight-streaming kernel of decode-sized batches the second product's
+ * weights stream right behind the first's through the same ring, and its
+ * activation rows load once every CTA of the expert has stored its share.
+ * Same results; for comparing the two (testing). */
 #define MOE_FLAG_FFN_SPLIT   (1u << 9)
 
 /*
@@ -265,11 +268,12 @@ int moe_layer_launches(const moe_desc* desc);
  * flags only.  Returns one of MOE_FFN_*, or a negative MOE_ERR_* for an
  * invalid desc.
  */
-#define MOE_FFN_STREAM    0 /* weight streaming for decode-sized batches: 2 launches */
+#define MOE_FFN_STREAM    0 /* weight streaming for decode-sized batches, both products in 1 launch */
 #define MOE_FFN_SIMT      1 /* CUDA cores (f32, or forced): 2 launches */
 #define MOE_FFN_TC_SINGLE 2 /* tensor cores, 128x256 tiles per SM: 2 launches */
 #define MOE_FFN_TC_PAIRS  3 /* tensor cores on SM pairs, one launch per product: 2 launches */
 #define MOE_FFN_TC_FUSED  4 /* tensor cores on SM pairs, both products in 1 launch */
+#define MOE_FFN_STREAM_SPLIT 5 /* weight streaming, one launch per product: 2 launches */
 int moe_ffn_kernel(const moe_desc* desc);
 
 /*

@@ -22,7 +22,8 @@ __all__ = [
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "moe_ffn_kernel",
-    "MOE_FFN_STREAM", "MOE_FFN_SIMT", "MOE_FFN_TC_SINGLE", "MOE_FFN_TC_PAIRS", "MOE_FFN_TC_FUSED", "workspace",
+    "MOE_FFN_STREAM", "MOE_FFN_SIMT", "MOE_FFN_TC_SINGLE", "MOE_FFN_TC_PAIRS", "MOE_FFN_TC_FUSED",
+    "MOE_FFN_STREAM_SPLIT", "workspace",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -37,7 +38,7 @@ MOE_FLAG_TEST_WAIT_TIMEOUT = 1 << 7
 MOE_FLAG_GEMM_ROWS = 1 << 8
 MOE_FLAG_FFN_SPLIT = 1 << 9
 # moe_ffn_kernel results
-MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED = 0, 1, 2, 3, 4
+MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED, MOE_FFN_STREAM_SPLIT = 0, 1, 2, 3, 4, 5
 
 MOE_OK = 0
 

@@ -16,7 +16,8 @@ cudaError_t launch_ffn_simt(const Shape& s, int64_t max_rows, const void* x_perm
                             void* h_perm, void* y_perm, cudaStream_t st);
 cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
                               const float* b1, const void* W2, const float* b2, void* h_perm,
-                              void* y_perm, int* err, cudaStream_t st);
+                              void* y_perm, int* err, int32_t* sched, cudaStream_t st);
+bool stream_fused(const Shape& s);
 // Tensor-core paths; return cudaErrorNotSupported when they do not apply.
 cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                           const void* W1, const float* b1, const void* W2, const float* b2,
@@ -96,7 +97,7 @@ int sm_count() {
 
 // The kernel launch_ffn runs (MOE_FFN_*); the same tests in the same order.
 int ffn_kernel(const Shape& s, int64_t max_rows) {
-  if (stream_ffn_eligible(s)) return MOE_FFN_STREAM;
+  if (stream_ffn_eligible(s)) return stream_fused(s) ? MOE_FFN_STREAM : MOE_FFN_STREAM_SPLIT;
   if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
     if (use_pair_gemm(s, max_rows)) return (s.flags & MOE_FLAG_FFN_SPLIT) ? MOE_FFN_TC_PAIRS : MOE_FFN_TC_FUSED;
     return MOE_FFN_TC_SINGLE;
@@ -109,7 +110,7 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
   if (s.T == 0 || max_rows == 0) return cudaSuccess;
   if (stream_ffn_eligible(s))
-    return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+    return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
   // bf16 runs on the tensor cores; there is no silent fallback (an
   // unsupported shape or a missing tensor-map entry point is an error)
   if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
@@ -337,7 +338,10 @@ int moe_layer_launches(const moe_desc* desc) {
   int n = 0;
   if (s.T > 0) n += 1;                                  // router
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
-  if (s.T > 0) n += (ffn_kernel(s, rows_for(*desc)) == MOE_FFN_TC_FUSED ? 1 : 2) + 1;   // expert FFN, combine
+  if (s.T > 0) {                                        // expert FFN, combine
+    const int k = ffn_kernel(s, rows_for(*desc));
+    n += (k == MOE_FFN_TC_FUSED || k == MOE_FFN_STREAM ? 1 : 2) + 1;
+  }
   return n;
 }
 

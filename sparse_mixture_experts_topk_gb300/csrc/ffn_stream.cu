@@ -17,6 +17,8 @@
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the error word, lets the other warps leave, waits (bounded) for the copies
 // it issued and returns.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -84,21 +86,94 @@ __device__ __forceinline__ void dot_rows(const uint4* w, const uint4* u, const u
   }
 }
 
+// One product of a launch: activation rows A [rows, K], weights B
+// [E, N, K] (SwiGLU: [E, 2N, K]), nullable bias, output rows C [rows, N],
+// rps weight rows per ring stage.
+template <typename T>
+struct StreamProduct {
+  const T* A;
+  const T* B;
+  const float* bias;
+  T* C;
+  int N, K, rps;
+};
+
+// The CTA's share of one product: its expert's output columns [n_begin,
+// n_end) (the CTAs of an expert split them into contiguous ranges) in
+// `groups` ring stages of rps rows.
+struct StreamRange {
+  int n_begin, n_end, groups;
+};
+__device__ __forceinline__ StreamRange stream_range(int N, int rps, int nblk, int slot) {
+  StreamRange r;
+  const int per = (N + nblk - 1) / nblk;
+  r.n_begin = slot * per;
+  r.n_end = min(N, r.n_begin + per);
+  r.groups = r.n_begin < r.n_end ? (r.n_end - r.n_begin + rps - 1) / rps : 0;
+  return r;
+}
+
+// Dot the staged weight rows of one stage with the staged activation rows:
+// consumer warp w takes row w (a body sized for the segment, so the hot
+// loop stays small).
+template <typename T, int kEpi>
+__device__ __forceinline__ void stage_rows(const uint8_t* st, int rps, uint32_t row_bytes, const uint4* act, int kv,
+                                           int m, const float* be, int n, int N, T* out) {
+  const int warp = threadIdx.x >> 5;
+  const uint4* wv = reinterpret_cast<const uint4*>(st + (size_t)warp * row_bytes);
+  const uint4* uv = reinterpret_cast<const uint4*>(st + (size_t)(rps + warp) * row_bytes);
+  if (m <= 1) dot_rows<T, kEpi, 1>(wv, uv, act, kv, m, be, n, N, out);
+  else if (m <= 2) dot_rows<T, kEpi, 2>(wv, uv, act, kv, m, be, n, N, out);
+  else if (m <= 4) dot_rows<T, kEpi, 4>(wv, uv, act, kv, m, be, n, N, out);
+  else if (m <= 8) dot_rows<T, kEpi, 8>(wv, uv, act, kv, m, be, n, N, out);
+  else dot_rows<T, kEpi, kMaxRows>(wv, uv, act, kv, m, be, n, N, out);
+}
+
+// Wait (bounded) until *p reaches `need`, acquire at GPU scope, then order
+// the observed writes before this thread's later bulk copies (which read
+// global memory through the async proxy).  False on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int* p, int need, const volatile int* abort) {
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= need) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (*abort) return false;
+    if ((i & 63) == 63) {
+      const uint64_t now = tc::globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitNs) return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// nphase = 1: the product P0 (activation kEpi).  nphase = 2: P0, then the
+// plain product P1 whose activation rows are P0's output rows of the same
+// expert.  One weight ring runs through both, so the second product's
+// weights stream right behind the first's; the second product's activation
+// rows are loaded once every CTA of the expert has stored (and fenced) its
+// share of them: each CTA adds 1 to done[e] after its first-product rows,
+// and the CTA's first consumer waits (bounded) for done[e] to reach the
+// expert's CTA count.  Every CTA finishes its first-product rows without
+// waiting on another CTA, so every such wait ends.
 template <typename T, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
-stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int E, int mcap,
-                  const T* __restrict__ B, const float* __restrict__ bias, int N, int K, int rps, int stages,
-                  T* __restrict__ C, int* err) {
+stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const int32_t* __restrict__ offs, int E,
+                  int mcap, int stages, uint32_t stage_bytes, int* __restrict__ done, int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_e, s_na, s_abort;
+  __shared__ int s_e, s_na, s_abort, s_act1;
   __shared__ __align__(8) uint64_t s_bar[2 * kMaxStages + 1];
   constexpr bool kSwi = kEpi == kEpiSwiglu;
   constexpr int V = Vec<T>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t row_bytes = (uint32_t)K * sizeof(T);
-  const uint32_t stage_bytes = (uint32_t)rps * row_bytes * (kSwi ? 2u : 1u);
   const uint32_t s_act = tc::smem_u32(smem);
-  const uint32_t s_ring = s_act + (uint32_t)act_bytes(mcap, K, sizeof(T));
+  const uint32_t act_room = (uint32_t)max(act_bytes(mcap, P0.K, sizeof(T)),
+                                          nphase > 1 ? act_bytes(mcap, P1.K, sizeof(T)) : (size_t)0);
+  const uint32_t s_ring = s_act + act_room;
   auto full = [&](int s) { return tc::smem_u32(&s_bar[s]); };
   auto empty = [&](int s) { return tc::smem_u32(&s_bar[kMaxStages + s]); };
   const uint32_t act_bar = tc::smem_u32(&s_bar[2 * kMaxStages]);
@@ -110,6 +185,7 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int
     }
     tc::mbar_init(act_bar, 1);
     s_abort = 0;
+    s_act1 = 0;
     tc::fence_barrier_init();
   }
   pdl_enter();
@@ -151,14 +227,14 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int
     if (threadIdx.x == 0) set_error(err, kDevBadIndex);
     m = mcap;
   }
-  // this CTA's contiguous range of output columns of expert e
+  // this CTA's share of expert e in each product
   const int a = (int)(blockIdx.x % (unsigned)na);
   const int nblk = ((int)gridDim.x - 1 - a) / na + 1;
-  const int per = (N + nblk - 1) / nblk;
-  const int n_begin = (int)(blockIdx.x / (unsigned)na) * per;
-  const int n_end = min(N, n_begin + per);
-  const int groups = n_begin < n_end ? (n_end - n_begin + rps - 1) / rps : 0;
-  const T* Be = B + (int64_t)e * N * K * (kSwi ? 2 : 1);
+  const int slot = (int)(blockIdx.x / (unsigned)na);
+  const StreamRange R0 = stream_range(P0.N, P0.rps, nblk, slot);
+  const StreamRange R1 = nphase > 1 ? stream_range(P1.N, P1.rps, nblk, slot) : StreamRange{0, 0, 0};
+  const int total = R0.groups + R1.groups;
+  const uint32_t row0 = (uint32_t)P0.K * sizeof(T), row1 = (uint32_t)P1.K * sizeof(T);
 
   uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
   bool producer = false;
@@ -166,19 +242,27 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int
     // ------------------------------------------------------------ producer
     if (tc::elect_one()) {
       producer = true;
-      tc::mbar_arrive_expect_tx(act_bar, (uint32_t)m * row_bytes);
-      tc::bulk_load(s_act, A + (int64_t)r0 * K, (uint32_t)m * row_bytes, act_bar);
+      tc::mbar_arrive_expect_tx(act_bar, (uint32_t)m * row0);
+      tc::bulk_load(s_act, P0.A + (int64_t)r0 * P0.K, (uint32_t)m * row0, act_bar);
       bool ok = true;
-      for (int g = 0; g < groups; ++g) {
+      for (int g = 0; g < total; ++g) {
         const int s = g % stages;
         const uint32_t ph = (uint32_t)(g / stages) & 1u;
         if (!tc::mbar_wait(empty(s), ph ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
-        const int n0 = n_begin + g * rps;
-        const uint32_t bytes = (uint32_t)min(rps, n_end - n0) * row_bytes;
-        tc::mbar_arrive_expect_tx(full(s), kSwi ? 2 * bytes : bytes);
         const uint32_t dst = s_ring + (uint32_t)s * stage_bytes;
-        tc::bulk_load(dst, Be + (int64_t)n0 * K, bytes, full(s));
-        if (kSwi) tc::bulk_load(dst + (uint32_t)rps * row_bytes, Be + (int64_t)(N + n0) * K, bytes, full(s));
+        if (g < R0.groups) {
+          const int n0 = R0.n_begin + g * P0.rps;
+          const uint32_t bytes = (uint32_t)min(P0.rps, R0.n_end - n0) * row0;
+          const T* Be = P0.B + (int64_t)e * P0.N * P0.K * (kSwi ? 2 : 1);
+          tc::mbar_arrive_expect_tx(full(s), kSwi ? 2 * bytes : bytes);
+          tc::bulk_load(dst, Be + (int64_t)n0 * P0.K, bytes, full(s));
+          if (kSwi) tc::bulk_load(dst + (uint32_t)P0.rps * row0, Be + (int64_t)(P0.N + n0) * P0.K, bytes, full(s));
+        } else {
+          const int n0 = R1.n_begin + (g - R0.groups) * P1.rps;
+          const uint32_t bytes = (uint32_t)min(P1.rps, R1.n_end - n0) * row1;
+          tc::mbar_arrive_expect_tx(full(s), bytes);
+          tc::bulk_load(dst, P1.B + ((int64_t)e * P1.N + n0) * P1.K, bytes, full(s));
+        }
         filled |= 1u << s;
         fill_par = (fill_par & ~(1u << s)) | (ph << s);
       }
@@ -190,29 +274,52 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers
-    const int kv = K / V;
+    // After a failed wait a warp does no more work but still passes the
+    // consumers' barrier below, so the other consumer warps never wait there
+    // for it (and every later wait of theirs sees the abort flag).
     const uint4* act = reinterpret_cast<const uint4*>(smem);
+    const uint8_t* ring = smem + act_room;
     bool ok = tc::mbar_wait(act_bar, 0, &s_abort, kWaitNs);
-    for (int g = 0; g < groups && ok; ++g) {
+    for (int g = 0; g < R0.groups; ++g) {
       const int s = g % stages;
       const uint32_t ph = (uint32_t)(g / stages) & 1u;
-      if (!tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; break; }
-      const int n = n_begin + g * rps + warp;
-      if (warp < rps && n < n_end) {
-        const uint8_t* st = smem + (s_ring - s_act) + (size_t)s * stage_bytes;
-        const uint4* wv = reinterpret_cast<const uint4*>(st + (size_t)warp * row_bytes);
-        const uint4* uv = reinterpret_cast<const uint4*>(st + (size_t)(rps + warp) * row_bytes);
-        const float* be = bias ? bias + (int64_t)e * N * (kSwi ? 2 : 1) : nullptr;
-        T* out = C + (int64_t)r0 * N + n;
-        // a body sized for the segment, so the hot loop stays small
-        if (m <= 1) dot_rows<T, kEpi, 1>(wv, uv, act, kv, m, be, n, N, out);
-        else if (m <= 2) dot_rows<T, kEpi, 2>(wv, uv, act, kv, m, be, n, N, out);
-        else if (m <= 4) dot_rows<T, kEpi, 4>(wv, uv, act, kv, m, be, n, N, out);
-        else if (m <= 8) dot_rows<T, kEpi, 8>(wv, uv, act, kv, m, be, n, N, out);
-        else dot_rows<T, kEpi, kMaxRows>(wv, uv, act, kv, m, be, n, N, out);
-      }
+      if (!ok || !tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; continue; }
+      const int n = R0.n_begin + g * P0.rps + warp;
+      if (warp < P0.rps && n < R0.n_end)
+        stage_rows<T, kEpi>(ring + (size_t)s * stage_bytes, P0.rps, row0, act, P0.K / V, m,
+                            P0.bias ? P0.bias + (int64_t)e * P0.N * (kSwi ? 2 : 1) : nullptr, n, P0.N,
+                            P0.C + (int64_t)r0 * P0.N + n);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(s));   // this warp is done with the stage
+    }
+    if (nphase > 1) {
+      // the first product is done here: its outputs fenced, the CTAs of the
+      // expert counted, then the second product's activation rows loaded
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+      if (warp == 0 && lane == 0) {
+        atomicAdd(done + e, 1);
+        if (ok && wait_count(done + e, nblk, &s_abort)) {
+          tc::mbar_arrive_expect_tx(act_bar, (uint32_t)m * row1);
+          tc::bulk_load(s_act, P1.A + (int64_t)r0 * P1.K, (uint32_t)m * row1, act_bar);
+          s_act1 = 1;
+        } else {
+          s_abort = 1;
+        }
+      }
+      ok = ok && tc::mbar_wait(act_bar, 1, &s_abort, kWaitNs);
+      for (int g = R0.groups; g < total; ++g) {
+        const int s = g % stages;
+        const uint32_t ph = (uint32_t)(g / stages) & 1u;
+        if (!ok || !tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; continue; }
+        const int n = R1.n_begin + (g - R0.groups) * P1.rps + warp;
+        if (warp < P1.rps && n < R1.n_end)
+          stage_rows<T, kEpiPlain>(ring + (size_t)s * stage_bytes, P1.rps, row1, act, P1.K / V, m,
+                                   P1.bias ? P1.bias + (int64_t)e * P1.N : nullptr, n, P1.N,
+                                   P1.C + (int64_t)r0 * P1.N + n);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(empty(s));
+      }
     }
     if (!ok) {
       if (lane == 0) set_error(err, kDevTimeout);
@@ -223,22 +330,22 @@ stream_ffn_kernel(const T* __restrict__ A, const int32_t* __restrict__ offs, int
   // after an abort, copies issued but never consumed land before the CTA leaves
   if (producer && s_abort) {
     tc::mbar_wait(act_bar, 0, nullptr, kWaitNs);
+    if (s_act1) tc::mbar_wait(act_bar, 1, nullptr, kWaitNs);
     for (int s = 0; s < stages; ++s)
       if ((filled >> s) & 1u) tc::mbar_wait(full(s), (fill_par >> s) & 1u, nullptr, kWaitNs);
   }
 }
 
 // Rows per stage and ring depth for one product: the most rows per stage
-// that still leave room for two stages beside the activation rows.
+// that still leave room for two stages beside `act` bytes of activation
+// rows.
 struct StreamCfg {
   int rps, stages;
   size_t smem;
 };
 
-StreamCfg stream_cfg(int mcap, int K, int esize, bool swi) {
+StreamCfg stream_cfg_room(size_t act, size_t row) {
   StreamCfg c{1, 0, 0};
-  const size_t act = act_bytes(mcap, K, esize);
-  const size_t row = (size_t)K * esize * (swi ? 2 : 1);
   for (int rps = kConsumers; rps >= 1; rps /= 2) {
     const size_t room = kSmemBudget > act ? kSmemBudget - act : 0;
     size_t st = room / ((size_t)rps * row);
@@ -253,34 +360,84 @@ StreamCfg stream_cfg(int mcap, int K, int esize, bool swi) {
   return c;
 }
 
+StreamCfg stream_cfg(int mcap, int K, int esize, bool swi) {
+  return stream_cfg_room(act_bytes(mcap, K, esize), (size_t)K * esize * (swi ? 2 : 1));
+}
+
+// Both products in one launch: one ring whose stages hold rps0 rows of the
+// first product's weights (gate and up rows for SwiGLU) and rps1 rows of
+// the second's, beside activation rows of the wider of the two.
+struct StreamFused {
+  bool ok;
+  StreamCfg c;
+  int rps1;
+  uint32_t stage_bytes;
+};
+
+StreamFused stream_fused_cfg(const Shape& s) {
+  StreamFused f{};
+  const int mcap = (int)(s.T < kMaxRows ? s.T : kMaxRows);
+  const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
+  const int es = s.esize();
+  const size_t act = std::max(act_bytes(mcap, s.H, es), act_bytes(mcap, s.F, es));
+  f.c = stream_cfg_room(act, (size_t)s.H * es * (swi ? 2 : 1));
+  f.stage_bytes = (uint32_t)((size_t)f.c.rps * s.H * es * (swi ? 2 : 1));
+  const size_t r1 = f.stage_bytes / ((size_t)s.F * es);
+  f.rps1 = (int)(r1 < (size_t)kConsumers ? r1 : kConsumers);
+  f.ok = f.c.stages >= 2 && f.rps1 >= 1;
+  return f;
+}
+
 template <typename T>
 cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
                        const float* b1, const void* W2, const float* b2, void* h_perm, void* y_perm,
-                       int* err, cudaStream_t st) {
+                       int* err, int32_t* sched, cudaStream_t st) {
   const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
   const int64_t experts = s.S() < s.E ? s.S() : s.E;   // at most T*K experts have rows
   const int mcap = (int)(s.T < kMaxRows ? s.T : kMaxRows);
   auto k1 = swi ? stream_ffn_kernel<T, kEpiSwiglu> : stream_ffn_kernel<T, kEpiGelu>;
   auto k2 = stream_ffn_kernel<T, kEpiPlain>;
+  // one CTA per SM, and no more CTAs than stages of rows to fill
+  auto grid = [&](int64_t groups_per_expert) {
+    int64_t g = sm_count();
+    const int64_t most = experts * groups_per_expert;
+    if (g > most) g = most;
+    return dim3((unsigned)(g > 0 ? g : 1));
+  };
+  const StreamProduct<T> P1{(const T*)x_perm, (const T*)W1, b1, (T*)h_perm, s.F, s.H, 0};
+  const StreamProduct<T> P2{(const T*)h_perm, (const T*)W2, b2, (T*)y_perm, s.H, s.F, 0};
+  if (stream_fused(s) && sched) {
+    // both products in one launch; the experts' counters sched[2 .. 2+E) are zero
+    const StreamFused f = stream_fused_cfg(s);
+    const size_t act = std::max(act_bytes(mcap, s.H, sizeof(T)), act_bytes(mcap, s.F, sizeof(T)));
+    const size_t smem = act + (size_t)f.c.stages * f.stage_bytes;
+    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    StreamProduct<T> a = P1, b = P2;
+    a.rps = f.c.rps;
+    b.rps = f.rps1;
+    const int64_t gpe = std::max<int64_t>((s.F + a.rps - 1) / a.rps, (s.H + b.rps - 1) / b.rps);
+    e = launch_kernel(k1, grid(gpe), dim3(kThreads), smem, st, 1, a, b, 2, offs, s.E, mcap, f.c.stages,
+                      f.stage_bytes, (int*)(sched + 2), err);
+    if (e != cudaSuccess) return e;
+    prof_mark(kMarkFirst, st);
+    return cudaSuccess;
+  }
   const StreamCfg c1 = stream_cfg(mcap, s.H, (int)sizeof(T), swi);
   const StreamCfg c2 = stream_cfg(mcap, s.F, (int)sizeof(T), false);
   if (c1.stages < 1 || c2.stages < 1) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c1.smem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c2.smem);
   if (e != cudaSuccess) return e;
-  // one CTA per SM, and no more CTAs than stages of rows to fill
-  auto grid = [&](int N, int rps) {
-    int64_t g = sm_count();
-    const int64_t most = experts * ((N + rps - 1) / rps);
-    if (g > most) g = most;
-    return dim3((unsigned)(g > 0 ? g : 1));
-  };
-  e = launch_kernel(k1, grid(s.F, c1.rps), dim3(kThreads), c1.smem, st, 1, (const T*)x_perm, offs, s.E, mcap,
-                    (const T*)W1, b1, s.F, s.H, c1.rps, c1.stages, (T*)h_perm, err);
+  StreamProduct<T> a = P1, b = P2;
+  a.rps = c1.rps;
+  b.rps = c2.rps;
+  e = launch_kernel(k1, grid((s.F + a.rps - 1) / a.rps), dim3(kThreads), c1.smem, st, 1, a, a, 1, offs, s.E, mcap,
+                    c1.stages, (uint32_t)((size_t)c1.rps * s.H * sizeof(T) * (swi ? 2 : 1)), (int*)nullptr, err);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
-  return launch_kernel(k2, grid(s.H, c2.rps), dim3(kThreads), c2.smem, st, 1, (const T*)h_perm, offs, s.E, mcap,
-                       (const T*)W2, b2, s.H, s.F, c2.rps, c2.stages, (T*)y_perm, err);
+  return launch_kernel(k2, grid((s.H + b.rps - 1) / b.rps), dim3(kThreads), c2.smem, st, 1, b, b, 1, offs, s.E,
+                       mcap, c2.stages, (uint32_t)((size_t)c2.rps * s.F * sizeof(T)), (int*)nullptr, err);
 }
 
 }  // namespace
@@ -296,12 +453,18 @@ bool stream_ffn_eligible(const Shape& s) {
   return stream_cfg(mcap, s.H, s.esize(), swi).stages >= 2 && stream_cfg(mcap, s.F, s.esize(), false).stages >= 2;
 }
 
+// The eligible batches run both products in one launch unless the flags ask
+// for one launch each or the two products' rows do not share a ring.
+bool stream_fused(const Shape& s) {
+  return stream_ffn_eligible(s) && !(s.flags & MOE_FLAG_FFN_SPLIT) && stream_fused_cfg(s).ok;
+}
+
 cudaError_t launch_ffn_stream(const Shape& s, const void* x_perm, const int32_t* offs, const void* W1,
                               const float* b1, const void* W2, const float* b2, void* h_perm,
-                              void* y_perm, int* err, cudaStream_t st) {
+                              void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
   if (s.dtype == MOE_BF16)
-    return run_stream<bf16>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
-  return run_stream<float>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
+    return run_stream<bf16>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
+  return run_stream<float>(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
 }
 
 }  // namespace moe

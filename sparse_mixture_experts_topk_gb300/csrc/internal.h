@@ -112,6 +112,11 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
 // The SM-pair expert GEMMs' counters: two tile counters, then one ready
 // counter per 256-row block of the kept rows (at most rows / 256 + E + 1).
 inline int64_t sched_words(int64_t rows, int E) { return 2 + rows / 256 + E + 1; }
+// Decode-sized batches that run the weight-streaming kernels, and those of
+// them that run both products in one launch (its per-expert counters are
+// sched[2 .. 2 + E)).
+bool stream_ffn_eligible(const Shape& s);
+bool stream_fused(const Shape& s);
 // sched: sched_words(max_rows, E) zeroed ints (the SM-pair kernel's counters)
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,

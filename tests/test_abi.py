@@ -77,7 +77,10 @@ def test_layer_launch_count(lib):
     assert moe.moe_layer_launches(f32) == 1 + 4 + 2 + 1
     decode = moe.make_desc(8, 3584, 32, 2, 2560)
     assert moe.moe_ffn_kernel(decode) == moe.MOE_FFN_STREAM
-    assert moe.moe_layer_launches(decode) == 1 + 1 + 2 + 1
+    assert moe.moe_layer_launches(decode) == 1 + 1 + 1 + 1
+    decode_split = moe.make_desc(8, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_FFN_SPLIT)
+    assert moe.moe_ffn_kernel(decode_split) == moe.MOE_FFN_STREAM_SPLIT
+    assert moe.moe_layer_launches(decode_split) == 1 + 1 + 2 + 1
     assert moe.moe_layer_launches(moe.make_desc(0, 3584, 32, 2, 2560)) == 1
     with pytest.raises(moe.MoeError):
         moe.moe_layer_launches(moe.make_desc(8, 3584, 32, 9, 2560))
