@@ -318,3 +318,23 @@ def test_fused_pair_products_equal_split_launches(name):
     for key in ("h_perm", "y_perm"):
         np.testing.assert_array_equal(to_np(fused[key])[:R], to_np(split[key])[:R], err_msg=key)
     np.testing.assert_array_equal(to_np(fused["out"]), to_np(split["out"]))
+
+
+@pytest.mark.parametrize("name", ["decode4", "one_token", "decode16_all", "swiglu_decode", "decode_f32",
+                                  "swiglu_decode_f32"])
+def test_streamed_products_in_one_launch_equal_two_launches(name):
+    """Decode-sized batches: both weight-streaming products in one launch
+    (the second's activation rows wait on the expert's counter) give the same
+    bits as one launch per product."""
+    w = SMALL[name]
+    dev = Dev(W.generate(w))
+    one = run_stages(dev, flags=0)
+    two = run_stages(dev, flags=moe.MOE_FLAG_FFN_SPLIT)
+    assert one["device_error"] == 0 and two["device_error"] == 0
+    R = int(to_np(one["offs"])[-1])
+    for key in ("h_perm", "y_perm"):
+        np.testing.assert_array_equal(to_np(one[key])[:R], to_np(two[key])[:R], err_msg=key)
+    np.testing.assert_array_equal(to_np(one["out"]), to_np(two["out"]))
+    L = run_layer(dev, flags=0)
+    assert L["device_error"] == 0
+    np.testing.assert_array_equal(to_np(L["out"]), to_np(one["out"]))
