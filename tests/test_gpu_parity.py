@@ -63,6 +63,10 @@ SMALL = {
     # fp32 decode-sized batches: the CUDA-core router and the fp32 streaming kernel
     "decode_f32": W.small("decode_f32", T=3, H=96, E=6, K=2, F=64, dtype=W.F32, ffn_bias=True),
     "swiglu_decode_f32": W.small("swiglu_decode_f32", T=6, H=128, E=8, K=3, F=72, dtype=W.F32, act="swiglu"),
+    # hidden size not a multiple of the 64-wide k-block: the tensor-core router's and the first
+    # expert product's last k-block is partly zero-filled
+    "h_ragged": W.small("h_ragged", T=300, H=200, E=8, K=2, F=264),
+    "h_ragged_decode": W.small("h_ragged_decode", T=5, H=200, E=8, K=2, F=264),
 }
 
 
@@ -259,7 +263,7 @@ def test_heavily_tied_scores_route_like_the_oracle():
 
 @pytest.mark.parametrize("kind", ["single", "pair", "pair_rows", "pair_split"])
 @pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "ffn_bias", "cap_zipf_k4", "e256_k3", "one_token",
-                                  "swiglu_ragged"])
+                                  "swiglu_ragged", "h_ragged"])
 def test_expert_gemm_kernels_match_oracle(name, kind):
     """The tensor-core GEMM kernels (128x256 tiles per SM; SM pairs with the
     token rows on the MMA's N side, the default, or on its M side; SM pairs
