@@ -13,10 +13,15 @@
 //     2-4 stages in shared memory: 100-200 KB in flight per SM;
 //   * consumer warp w dots weight row w of each stage with every activation
 //     row (fp32 sums over 16-byte vectors, a shuffle reduction per row), adds
-//     the bias, applies the activation and stores one output value per row.
-// Every mbarrier wait is bounded; on expiry the kernel records a timeout in
-// the error word, lets the other warps leave, waits (bounded) for the copies
-// it issued and returns.
+//     the bias, applies the activation and stores one output value per row;
+//   * both products run in one launch: the ring carries the first product's
+//     weight rows and then the second's, so the second product's weights
+//     stream right behind the first's, and its activation rows (the first
+//     product's outputs for the expert) are loaded once every CTA of the
+//     expert has stored and fenced its share (a per-expert counter).
+// Every mbarrier wait and counter wait is bounded; on expiry the kernel
+// records a timeout in the error word, lets the other warps leave, waits
+// (bounded) for the copies it issued and returns.
 #include <algorithm>
 
 #include "common.cuh"
