@@ -4,16 +4,18 @@
 // section 2.2: each expert is Linear -> GELU -> Linear), for segments of at
 // most 16 rows.  The time is reading every used expert's weights once, so
 // the kernel is built around bytes in flight rather than arithmetic:
-//   * one CTA per SM; CTA b serves the (b mod A)-th of the A experts that
-//     have rows (found from offs with a warp ballot), and the CTAs of one
-//     expert split its output columns into contiguous ranges;
+//   * one CTA per SM (two for batches of at most 2 tokens); CTA b serves
+//     the (b mod A)-th of the A experts that have rows (found from offs with
+//     a warp ballot), and the CTAs of one expert split its output columns
+//     into contiguous ranges;
 //   * a producer thread moves the expert's activation rows and then, stage
 //     after stage, `rps` consecutive weight rows (one untiled bulk copy per
 //     stage; SwiGLU: a second copy for the matching up rows) into a ring of
 //     2-4 stages in shared memory: 100-200 KB in flight per SM;
-//   * consumer warp w dots weight row w of each stage with every activation
-//     row (fp32 sums over 16-byte vectors, a shuffle reduction per row), adds
-//     the bias, applies the activation and stores one output value per row;
+//   * consumer warps dot the staged weight rows with every activation row
+//     (fp32 sums over 16-byte vectors, a shuffle reduction per row), add the
+//     bias, apply the activation and store one output value per row; row r
+//     of the CTA's range goes to warp r mod 8;
 //   * both products run in one launch: the ring carries the first product's
 //     weight rows and then the second's, so the second product's weights
 //     stream right behind the first's, and its activation rows (the first
@@ -118,20 +120,26 @@ __device__ __forceinline__ StreamRange stream_range(int N, int rps, int nblk, in
   return r;
 }
 
-// Dot the staged weight rows of one stage with the staged activation rows:
-// consumer warp w takes row w (a body sized for the segment, so the hot
-// loop stays small).
-template <typename T, int kEpi>
-__device__ __forceinline__ void stage_rows(const uint8_t* st, int rps, uint32_t row_bytes, const uint4* act, int kv,
-                                           int m, const float* be, int n, int N, T* out) {
-  const int warp = threadIdx.x >> 5;
-  const uint4* wv = reinterpret_cast<const uint4*>(st + (size_t)warp * row_bytes);
-  const uint4* uv = reinterpret_cast<const uint4*>(st + (size_t)(rps + warp) * row_bytes);
+// Dot weight row j of a staged ring stage with the staged activation rows
+// (a body sized for the segment, so the hot loop stays small; kMR bounds the
+// segment, and with it the registers the bodies take).
+template <typename T, int kEpi, int kMR>
+__device__ __forceinline__ void stage_row(const uint8_t* st, int j, int rps, uint32_t row_bytes, const uint4* act,
+                                          int kv, int m, const float* be, int n, int N, T* out) {
+  const uint4* wv = reinterpret_cast<const uint4*>(st + (size_t)j * row_bytes);
+  const uint4* uv = reinterpret_cast<const uint4*>(st + (size_t)(rps + j) * row_bytes);
   if (m <= 1) dot_rows<T, kEpi, 1>(wv, uv, act, kv, m, be, n, N, out);
-  else if (m <= 2) dot_rows<T, kEpi, 2>(wv, uv, act, kv, m, be, n, N, out);
-  else if (m <= 4) dot_rows<T, kEpi, 4>(wv, uv, act, kv, m, be, n, N, out);
-  else if (m <= 8) dot_rows<T, kEpi, 8>(wv, uv, act, kv, m, be, n, N, out);
-  else dot_rows<T, kEpi, kMaxRows>(wv, uv, act, kv, m, be, n, N, out);
+  else if (kMR <= 2 || m <= 2) dot_rows<T, kEpi, 2>(wv, uv, act, kv, m, be, n, N, out);
+  else if (kMR <= 4 || m <= 4) dot_rows<T, kEpi, (kMR < 4 ? kMR : 4)>(wv, uv, act, kv, m, be, n, N, out);
+  else if (kMR <= 8 || m <= 8) dot_rows<T, kEpi, (kMR < 8 ? kMR : 8)>(wv, uv, act, kv, m, be, n, N, out);
+  else dot_rows<T, kEpi, kMR>(wv, uv, act, kv, m, be, n, N, out);
+}
+
+// Row j of stage g (rps rows a stage) is the CTA's row g rps + j of the
+// product, and goes to consumer warp (g rps + j) mod kConsumers: with fewer
+// rows than warps in a stage, the idle warps work on the next stage.
+__device__ __forceinline__ int stage_row_of_warp(int g, int rps, int warp) {
+  return ((warp - g * rps) % kConsumers + kConsumers) % kConsumers;
 }
 
 // Wait (bounded) until *p reaches `need`, acquire at GPU scope, then order
@@ -165,8 +173,8 @@ __device__ __forceinline__ bool wait_count(const int* p, int need, const volatil
 // and the CTA's first consumer waits (bounded) for done[e] to reach the
 // expert's CTA count.  Every CTA finishes its first-product rows without
 // waiting on another CTA, so every such wait ends.
-template <typename T, int kEpi>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, int kEpi, int kMR>
+__global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1)
 stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const int32_t* __restrict__ offs, int E,
                   int mcap, int stages, uint32_t stage_bytes, int* __restrict__ done, int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -289,11 +297,12 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
       const int s = g % stages;
       const uint32_t ph = (uint32_t)(g / stages) & 1u;
       if (!ok || !tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; continue; }
-      const int n = R0.n_begin + g * P0.rps + warp;
-      if (warp < P0.rps && n < R0.n_end)
-        stage_rows<T, kEpi>(ring + (size_t)s * stage_bytes, P0.rps, row0, act, P0.K / V, m,
-                            P0.bias ? P0.bias + (int64_t)e * P0.N * (kSwi ? 2 : 1) : nullptr, n, P0.N,
-                            P0.C + (int64_t)r0 * P0.N + n);
+      const int j = stage_row_of_warp(g, P0.rps, warp);
+      const int n = R0.n_begin + g * P0.rps + j;
+      if (j < P0.rps && n < R0.n_end)
+        stage_row<T, kEpi, kMR>(ring + (size_t)s * stage_bytes, j, P0.rps, row0, act, P0.K / V, m,
+                                P0.bias ? P0.bias + (int64_t)e * P0.N * (kSwi ? 2 : 1) : nullptr, n, P0.N,
+                                P0.C + (int64_t)r0 * P0.N + n);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(s));   // this warp is done with the stage
     }
@@ -317,11 +326,12 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
         const int s = g % stages;
         const uint32_t ph = (uint32_t)(g / stages) & 1u;
         if (!ok || !tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; continue; }
-        const int n = R1.n_begin + (g - R0.groups) * P1.rps + warp;
-        if (warp < P1.rps && n < R1.n_end)
-          stage_rows<T, kEpiPlain>(ring + (size_t)s * stage_bytes, P1.rps, row1, act, P1.K / V, m,
-                                   P1.bias ? P1.bias + (int64_t)e * P1.N : nullptr, n, P1.N,
-                                   P1.C + (int64_t)r0 * P1.N + n);
+        const int j = stage_row_of_warp(g - R0.groups, P1.rps, warp);
+        const int n = R1.n_begin + (g - R0.groups) * P1.rps + j;
+        if (j < P1.rps && n < R1.n_end)
+          stage_row<T, kEpiPlain, kMR>(ring + (size_t)s * stage_bytes, j, P1.rps, row1, act, P1.K / V, m,
+                                       P1.bias ? P1.bias + (int64_t)e * P1.N : nullptr, n, P1.N,
+                                       P1.C + (int64_t)r0 * P1.N + n);
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(empty(s));
       }
@@ -349,10 +359,10 @@ struct StreamCfg {
   size_t smem;
 };
 
-StreamCfg stream_cfg_room(size_t act, size_t row) {
+StreamCfg stream_cfg_room(size_t act, size_t row, size_t budget = kSmemBudget) {
   StreamCfg c{1, 0, 0};
   for (int rps = kConsumers; rps >= 1; rps /= 2) {
-    const size_t room = kSmemBudget > act ? kSmemBudget - act : 0;
+    const size_t room = budget > act ? budget - act : 0;
     size_t st = room / ((size_t)rps * row);
     if (st > (size_t)kMaxStages) st = kMaxStages;
     if (st >= 2 || rps == 1) {
@@ -379,13 +389,17 @@ struct StreamFused {
   uint32_t stage_bytes;
 };
 
+// Batches of at most kPairRows tokens run two CTAs per SM (bodies for at
+// most 2 rows, so both fit the register file), each with half the ring.
+constexpr int kPairRows = 2;
+
 StreamFused stream_fused_cfg(const Shape& s) {
   StreamFused f{};
   const int mcap = (int)(s.T < kMaxRows ? s.T : kMaxRows);
   const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
   const int es = s.esize();
   const size_t act = std::max(act_bytes(mcap, s.H, es), act_bytes(mcap, s.F, es));
-  f.c = stream_cfg_room(act, (size_t)s.H * es * (swi ? 2 : 1));
+  f.c = stream_cfg_room(act, (size_t)s.H * es * (swi ? 2 : 1), mcap <= kPairRows ? kSmemBudget / 2 : kSmemBudget);
   f.stage_bytes = (uint32_t)((size_t)f.c.rps * s.H * es * (swi ? 2 : 1));
   const size_t r1 = f.stage_bytes / ((size_t)s.F * es);
   f.rps1 = (int)(r1 < (size_t)kConsumers ? r1 : kConsumers);
@@ -400,11 +414,13 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
   const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
   const int64_t experts = s.S() < s.E ? s.S() : s.E;   // at most T*K experts have rows
   const int mcap = (int)(s.T < kMaxRows ? s.T : kMaxRows);
-  auto k1 = swi ? stream_ffn_kernel<T, kEpiSwiglu> : stream_ffn_kernel<T, kEpiGelu>;
-  auto k2 = stream_ffn_kernel<T, kEpiPlain>;
-  // one CTA per SM, and no more CTAs than stages of rows to fill
-  auto grid = [&](int64_t groups_per_expert) {
-    int64_t g = sm_count();
+  auto k1 = swi ? stream_ffn_kernel<T, kEpiSwiglu, kMaxRows> : stream_ffn_kernel<T, kEpiGelu, kMaxRows>;
+  auto k2 = stream_ffn_kernel<T, kEpiPlain, kMaxRows>;
+  auto k1p = swi ? stream_ffn_kernel<T, kEpiSwiglu, kPairRows> : stream_ffn_kernel<T, kEpiGelu, kPairRows>;
+  const int per_sm = mcap <= kPairRows ? 2 : 1;
+  // per_sm CTAs per SM, and no more CTAs than stages of rows to fill
+  auto grid = [&](int64_t groups_per_expert, int ctas_per_sm) {
+    int64_t g = (int64_t)sm_count() * ctas_per_sm;
     const int64_t most = experts * groups_per_expert;
     if (g > most) g = most;
     return dim3((unsigned)(g > 0 ? g : 1));
@@ -416,13 +432,14 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
     const StreamFused f = stream_fused_cfg(s);
     const size_t act = std::max(act_bytes(mcap, s.H, sizeof(T)), act_bytes(mcap, s.F, sizeof(T)));
     const size_t smem = act + (size_t)f.c.stages * f.stage_bytes;
-    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kf = per_sm > 1 ? k1p : k1;
+    cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     StreamProduct<T> a = P1, b = P2;
     a.rps = f.c.rps;
     b.rps = f.rps1;
     const int64_t gpe = std::max<int64_t>((s.F + a.rps - 1) / a.rps, (s.H + b.rps - 1) / b.rps);
-    e = launch_kernel(k1, grid(gpe), dim3(kThreads), smem, st, 1, a, b, 2, offs, s.E, mcap, f.c.stages,
+    e = launch_kernel(kf, grid(gpe, per_sm), dim3(kThreads), smem, st, 1, a, b, 2, offs, s.E, mcap, f.c.stages,
                       f.stage_bytes, (int*)(sched + 2), err);
     if (e != cudaSuccess) return e;
     prof_mark(kMarkFirst, st);
@@ -437,11 +454,11 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
   StreamProduct<T> a = P1, b = P2;
   a.rps = c1.rps;
   b.rps = c2.rps;
-  e = launch_kernel(k1, grid((s.F + a.rps - 1) / a.rps), dim3(kThreads), c1.smem, st, 1, a, a, 1, offs, s.E, mcap,
+  e = launch_kernel(k1, grid((s.F + a.rps - 1) / a.rps, 1), dim3(kThreads), c1.smem, st, 1, a, a, 1, offs, s.E, mcap,
                     c1.stages, (uint32_t)((size_t)c1.rps * s.H * sizeof(T) * (swi ? 2 : 1)), (int*)nullptr, err);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
-  return launch_kernel(k2, grid((s.H + b.rps - 1) / b.rps), dim3(kThreads), c2.smem, st, 1, b, b, 1, offs, s.E,
+  return launch_kernel(k2, grid((s.H + b.rps - 1) / b.rps, 1), dim3(kThreads), c2.smem, st, 1, b, b, 1, offs, s.E,
                        mcap, c2.stages, (uint32_t)((size_t)c2.rps * s.F * sizeof(T)), (int*)nullptr, err);
 }
 
