@@ -1,0 +1,48 @@
+"""Host-side pieces of bench.py that need no GPU: the oracle arm's JSON line and
+the CPU-baseline sample, which must never credit the oracle with more tokens
+than the batch holds."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from sparse_mixture_experts_topk_gb300 import workloads as W  # noqa: E402
+
+
+@pytest.mark.parametrize("T", [1, 3, 64, 100])
+def test_cpu_baseline_counts_only_the_batch(T):
+    w = W.small("cb", T=T, H=64, E=4, K=2, F=32, dtype=W.F32)
+    inp = W.generate(w)
+    cb = bench.cpu_baseline(inp, 0.05)
+    n = int(cb["sample"].split("first ")[1].split(" of ")[0])
+    assert 0 < n <= T
+    assert f"of {T} tokens" in cb["sample"]
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0
+
+
+def test_oracle_rate_rejects_more_tokens_than_the_batch():
+    w = W.small("cb", T=2, H=64, E=4, K=2, F=32, dtype=W.F32)
+    inp = W.generate(w)
+    with pytest.raises(AssertionError):
+        bench.oracle_rate(inp, bench.widen_inputs(inp), 3)
+
+
+def test_reference_arm_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["config"]["sample_tokens_per_step"] <= W.WORKLOADS["tiny"].T
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
