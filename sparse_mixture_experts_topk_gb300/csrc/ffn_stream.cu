@@ -11,7 +11,8 @@
 //   * a producer thread moves the expert's activation rows and then, stage
 //     after stage, `rps` consecutive weight rows (one untiled bulk copy per
 //     stage; SwiGLU: a second copy for the matching up rows) into a ring of
-//     2-4 stages in shared memory: 100-200 KB in flight per SM;
+//     2-6 stages in shared memory (as many as fit beside the expert's
+//     activation rows): 100-200 KB in flight per SM;
 //   * consumer warps dot the staged weight rows with every activation row
 //     (fp32 sums over 16-byte vectors, a shuffle reduction per row), add the
 //     bias, apply the activation and store one output value per row; row r
@@ -25,6 +26,7 @@
 // records a timeout in the error word, lets the other warps leave, waits
 // (bounded) for the copies it issued and returns.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -37,16 +39,38 @@ namespace {
 constexpr int kMaxRows = 16;
 constexpr int kConsumers = 8;                    // consumer warps; a stage holds <= 8 rows
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr size_t kSmemBudget = 220 * 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __host__ __device__ inline size_t act_bytes(int mcap, int K, int esize) { return ((size_t)mcap * K * esize + 127) / 128 * 128; }
 
+// acc + x.lo w.lo + x.hi w.hi for bf16 pairs packed in 32-bit words: two
+// fused multiply-adds with bf16 operands and an fp32 addend and result.  A
+// product of two bf16 values is exact in fp32, so each step rounds once,
+// exactly like fmaf on the widened values, without widening them first.
+__device__ __forceinline__ float fma2_bf16(uint32_t x, uint32_t w, float acc) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %1;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(x), "r"(w));
+  return acc;
+}
+__device__ __forceinline__ float fma8_bf16(const uint4& x, const uint4& w, float acc) {
+  acc = fma2_bf16(x.x, w.x, acc);
+  acc = fma2_bf16(x.y, w.y, acc);
+  acc = fma2_bf16(x.z, w.z, acc);
+  return fma2_bf16(x.w, w.w, acc);
+}
+
 // One weight row (SwiGLU: gate row w and up row u) against the m <= MR
 // staged activation rows: lane l takes vectors l, l + 32, ...; fp32 sums,
 // reduced across the warp; lane 0 adds the bias, applies the activation and
-// writes out[r * N] for r < m.
+// writes out[r * N] for r < m.  bf16 rows are multiplied without widening
+// (fma8_bf16); fp32 rows element by element.
 template <typename T, int kEpi, int MR>
 __device__ __forceinline__ void dot_rows(const uint4* w, const uint4* u, const uint4* act, int kv, int m,
                                          const float* be, int n, int N, T* out) {
@@ -58,18 +82,25 @@ __device__ __forceinline__ void dot_rows(const uint4* w, const uint4* u, const u
   for (int r = 0; r < MR; ++r) acc[r] = accu[r] = 0.f;
 #pragma unroll 2
   for (int v = lane; v < kv; v += 32) {
-    float b[V], bu[V];
-    Vec<T>::unpack(w[v], b);
-    if (kSwi) Vec<T>::unpack(u[v], bu);
+    const uint4 wq = w[v];
+    const uint4 uq = kSwi ? u[v] : wq;
 #pragma unroll
     for (int r = 0; r < MR; ++r) {
       if (r < m) {
-        float x[V];
-        Vec<T>::unpack(act[r * kv + v], x);
+        const uint4 xq = act[r * kv + v];
+        if constexpr (std::is_same<T, bf16>::value) {
+          acc[r] = fma8_bf16(xq, wq, acc[r]);
+          if (kSwi) accu[r] = fma8_bf16(xq, uq, accu[r]);
+        } else {
+          float x[V], b[V], bu[V];
+          Vec<T>::unpack(xq, x);
+          Vec<T>::unpack(wq, b);
+          if (kSwi) Vec<T>::unpack(uq, bu);
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-          acc[r] = fmaf(x[i], b[i], acc[r]);
-          if (kSwi) accu[r] = fmaf(x[i], bu[i], accu[r]);
+          for (int i = 0; i < V; ++i) {
+            acc[r] = fmaf(x[i], b[i], acc[r]);
+            if (kSwi) accu[r] = fmaf(x[i], bu[i], accu[r]);
+          }
         }
       }
     }
@@ -176,7 +207,7 @@ __device__ __forceinline__ bool wait_count(const int* p, int need, const volatil
 template <typename T, int kEpi, int kMR>
 __global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1)
 stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const int32_t* __restrict__ offs, int E,
-                  int mcap, int stages, uint32_t stage_bytes, int* __restrict__ done, int* err) {
+                  int mcap, uint32_t dyn_bytes, uint32_t stage_bytes, int* __restrict__ done, int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_e, s_na, s_abort, s_act1;
   __shared__ __align__(8) uint64_t s_bar[2 * kMaxStages + 1];
@@ -184,15 +215,12 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
   constexpr int V = Vec<T>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t s_act = tc::smem_u32(smem);
-  const uint32_t act_room = (uint32_t)max(act_bytes(mcap, P0.K, sizeof(T)),
-                                          nphase > 1 ? act_bytes(mcap, P1.K, sizeof(T)) : (size_t)0);
-  const uint32_t s_ring = s_act + act_room;
   auto full = [&](int s) { return tc::smem_u32(&s_bar[s]); };
   auto empty = [&](int s) { return tc::smem_u32(&s_bar[kMaxStages + s]); };
   const uint32_t act_bar = tc::smem_u32(&s_bar[2 * kMaxStages]);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       tc::mbar_init(full(s), 1);
       tc::mbar_init(empty(s), kConsumers);
     }
@@ -240,6 +268,13 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
     if (threadIdx.x == 0) set_error(err, kDevBadIndex);
     m = mcap;
   }
+  // the expert's activation rows first, then as many ring stages as the rest
+  // of the shared memory holds (the launch leaves room for at least two
+  // beside mcap rows; an expert with fewer rows gets a deeper ring)
+  const uint32_t act_room = (uint32_t)max(act_bytes(m, P0.K, sizeof(T)),
+                                          nphase > 1 ? act_bytes(m, P1.K, sizeof(T)) : (size_t)0);
+  const int stages = min(kMaxStages, (int)((dyn_bytes - act_room) / stage_bytes));
+  const uint32_t s_ring = s_act + act_room;
   // this CTA's share of expert e in each product
   const int a = (int)(blockIdx.x % (unsigned)na);
   const int nblk = ((int)gridDim.x - 1 - a) / na + 1;
@@ -351,27 +386,27 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
   }
 }
 
-// Rows per stage and ring depth for one product: the most rows per stage
-// that still leave room for two stages beside `act` bytes of activation
-// rows.
+// Rows per stage for one product, and the ring depth it guarantees: the
+// most rows per stage (8, 4, 2 or 1) that leave room for two stages beside
+// act_max bytes of activation rows (mcap rows).  The launch takes the whole
+// budget of shared memory; in it an expert's activation rows come first and
+// the ring takes what is left, so an expert with fewer rows gets a deeper
+// ring (at one activation row of 7 KB, three 8-row stages instead of two).
 struct StreamCfg {
-  int rps, stages;
+  int rps, stages;   // stages: the depth with mcap rows staged
   size_t smem;
 };
 
-StreamCfg stream_cfg_room(size_t act, size_t row, size_t budget = kSmemBudget) {
-  StreamCfg c{1, 0, 0};
+StreamCfg stream_cfg_room(size_t act_max, size_t row, size_t budget = kSmemBudget) {
+  StreamCfg c{1, 0, budget};
   for (int rps = kConsumers; rps >= 1; rps /= 2) {
-    const size_t room = budget > act ? budget - act : 0;
-    size_t st = room / ((size_t)rps * row);
-    if (st > (size_t)kMaxStages) st = kMaxStages;
-    if (st >= 2 || rps == 1) {
+    const size_t lo = budget > act_max ? (budget - act_max) / ((size_t)rps * row) : 0;
+    if (lo >= 2 || rps == 1) {
       c.rps = rps;
-      c.stages = (int)st;
+      c.stages = (int)std::min<size_t>(lo, kMaxStages);
       break;
     }
   }
-  c.smem = act + (size_t)c.stages * c.rps * row;
   return c;
 }
 
@@ -430,8 +465,7 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
   if (stream_fused(s) && sched) {
     // both products in one launch; the experts' counters sched[2 .. 2+E) are zero
     const StreamFused f = stream_fused_cfg(s);
-    const size_t act = std::max(act_bytes(mcap, s.H, sizeof(T)), act_bytes(mcap, s.F, sizeof(T)));
-    const size_t smem = act + (size_t)f.c.stages * f.stage_bytes;
+    const size_t smem = f.c.smem;
     auto kf = per_sm > 1 ? k1p : k1;
     cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -439,8 +473,8 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
     a.rps = f.c.rps;
     b.rps = f.rps1;
     const int64_t gpe = std::max<int64_t>((s.F + a.rps - 1) / a.rps, (s.H + b.rps - 1) / b.rps);
-    e = launch_kernel(kf, grid(gpe, per_sm), dim3(kThreads), smem, st, 1, a, b, 2, offs, s.E, mcap, f.c.stages,
-                      f.stage_bytes, (int*)(sched + 2), err);
+    e = launch_kernel(kf, grid(gpe, per_sm), dim3(kThreads), smem, st, 1, a, b, 2, offs, s.E, mcap,
+                      (uint32_t)smem, f.stage_bytes, (int*)(sched + 2), err);
     if (e != cudaSuccess) return e;
     prof_mark(kMarkFirst, st);
     return cudaSuccess;
@@ -455,11 +489,12 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
   a.rps = c1.rps;
   b.rps = c2.rps;
   e = launch_kernel(k1, grid((s.F + a.rps - 1) / a.rps, 1), dim3(kThreads), c1.smem, st, 1, a, a, 1, offs, s.E, mcap,
-                    c1.stages, (uint32_t)((size_t)c1.rps * s.H * sizeof(T) * (swi ? 2 : 1)), (int*)nullptr, err);
+                    (uint32_t)c1.smem, (uint32_t)((size_t)c1.rps * s.H * sizeof(T) * (swi ? 2 : 1)), (int*)nullptr,
+                    err);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
   return launch_kernel(k2, grid((s.H + b.rps - 1) / b.rps, 1), dim3(kThreads), c2.smem, st, 1, b, b, 1, offs, s.E,
-                       mcap, c2.stages, (uint32_t)((size_t)c2.rps * s.F * sizeof(T)), (int*)nullptr, err);
+                       mcap, (uint32_t)c2.smem, (uint32_t)((size_t)c2.rps * s.F * sizeof(T)), (int*)nullptr, err);
 }
 
 }  // namespace
