@@ -135,21 +135,25 @@ class Clocks:
                 "reasons": reasons, "samples": len(sel), "window": window}
 
 
-def source_hash() -> str:
+GEMM_SOURCES = ("ffn_tc.cu", "ffn_tc2.cu", "tc_ptx.cuh", "common.cuh")
+STREAM_SOURCES = ("ffn_stream.cu", "tc_ptx.cuh", "common.cuh")
+
+
+def source_hash(files=GEMM_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("ffn_tc.cu", "ffn_tc2.cu", "tc_ptx.cuh", "common.cuh"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "sparse_mixture_experts_topk_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, files=GEMM_SOURCES):
     """DRAM bytes per launch of each expert product from the committed ncu
     summary (profiles/traffic.json), if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
         e = d[workload]
-        if e.get("source_hash") == source_hash():
+        if e.get("source_hash") == source_hash(files):
             return e
     except Exception:
         pass
@@ -357,7 +361,8 @@ def run_ours(args, w: W.Workload):
         roof = {"kernel": "weight-streaming expert kernel (both products, one launch)" if fused
                 else f"weight-streaming expert kernel ({dom})", "bound": "hbm", "achieved": achieved,
                 "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{src} HBM copy",
-                "traffic": None, "algorithmic_bytes_per_launch": work[dom + "_bytes"]}
+                "traffic": (ncu_traffic(w.name, STREAM_SOURCES) or {}).get(dom),
+                "algorithmic_bytes_per_launch": work[dom + "_bytes"]}
     else:
         achieved = flops[dom] / (dom_ms / 1e3) / 1e12
         traffic = ncu_traffic(w.name)
