@@ -14,9 +14,10 @@
 //     2-6 stages in shared memory (as many as fit beside the expert's
 //     activation rows): 100-200 KB in flight per SM;
 //   * consumer warps dot the staged weight rows with every activation row
-//     (fp32 sums over 16-byte vectors, a shuffle reduction per row), add the
-//     bias, apply the activation and store one output value per row; row r
-//     of the CTA's range goes to warp r mod 8;
+//     (bf16 operands multiplied into fp32 sums over 16-byte vectors, a
+//     shuffle reduction per row), add the bias, apply the activation and
+//     store one output value per row; row r of the CTA's range goes to
+//     warp r mod 8;
 //   * both products run in one launch: the ring carries the first product's
 //     weight rows and then the second's, so the second product's weights
 //     stream right behind the first's, and its activation rows (the first
