@@ -136,7 +136,7 @@ class Clocks:
 
 
 GEMM_SOURCES = ("ffn_tc.cu", "ffn_tc2.cu", "tc_ptx.cuh", "common.cuh")
-STREAM_SOURCES = ("ffn_stream.cu", "tc_ptx.cuh", "common.cuh")
+STREAM_SOURCES = ("ffn_stream.cu", "bf16_dot.cuh", "tc_ptx.cuh", "common.cuh")
 
 
 def source_hash(files=GEMM_SOURCES) -> str:

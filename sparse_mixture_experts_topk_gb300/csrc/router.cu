@@ -10,6 +10,7 @@
 // router temperature, MoE sparse-activation article, wmrh.cn, section 5.2).
 #include <float.h>
 
+#include "bf16_dot.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -206,7 +207,6 @@ inline size_t small_smem(int64_t T, int H, int E) {
 template <int MR>
 __device__ __forceinline__ void small_unit(const uint4 (&gw)[kSmallChunk], const uint4* s_x, int kv, int c0,
                                            int Tn, int E, uint32_t dst) {
-  constexpr int V = Vec<bf16>::N;
   const int lane = threadIdx.x & 31;
   float acc[MR];
 #pragma unroll
@@ -215,17 +215,9 @@ __device__ __forceinline__ void small_unit(const uint4 (&gw)[kSmallChunk], const
   for (int u = 0; u < kSmallChunk; ++u) {
     const int v = c0 + lane + 32 * u;
     if (v < kv) {
-      float b[V];
-      Vec<bf16>::unpack(gw[u], b);
 #pragma unroll
-      for (int t = 0; t < MR; ++t) {
-        if (t < Tn) {
-          float a[V];
-          Vec<bf16>::unpack(s_x[t * kv + v], a);
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc[t] = fmaf(a[i], b[i], acc[t]);
-        }
-      }
+      for (int t = 0; t < MR; ++t)
+        if (t < Tn) acc[t] = fma8_bf16(s_x[t * kv + v], gw[u], acc[t]);
     }
   }
 #pragma unroll

@@ -46,3 +46,17 @@ def test_reference_arm_line():
     assert d["config"]["sample_tokens_per_step"] <= W.WORKLOADS["tiny"].T
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+
+
+def test_ncu_traffic_follows_the_kernel_sources():
+    """Measured DRAM bytes are reported only for the kernel sources they were
+    taken on: an entry is keyed by the hash of its kernel's files."""
+    assert bench.ncu_traffic("no such workload") is None
+    stream = bench.ncu_traffic("decode8", bench.STREAM_SOURCES)
+    if stream is not None:
+        assert stream["ffn"] > 0
+        # the same entry checked against the tensor-core GEMM's files does not match
+        assert bench.ncu_traffic("decode8", bench.GEMM_SOURCES) is None
+    gemm = bench.ncu_traffic("prefill", bench.GEMM_SOURCES)
+    if gemm is not None:
+        assert bench.ncu_traffic("prefill", bench.STREAM_SOURCES) is None
