@@ -66,6 +66,8 @@ WORKLOADS = {
     # decode-sized batches; x is built so token t routes to experts 2t, 2t+1
     "decode1": Workload("decode1", T=1, H=3584, E=32, K=2, F=2560, x_kind="decode_distinct"),
     "decode8": Workload("decode8", T=8, H=3584, E=32, K=2, F=2560, x_kind="decode_distinct"),
+    # a 16-token decode batch routed by the gate as it falls: experts get 0-3 rows
+    "decode16r": Workload("decode16r", T=16, H=3584, E=32, K=2, F=2560),
     # top-4 with a Zipf(1.2) gate bias and capacity ceil(T/E)*k = 2048
     "zipf_cap": Workload("zipf_cap", T=16384, H=3584, E=32, K=4, F=2560,
                          capacity=capacity_ceil(16384, 32, 4), gate_bias="zipf"),
