@@ -188,7 +188,7 @@ __device__ __forceinline__ bool wait_count(const int* p, int need, const volatil
 template <typename T, int kEpi, int kMR>
 __global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1)
 stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const int32_t* __restrict__ offs, int E,
-                  int mcap, uint32_t dyn_bytes, uint32_t stage_bytes, int* __restrict__ done, int* err) {
+                  int mcap, uint32_t dyn_bytes, int* __restrict__ done, int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_e, s_na, s_abort, s_act1;
   __shared__ __align__(8) uint64_t s_bar[2 * kMaxStages + 1];
@@ -249,21 +249,33 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
     if (threadIdx.x == 0) set_error(err, kDevBadIndex);
     m = mcap;
   }
-  // the expert's activation rows first, then as many ring stages as the rest
-  // of the shared memory holds (the launch leaves room for at least two
-  // beside mcap rows; an expert with fewer rows gets a deeper ring)
+  // the expert's activation rows first, then the ring in the rest of the
+  // shared memory.  The launch's P0.rps rows per stage leave room for two
+  // stages beside mcap rows; with fewer rows staged the CTA takes the most
+  // rows per stage (up to kConsumers) that still leave three stages, and as
+  // many stages as fit.  A second-product stage holds as many of its rows
+  // as fit the same bytes.
   const uint32_t act_room = (uint32_t)max(act_bytes(m, P0.K, sizeof(T)),
                                           nphase > 1 ? act_bytes(m, P1.K, sizeof(T)) : (size_t)0);
-  const int stages = min(kMaxStages, (int)((dyn_bytes - act_room) / stage_bytes));
+  const uint32_t row0 = (uint32_t)P0.K * sizeof(T), row1 = (uint32_t)P1.K * sizeof(T);
+  const uint32_t room = dyn_bytes - act_room, wrow0 = row0 * (kSwi ? 2u : 1u);
+  int rps0 = P0.rps;
+  for (int r = kConsumers; r > P0.rps; r >>= 1)
+    if (room / ((uint32_t)r * wrow0) >= 3u) {
+      rps0 = r;
+      break;
+    }
+  const uint32_t stage_bytes = (uint32_t)rps0 * wrow0;
+  const int rps1 = min(kConsumers, (int)(stage_bytes / row1));
+  const int stages = min(kMaxStages, (int)(room / stage_bytes));
   const uint32_t s_ring = s_act + act_room;
   // this CTA's share of expert e in each product
   const int a = (int)(blockIdx.x % (unsigned)na);
   const int nblk = ((int)gridDim.x - 1 - a) / na + 1;
   const int slot = (int)(blockIdx.x / (unsigned)na);
-  const StreamRange R0 = stream_range(P0.N, P0.rps, nblk, slot);
-  const StreamRange R1 = nphase > 1 ? stream_range(P1.N, P1.rps, nblk, slot) : StreamRange{0, 0, 0};
+  const StreamRange R0 = stream_range(P0.N, rps0, nblk, slot);
+  const StreamRange R1 = nphase > 1 ? stream_range(P1.N, rps1, nblk, slot) : StreamRange{0, 0, 0};
   const int total = R0.groups + R1.groups;
-  const uint32_t row0 = (uint32_t)P0.K * sizeof(T), row1 = (uint32_t)P1.K * sizeof(T);
 
   uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
   bool producer = false;
@@ -280,15 +292,15 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
         if (!tc::mbar_wait(empty(s), ph ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
         const uint32_t dst = s_ring + (uint32_t)s * stage_bytes;
         if (g < R0.groups) {
-          const int n0 = R0.n_begin + g * P0.rps;
-          const uint32_t bytes = (uint32_t)min(P0.rps, R0.n_end - n0) * row0;
+          const int n0 = R0.n_begin + g * rps0;
+          const uint32_t bytes = (uint32_t)min(rps0, R0.n_end - n0) * row0;
           const T* Be = P0.B + (int64_t)e * P0.N * P0.K * (kSwi ? 2 : 1);
           tc::mbar_arrive_expect_tx(full(s), kSwi ? 2 * bytes : bytes);
           tc::bulk_load(dst, Be + (int64_t)n0 * P0.K, bytes, full(s));
-          if (kSwi) tc::bulk_load(dst + (uint32_t)P0.rps * row0, Be + (int64_t)(P0.N + n0) * P0.K, bytes, full(s));
+          if (kSwi) tc::bulk_load(dst + (uint32_t)rps0 * row0, Be + (int64_t)(P0.N + n0) * P0.K, bytes, full(s));
         } else {
-          const int n0 = R1.n_begin + (g - R0.groups) * P1.rps;
-          const uint32_t bytes = (uint32_t)min(P1.rps, R1.n_end - n0) * row1;
+          const int n0 = R1.n_begin + (g - R0.groups) * rps1;
+          const uint32_t bytes = (uint32_t)min(rps1, R1.n_end - n0) * row1;
           tc::mbar_arrive_expect_tx(full(s), bytes);
           tc::bulk_load(dst, P1.B + ((int64_t)e * P1.N + n0) * P1.K, bytes, full(s));
         }
@@ -313,10 +325,10 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
       const int s = g % stages;
       const uint32_t ph = (uint32_t)(g / stages) & 1u;
       if (!ok || !tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; continue; }
-      const int j = stage_row_of_warp(g, P0.rps, warp);
-      const int n = R0.n_begin + g * P0.rps + j;
-      if (j < P0.rps && n < R0.n_end)
-        stage_row<T, kEpi, kMR>(ring + (size_t)s * stage_bytes, j, P0.rps, row0, act, P0.K / V, m,
+      const int j = stage_row_of_warp(g, rps0, warp);
+      const int n = R0.n_begin + g * rps0 + j;
+      if (j < rps0 && n < R0.n_end)
+        stage_row<T, kEpi, kMR>(ring + (size_t)s * stage_bytes, j, rps0, row0, act, P0.K / V, m,
                                 P0.bias ? P0.bias + (int64_t)e * P0.N * (kSwi ? 2 : 1) : nullptr, n, P0.N,
                                 P0.C + (int64_t)r0 * P0.N + n);
       __syncwarp();
@@ -342,10 +354,10 @@ stream_ffn_kernel(StreamProduct<T> P0, StreamProduct<T> P1, int nphase, const in
         const int s = g % stages;
         const uint32_t ph = (uint32_t)(g / stages) & 1u;
         if (!ok || !tc::mbar_wait(full(s), ph, &s_abort, kWaitNs)) { ok = false; continue; }
-        const int j = stage_row_of_warp(g - R0.groups, P1.rps, warp);
-        const int n = R1.n_begin + (g - R0.groups) * P1.rps + j;
-        if (j < P1.rps && n < R1.n_end)
-          stage_row<T, kEpiPlain, kMR>(ring + (size_t)s * stage_bytes, j, P1.rps, row1, act, P1.K / V, m,
+        const int j = stage_row_of_warp(g - R0.groups, rps1, warp);
+        const int n = R1.n_begin + (g - R0.groups) * rps1 + j;
+        if (j < rps1 && n < R1.n_end)
+          stage_row<T, kEpiPlain, kMR>(ring + (size_t)s * stage_bytes, j, rps1, row1, act, P1.K / V, m,
                                        P1.bias ? P1.bias + (int64_t)e * P1.N : nullptr, n, P1.N,
                                        P1.C + (int64_t)r0 * P1.N + n);
         __syncwarp();
@@ -455,7 +467,7 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
     b.rps = f.rps1;
     const int64_t gpe = std::max<int64_t>((s.F + a.rps - 1) / a.rps, (s.H + b.rps - 1) / b.rps);
     e = launch_kernel(kf, grid(gpe, per_sm), dim3(kThreads), smem, st, 1, a, b, 2, offs, s.E, mcap,
-                      (uint32_t)smem, f.stage_bytes, (int*)(sched + 2), err);
+                      (uint32_t)smem, (int*)(sched + 2), err);
     if (e != cudaSuccess) return e;
     prof_mark(kMarkFirst, st);
     return cudaSuccess;
@@ -470,12 +482,11 @@ cudaError_t run_stream(const Shape& s, const void* x_perm, const int32_t* offs, 
   a.rps = c1.rps;
   b.rps = c2.rps;
   e = launch_kernel(k1, grid((s.F + a.rps - 1) / a.rps, 1), dim3(kThreads), c1.smem, st, 1, a, a, 1, offs, s.E, mcap,
-                    (uint32_t)c1.smem, (uint32_t)((size_t)c1.rps * s.H * sizeof(T) * (swi ? 2 : 1)), (int*)nullptr,
-                    err);
+                    (uint32_t)c1.smem, (int*)nullptr, err);
   if (e != cudaSuccess) return e;
   prof_mark(kMarkFirst, st);
   return launch_kernel(k2, grid((s.H + b.rps - 1) / b.rps, 1), dim3(kThreads), c2.smem, st, 1, b, b, 1, offs, s.E,
-                       mcap, (uint32_t)c2.smem, (uint32_t)((size_t)c2.rps * s.F * sizeof(T)), (int*)nullptr, err);
+                       mcap, (uint32_t)c2.smem, (int*)nullptr, err);
 }
 
 }  // namespace
