@@ -357,12 +357,14 @@ cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const f
   const int64_t grid = router_partials(s);
   if (s.dtype == MOE_BF16) {
     auto k = router_simt_kernel<bf16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kRouterThreads), smem, st, 1, (const bf16*)x,
                          (const bf16*)Wg, gate_bias, s.T, s.H, s.E, s.K, s.inv_tau, logits, ids, w, psum_part);
   }
   auto k = router_simt_kernel<float>;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   return launch_kernel(k, dim3((unsigned)grid), dim3(kRouterThreads), smem, st, 1, (const float*)x,
                        (const float*)Wg, gate_bias, s.T, s.H, s.E, s.K, s.inv_tau, logits, ids, w, psum_part);
 }
