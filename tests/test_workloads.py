@@ -65,3 +65,17 @@ def test_hot_gate_bias_sends_every_token_to_the_first_k_experts():
     l = O.gate_logits(O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype), inp.gate_bias)
     ids, _, _ = O.route(l, w.K)
     assert set(np.unique(ids)) == {0, 1}
+
+
+def test_decode16r_recipe_gives_experts_several_rows():
+    """The 16-token decode batch is routed by the gate as it falls, so some
+    experts stream with several activation rows (the streaming kernel's
+    per-CTA stage sizing depends on it) and none with more than the batch."""
+    w = W.WORKLOADS["decode16r"]
+    Wg = W.gen_gate(w)
+    x = W.gen_x(w, Wg)
+    l = O.gate_logits(O.widen(x, w.dtype), O.widen(Wg, w.dtype))
+    count = np.bincount(O.topk_select(l, w.K).ravel(), minlength=w.E)
+    assert count.sum() == w.T * w.K
+    assert count.max() >= 2 and count.max() <= w.T
+    assert (count > 0).sum() < w.T * w.K              # shared experts, not 32 distinct ones
