@@ -179,12 +179,15 @@ int moe_dispatch(const moe_desc* desc, const int32_t* ids, const void* x,
  *   a nonzero code if an id is out of range (such slots are dropped).
  * The per-block histograms live in a 64 KiB array in device memory owned by
  * the library (held by every GPU that loads it until the process exits).  The
- * layer must fit it: E * blocks <= 8192, where blocks = ceil(T*K / 2048) for
- * T*K <= 131072 and 64 above (so E <= 128 always fits, E = 256 up to
- * T*K = 65536); larger layers get MOE_ERR_UNSUPPORTED.  The call allocates
- * nothing.  The first call on each device looks up the array's address (make
- * it before any stream capture).  All calls on a device share the array:
- * calls that overlap on the GPU race and must be serialised by the caller.
+ * layer must fit it: E * blocks <= 8192, where for S = T*K slots
+ * blocks = ceil(S / b), b = max(2048, ceil(S / 64)) rounded up to a multiple
+ * of 256 (so at most 64 blocks: E <= 128 always fits, E = 256 up to
+ * S = 65536); larger layers get MOE_ERR_UNSUPPORTED.  The call allocates
+ * nothing.  Each call outside stream capture looks up the array's address on
+ * the current device; a call during capture reuses the last one, so make the
+ * first call on each device before any stream capture (and one more after a
+ * device reset).  All calls on a device share the array: calls that overlap
+ * on the GPU race and must be serialised by the caller.
  */
 int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, const void* x,
                          int32_t* count, int32_t* offs, int32_t* src, int32_t* pos,

@@ -121,6 +121,15 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
   return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
 }
 
+Shape shape_of(const moe_desc& d) {
+  Shape s;
+  s.T = d.T; s.H = d.H; s.E = d.E; s.K = d.K; s.F = d.F;
+  s.C = d.capacity > 0 ? d.capacity : 0;
+  s.dtype = d.dtype; s.flags = d.flags;
+  s.inv_tau = d.temperature > 0.f ? 1.f / d.temperature : 1.f;
+  return s;
+}
+
 namespace {
 
 struct Layout {
@@ -150,15 +159,6 @@ int check_desc(const moe_desc* d) {
   if (!(d->temperature == d->temperature) || d->temperature > 3.0e38f || d->temperature < -3.0e38f)
     return MOE_ERR_INVALID;   // NaN or infinite
   return MOE_OK;
-}
-
-Shape shape_of(const moe_desc& d) {
-  Shape s;
-  s.T = d.T; s.H = d.H; s.E = d.E; s.K = d.K; s.F = d.F;
-  s.C = d.capacity > 0 ? d.capacity : 0;
-  s.dtype = d.dtype; s.flags = d.flags;
-  s.inv_tau = d.temperature > 0.f ? 1.f / d.temperature : 1.f;
-  return s;
 }
 
 Layout layout_of(const moe_desc& d) {

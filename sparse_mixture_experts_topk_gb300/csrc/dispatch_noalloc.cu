@@ -11,15 +11,18 @@
 //
 // The array is a file-scope __device__ variable of kScratchBytes (64 KiB).
 // Every GPU that loads the library holds it until the process exits.  Host
-// code cannot use the array's name as a device address, so the first call on
-// each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it; make that first call before any stream
-// capture.  All calls on a device share the one array, so calls that overlap
-// on the GPU (different streams, or different host threads) race on it and
-// must be serialised by the caller.  The histogram and prefix kernels write
-// every scratch word they later read, so stale contents from an earlier call
-// are never used and nothing needs clearing; the optional error word the
-// caller passes is cleared by each call.
+// code cannot use the array's name as a device address: each call looks the
+// address up with cudaGetSymbolAddress, with the call's device current, and
+// keeps it per device.  A call made while its stream is being captured uses
+// the kept address instead, so the first call on each device must come before
+// any stream capture; a device reset (cudaDeviceReset) or an unload of the
+// library makes the kept address stale until the next call outside capture.
+// All calls on a device share the one array, so calls that overlap on the
+// GPU (different streams, or different host threads) race on it and must be
+// serialised by the caller.  The histogram and prefix kernels write every
+// scratch word they later read, so stale contents from an earlier call are
+// never used and nothing needs clearing; the optional error word the caller
+// passes is cleared by each call.
 #include <mutex>
 
 #include "internal.h"
@@ -37,14 +40,18 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device (looked up once).
-cudaError_t scratch_address(void** out) {
+// Device address of the scratch array on the current device: looked up
+// afresh outside stream capture (cheap), the address kept from the last such
+// lookup while `st` is being captured.
+cudaError_t scratch_address(cudaStream_t st, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  if (!capturing || !g_addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
     if (e != cudaSuccess) return e;
@@ -68,16 +75,12 @@ extern "C" int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, co
   const moe_desc& d = *desc;
   if (!count || !offs || (d.T > 0 && (!ids || !src || !pos))) return MOE_ERR_INVALID;
   if (x && (!x_perm || ((uintptr_t)x & 15u) || ((uintptr_t)x_perm & 15u))) return MOE_ERR_INVALID;
-  Shape s;
-  s.T = d.T; s.H = d.H; s.E = d.E; s.K = d.K; s.F = d.F;
-  s.C = d.capacity > 0 ? d.capacity : 0;
-  s.dtype = d.dtype; s.flags = d.flags;
-  s.inv_tau = 1.f;
+  const Shape s = shape_of(d);
   const size_t table = (size_t)dispatch_blocks(s) * s.E * sizeof(int32_t);
   if (2 * table > kScratchBytes) return MOE_ERR_UNSUPPORTED;   // beyond the fixed scratch
-  void* base = nullptr;
-  if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
+  void* base = nullptr;
+  if (scratch_address(st, &base) != cudaSuccess) return MOE_ERR_CUDA;
   if (device_error && cudaMemsetAsync(device_error, 0, sizeof(int32_t), st) != cudaSuccess)
     return MOE_ERR_CUDA;
   DispatchOut o = {};

@@ -23,6 +23,9 @@ struct Shape {
   size_t esize() const { return dtype == MOE_BF16 ? 2 : 4; }
 };
 
+// The kernels' view of a validated layer description (temperature -> 1/tau).
+Shape shape_of(const moe_desc& d);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -43,7 +43,11 @@ def test_reference_arm_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
     assert d["higher_is_better"] is True and d["unit"] == "tokens/s" and d["value"] > 0
-    assert d["config"]["sample_tokens_per_step"] <= W.WORKLOADS["tiny"].T
+    n = int(d["cpu_baseline"]["sample"].split("first ")[1].split(" of ")[0])
+    assert 0 < n <= W.WORKLOADS["tiny"].T
+    # the same config keys and values the GPU arm prints for this workload
+    w = W.WORKLOADS["tiny"]
+    assert d["config"] == bench.config_of(w, 1, w.T * w.K, w.E, "auto")
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
 
@@ -60,3 +64,16 @@ def test_ncu_traffic_follows_the_kernel_sources():
     gemm = bench.ncu_traffic("prefill", bench.GEMM_SOURCES)
     if gemm is not None:
         assert bench.ncu_traffic("prefill", bench.STREAM_SOURCES) is None
+
+
+def test_tensor_peak_follows_the_clock_record():
+    """Burst peak when no power cap was seen; burst scaled by the sampled SM
+    clock when it was."""
+    p, why = bench.tensor_peak(1900.0, 1700.0, 2000.0, {"reasons": [], "sm_mhz": 2000.0}, "measured")
+    assert p == 1900.0 and "burst" in why
+    p, why = bench.tensor_peak(1900.0, 1700.0, 2000.0, {"reasons": ["sw_power_cap"], "sm_mhz": 1800.0}, "measured")
+    assert p == pytest.approx(1710.0) and "1800" in why
+    p, _ = bench.tensor_peak(1900.0, 1700.0, 2000.0, {"reasons": ["sw_power_cap"], "sm_mhz": None}, "measured")
+    assert p == 1700.0
+    p, _ = bench.tensor_peak(1900.0, 1700.0, 2000.0, None, "measured")
+    assert p == 1900.0

@@ -1,7 +1,8 @@
-"""Data-parallel load-balancing loss with two gloo ranks on the CPU: the
-sharded statistics, all-reduced, give the oracle's full-batch loss; a rank
-that dies before the collective makes the survivor fail with a timeout
-instead of hanging."""
+"""Data-parallel load-balancing loss.  With two gloo ranks on the CPU: the
+sharded statistics, all-reduced, are the full batch's statistics and give the
+oracle's full-batch loss; a rank that dies before the collective makes the
+survivor fail with a timeout instead of hanging.  On the GPU: the loss formed
+from the reduced statistics by the library's kernel matches the oracle."""
 import datetime
 import os
 import socket
@@ -40,16 +41,18 @@ def _worker(rank, world, port, q, die):
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=10))
-    from sparse_mixture_experts_topk_gb300.distributed import global_aux_loss
+    from sparse_mixture_experts_topk_gb300.distributed import reduce_aux_stats
+    from oracle import moe_oracle as O
     T, E, k = 100, 8, 2
     psum, count, n, full = _shard_stats(rank, world, T, E, k)
     if die and rank == 1:
         os._exit(0)                      # leaves between steps, before the collective
     try:
-        L = global_aux_loss(torch.from_numpy(psum), torch.from_numpy(count), n, k)
-        q.put((rank, "ok", float(L), full))
+        ps, cnt, tot = reduce_aux_stats(torch.from_numpy(psum), torch.from_numpy(count), n)
+        L = O.aux_loss_from_psum(ps.numpy(), cnt.numpy(), tot, k)
+        q.put((rank, "ok", float(L), full, tot, cnt.tolist()))
     except Exception as ex:              # the survivor's collective must fail, not hang
-        q.put((rank, "error", type(ex).__name__, full))
+        q.put((rank, "error", type(ex).__name__, full, None, None))
     try:
         dist.destroy_process_group()
     except Exception:
@@ -75,20 +78,45 @@ def _run(world, die):
 def test_sharded_aux_equals_full_batch():
     res = _run(2, die=False)
     assert len(res) == 2
-    for rank, status, L, full in res:
+    _, _, _, full_count = _full_stats(100, 8, 2)
+    for rank, status, L, full, tot, cnt in res:
         assert status == "ok"
+        assert tot == 100 and cnt == full_count.tolist()
         assert L == pytest.approx(full, rel=1e-12)
 
 
-def test_single_process_without_group_is_local_loss():
-    from sparse_mixture_experts_topk_gb300.distributed import global_aux_loss
+def _full_stats(T, E, k):
+    from oracle import moe_oracle as O
+    rng = np.random.default_rng(11)
+    l = rng.standard_normal((T, E)) * 1.5 + np.linspace(1, 0, E)[None, :]
+    ids, _, p = O.route(l, k)
+    return l, p, ids, np.bincount(ids.reshape(-1), minlength=E)
+
+
+def test_single_process_without_group_is_local_stats():
+    from sparse_mixture_experts_topk_gb300.distributed import reduce_aux_stats
     psum, count, n, full = _shard_stats(0, 1, 100, 8, 2)
-    assert float(global_aux_loss(torch.from_numpy(psum), torch.from_numpy(count), n, 2)) == \
-        pytest.approx(full, rel=1e-12)
+    ps, cnt, tot = reduce_aux_stats(torch.from_numpy(psum), torch.from_numpy(count), n)
+    assert tot == n and np.array_equal(cnt.numpy(), count)
+    assert np.array_equal(ps.numpy(), psum)
 
 
 def test_dead_rank_gives_error_not_hang():
     res = _run(2, die=True)
     assert len(res) == 1
-    rank, status, what, _ = res[0]
+    rank, status, what = res[0][:3]
     assert rank == 0 and status == "error"
+
+
+@pytest.mark.gpu
+def test_global_aux_loss_on_device_matches_oracle():
+    """One process, no group: the statistics go to the library's loss kernel."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_mixture_experts_topk_gb300 import build
+    from sparse_mixture_experts_topk_gb300.distributed import global_aux_loss
+    build.build()
+    psum, count, n, full = _shard_stats(0, 1, 100, 8, 2)
+    L = global_aux_loss(torch.from_numpy(psum), torch.from_numpy(count), n, 2)
+    torch.cuda.synchronize()
+    assert L.is_cuda and float(L.item()) == pytest.approx(full, rel=1e-5)

@@ -1,12 +1,14 @@
 """moe_dispatch_noalloc, the dispatch entry point for callers that cannot
 allocate device memory (allocator callbacks, runtimes that reserve all device
 memory up front, hosts that forbid allocation on their execution path), gives
-the same results as moe_dispatch on two calls in a row.
+the same results as moe_dispatch, and as the oracle, on calls in a row.
 
-The two calls use different layers, so stale scratch left by the first call
-would show up in the second.  Integer outputs and the gathered rows must match
-bit for bit, as in every other dispatch test.  This file is collected last so
-that a stop-at-first-failure run has already run everything else."""
+The calls use different layers, so stale scratch left by one call would show
+up in the next: the multi-block path with capacity drops, the one-block path
+(at most 1024 slots), and a multi-block call with no error word.  Integer
+outputs and the gathered rows must match bit for bit, as in every other
+dispatch test.  This file is collected last so that a stop-at-first-failure
+run has already run everything else."""
 import ctypes
 
 import numpy as np
@@ -14,6 +16,7 @@ import pytest
 
 import sparse_mixture_experts_topk_gb300 as moe
 from sparse_mixture_experts_topk_gb300 import workloads as W
+from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +38,9 @@ def _route(torch, w, inp):
     ws = moe.workspace(d)
     ids = torch.empty((w.T, w.K), dtype=torch.int32, device="cuda")
     wts = torch.empty((w.T, w.K), dtype=torch.float32, device="cuda")
-    moe.moe_router_topk(d, dev.x, dev.Wg, dev.gb, None, ids, wts, None, ws)
-    return dev, d, ws, ids
+    logits = torch.empty((w.T, w.E), dtype=torch.float32, device="cuda")
+    moe.moe_router_topk(d, dev.x, dev.Wg, dev.gb, logits, ids, wts, None, ws)
+    return dev, d, ws, ids, logits
 
 
 def _outputs(torch, w, dev):
@@ -49,37 +53,70 @@ def _outputs(torch, w, dev):
                 dropped=torch.full((1,), -9, dtype=torch.int32, device="cuda"))
 
 
-def test_noalloc_dispatch_matches_workspace_dispatch_twice():
+CASES = [
+    # multi-block, capacity drops, error word passed
+    (W.small("na_first", T=3000, H=256, E=64, K=4, F=64, gate_bias="zipf",
+             capacity=W.capacity_ceil(3000, 64, 4)), True),
+    # one-block path (300 slots), error word passed
+    (W.small("na_one_block", T=150, H=128, E=8, K=2, F=64, gate_bias="zipf",
+             capacity=W.capacity_ceil(150, 8, 2) // 2), True),
+    # multi-block, no capacity, no error word
+    (W.small("na_second", T=700, H=128, E=16, K=2, F=64), False),
+]
+
+
+def test_noalloc_dispatch_matches_workspace_dispatch_and_oracle():
     torch = pytest.importorskip("torch")
-    cases = [
-        W.small("na_first", T=3000, H=256, E=64, K=4, F=64, gate_bias="zipf",
-                capacity=W.capacity_ceil(3000, 64, 4)),
-        W.small("na_second", T=700, H=128, E=16, K=2, F=64),
-    ]
-    for w in cases:
+    for w, with_err in CASES:
         inp = W.generate(w)
-        dev, d, ws, ids = _route(torch, w, inp)
+        dev, d, ws, ids, logits = _route(torch, w, inp)
         ref = _outputs(torch, w, dev)
         moe.moe_dispatch(d, ids, dev.x, ref["count"], ref["offs"], ref["src"], ref["pos"],
                          ref["x_perm"], ref["dropped"], ws)
         got = _outputs(torch, w, dev)
-        err = torch.full((1,), -5, dtype=torch.int32, device="cuda")
+        err = torch.full((1,), -5, dtype=torch.int32, device="cuda") if with_err else None
         moe.moe_dispatch_noalloc(d, ids, dev.x, got["count"], got["offs"], got["src"], got["pos"],
                                  got["x_perm"], got["dropped"], err)
         torch.cuda.synchronize()
         R = int(ref["offs"][-1].item())
-        assert int(err.item()) == 0
+        if with_err:
+            assert int(err.item()) == 0
         for k in ("count", "offs", "pos", "dropped"):
             assert torch.equal(got[k], ref[k]), (w.name, k)
         assert torch.equal(got["src"][:R], ref["src"][:R]), w.name
         assert torch.equal(got["x_perm"][:R], ref["x_perm"][:R]), w.name
+        # and against the oracle's dispatch of the same routing
+        ids_o, _, _ = O.route(logits.cpu().numpy().astype(np.float64), w.K, w.temperature)
+        assert np.array_equal(ids.cpu().numpy(), ids_o), w.name
+        o = O.dispatch(ids_o, w.E, w.capacity)
+        for k in ("count", "offs", "pos"):
+            assert np.array_equal(got[k].cpu().numpy(), o[k]), (w.name, k)
+        assert np.array_equal(got["src"][:R].cpu().numpy(), o["src"]), w.name
+        assert int(got["dropped"].item()) == o["dropped"], w.name
+        xp = got["x_perm"][:R].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(xp, inp.x[o["src"] // w.K]), w.name
         if w.capacity > 0:
-            assert int(ref["dropped"].item()) > 0
+            assert o["dropped"] > 0
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch():
-    lib = moe.lib()
-    d = moe.make_desc(T=100000, H=64, E=256, K=2, F=64)     # 64 blocks x 256 experts
-    A = 1 << 20
-    rc = lib.moe_dispatch_noalloc(ctypes.byref(d), A, None, A, A, A, A, None, None, None, None)
+    """A layer whose per-block tables exceed the fixed scratch is refused
+    before anything launches.  Every buffer is real and sized for the call, so
+    a regression in the size check gives a wrong return code, never a fault."""
+    torch = pytest.importorskip("torch")
+    T, E, K = 100000, 256, 2                                  # 64 blocks x 256 experts
+    d = moe.make_desc(T=T, H=64, E=E, K=K, F=64)
+    R = moe.moe_max_rows(d)
+    ids = torch.zeros((T, K), dtype=torch.int32, device="cuda")
+    ids[:, 1] = 1                                             # valid, distinct experts
+    count = torch.empty((E,), dtype=torch.int32, device="cuda")
+    offs = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+    src = torch.empty((R,), dtype=torch.int32, device="cuda")
+    pos = torch.empty((T * K,), dtype=torch.int32, device="cuda")
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    rc = moe.lib().moe_dispatch_noalloc(ctypes.byref(d), ids.data_ptr(), None, count.data_ptr(),
+                                        offs.data_ptr(), src.data_ptr(), pos.data_ptr(), None, None,
+                                        err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
     assert rc == -2                                           # MOE_ERR_UNSUPPORTED
