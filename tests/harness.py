@@ -144,6 +144,26 @@ def out_errors(gpu: np.ndarray, ref: np.ndarray):
     return float(np.abs(diff).max()), rel
 
 
+def product_tol(ref, A, B, slope=1.0):
+    """Tolerance of one bf16 expert product ``bf16(act(A @ B^T))`` computed with
+    fp32 accumulation, against the oracle's fp64 product rounded to bf16:
+    one bf16 ulp (each side rounds once; at most |ref| 2^-7) plus the fp32
+    accumulation error carried through the activation.  The tensor cores add
+    16 products exactly per step and then round into the fp32 accumulator, so
+    over n = A.shape[1] terms the accumulated error is modelled as
+    sqrt(ceil(n / 16)) roundings of at most 2^-23 relative to sum_i |a_i b_i|,
+    which is bounded by |a| |b| (Cauchy-Schwarz), times the activation's
+    largest slope.  A dropped or doubled term moves a result by about one
+    product |a_i b_i|, hundreds of times this bound at the layer sizes."""
+    n = A.shape[1]
+    acc = np.sqrt(np.ceil(n / 16.0)) * 2.0 ** -23 * np.outer(np.linalg.norm(A, axis=1), np.linalg.norm(B, axis=1))
+    return np.abs(ref) * 2.0 ** -7 + slope * acc
+
+
+# largest slope of the activations: GELU'(a) = Phi(a) + a phi(a) <= 1.129
+GELU_SLOPE = 1.13
+
+
 # tolerances (floating point); integer outputs are compared bit-exactly
 LOGITS_REL = 1e-4          # router scores, max|d| / max|ref| per row
 W_ABS = 2e-6               # renormalised weights from the same fp32 scores

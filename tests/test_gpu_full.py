@@ -6,13 +6,23 @@ benchmark times (``moe_layer_forward`` on device buffers), element by element.
 * Each expert product, every row of every expert: the GPU's ``h_perm`` against
   the oracle's first product of the GPU's own ``x_perm`` (itself bit-exact),
   and the GPU's ``y_perm`` against the oracle's second product of the GPU's
-  own ``h_perm``, both within one bf16 ulp (an fp32 and an fp64 accumulation
-  can round to either neighbour).
-* The layer output, every element of every token: against the oracle's whole
-  layer (its own expert products from x, rounded to bf16 at h and y, combined
-  in fp64), within 2e-2 max-abs and 1e-2 relative L2.  The layer call's output
-  also equals the stage-by-stage output bit for bit, so the products checked
-  above are the ones the layer combined.
+  own ``h_perm``, both within one bf16 ulp plus the error of an fp32
+  accumulation over the layer's reduction length (``harness.product_tol``):
+  near zero, where a bf16 ulp is tiny, the fp32 sums of 3584 products differ
+  from fp64 by more than an ulp.
+* The layer output, every element of every token, against the oracle's whole
+  layer (its own routing from the GPU's scores, its own expert products from
+  x, combined in fp64):
+    - computed exactly (fp64 throughout): within 2e-2 max-abs and 1e-2
+      relative L2;
+    - with h and y rounded to bf16 like the GPU's: within 1e-2 relative L2,
+      and per element within 2e-2 plus one bf16 ulp of the output value.  At
+      these sizes the fp32 and fp64 sums round about one y element in twenty
+      to different bf16 neighbours, so two computations that both round h
+      and y can differ by a y ulp (up to 0.0156 below |y| = 4) on top of the
+      output's own rounding.
+  The layer call's output also equals the stage-by-stage output bit for bit,
+  so the products checked above are the ones the layer combined.
 
 The oracle widens one expert's weights at a time so host memory stays bounded
 at the widest layer.
@@ -24,8 +34,8 @@ from sparse_mixture_experts_topk_gb300 import workloads as W
 import sparse_mixture_experts_topk_gb300 as moe
 from oracle import moe_oracle as O
 
-from harness import (Dev, run_stages, run_layer, to_np, as_f64, logits_rel_err, out_errors,
-                     LOGITS_REL, W_ABS, PSUM_REL, OUT_MAXABS_BF16, OUT_REL_L2_BF16)
+from harness import (Dev, run_stages, run_layer, to_np, as_f64, logits_rel_err, out_errors, product_tol,
+                     GELU_SLOPE, LOGITS_REL, W_ABS, PSUM_REL, OUT_MAXABS_BF16, OUT_REL_L2_BF16)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,11 +60,6 @@ class _PerExpert:
 
     def __getitem__(self, e):
         return O.widen(self.a[e], self.dtype)
-
-
-def _ulp_tol(ref):
-    # one bf16 ulp at |ref| is at most |ref| * 2^-7; 1e-6 covers values near 0
-    return np.abs(ref) * 2.0 ** -7 + 1e-6
 
 
 @pytest.mark.parametrize("name", ["decode1", "decode8", "decode16r", "prefill", "zipf_cap", "wide",
@@ -111,20 +116,37 @@ def test_full_size(name):
         a, b = int(d["offs"][e]), int(d["offs"][e + 1])
         if a == b:
             continue
-        pre = O.widen(xp_bits[a:b], w.dtype) @ W1[e].T
-        h_ref = O.round_bf16(O.silu(pre[:, :w.F]) * pre[:, w.F:] if w.act == "swiglu" else O.gelu(pre))
+        xe, W1e, W2e = O.widen(xp_bits[a:b], w.dtype), W1[e], W2[e]
+        pre = xe @ W1e.T
+        if w.act == "swiglu":
+            g, u = pre[:, :w.F], pre[:, w.F:]
+            h_ref = O.round_bf16(O.silu(g) * u)
+            # d(SiLU(g) u) = SiLU'(g) u dg + SiLU(g) du, |SiLU'| <= 1.1
+            tol_g = product_tol(0 * g, xe, W1e[:w.F])
+            tol_u = product_tol(0 * u, xe, W1e[w.F:])
+            tol_h = np.abs(h_ref) * 2.0 ** -7 + 1.1 * np.abs(u) * tol_g + np.abs(O.silu(g)) * tol_u
+        else:
+            h_ref = O.round_bf16(O.gelu(pre))
+            tol_h = product_tol(h_ref, xe, W1e, GELU_SLOPE)
         h_gpu = O.widen(hp_bits[a:b], w.dtype)
-        bad = np.abs(h_gpu - h_ref) > _ulp_tol(h_ref)
+        bad = np.abs(h_gpu - h_ref) > tol_h
         assert not bad.any(), (name, "h", e, int(bad.sum()))
-        y_ref = O.round_bf16(h_gpu @ W2[e].T)
+        y_ref = O.round_bf16(h_gpu @ W2e.T)
         y_gpu = O.widen(yp_bits[a:b], w.dtype)
-        bad = np.abs(y_gpu - y_ref) > _ulp_tol(y_ref)
+        bad = np.abs(y_gpu - y_ref) > product_tol(y_ref, h_gpu, W2e)
         assert not bad.any(), (name, "y", e, int(bad.sum()))
     if R:
         assert int(kept.max()) > 256 or w.T <= 16     # prefill-sized layers span several row blocks
 
     # the layer output, every element, against the oracle's whole layer
-    y_perm = O.expert_outputs(x64, d, W1, W2, bf16=(w.dtype == W.BF16), E=w.E, ids=ids_o, act=w.act)
-    ref = O.combine(y_perm, d["pos"], w_o)
-    mx, rel = out_errors(as_f64(L["out"]), ref)
-    assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (name, mx, rel)
+    out = as_f64(L["out"])
+    exact = O.combine(O.expert_outputs(x64, d, W1, W2, bf16=False, E=w.E, ids=ids_o, act=w.act),
+                      d["pos"], w_o)
+    mx, rel = out_errors(out, exact)
+    assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (name, "exact", mx, rel)
+    rounded = O.combine(O.expert_outputs(x64, d, W1, W2, bf16=True, E=w.E, ids=ids_o, act=w.act),
+                        d["pos"], w_o)
+    mx, rel = out_errors(out, rounded)
+    assert rel <= OUT_REL_L2_BF16, (name, "rounded", rel)
+    over = np.abs(out - rounded) > OUT_MAXABS_BF16 + np.abs(rounded) * 2.0 ** -7
+    assert not over.any(), (name, "rounded", mx, int(over.sum()))
