@@ -12,15 +12,14 @@ benchmark times (``moe_layer_forward`` on device buffers), element by element.
   from fp64 by more than an ulp.
 * The layer output, every element of every token, against the oracle's whole
   layer (its own routing from the GPU's scores, its own expert products from
-  x, combined in fp64):
-    - computed exactly (fp64 throughout): within 2e-2 max-abs and 1e-2
-      relative L2;
-    - with h and y rounded to bf16 like the GPU's: within 1e-2 relative L2,
-      and per element within 2e-2 plus one bf16 ulp of the output value.  At
-      these sizes the fp32 and fp64 sums round about one y element in twenty
-      to different bf16 neighbours, so two computations that both round h
-      and y can differ by a y ulp (up to 0.0156 below |y| = 4) on top of the
-      output's own rounding.
+  x, combined in fp64), both computed exactly (fp64 throughout) and with h
+  and y rounded to bf16 like the GPU's: within 1e-2 relative L2, and each
+  element within 2e-2 plus one bf16 ulp of its value.  The ulp term is the
+  bf16 storage of the output and of y: at |out| >= 2 one ulp (>= 0.0156) is
+  most of 2e-2, and the fp32 and fp64 sums round about one y element in
+  twenty to different bf16 neighbours.  Where every output is below 4 in
+  magnitude (the prefill-sized layers) the plain 2e-2 max-abs also holds
+  against the exact layer.
   The layer call's output also equals the stage-by-stage output bit for bit,
   so the products checked above are the ones the layer combined.
 
@@ -140,13 +139,12 @@ def test_full_size(name):
 
     # the layer output, every element, against the oracle's whole layer
     out = as_f64(L["out"])
-    exact = O.combine(O.expert_outputs(x64, d, W1, W2, bf16=False, E=w.E, ids=ids_o, act=w.act),
-                      d["pos"], w_o)
-    mx, rel = out_errors(out, exact)
-    assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (name, "exact", mx, rel)
-    rounded = O.combine(O.expert_outputs(x64, d, W1, W2, bf16=True, E=w.E, ids=ids_o, act=w.act),
-                        d["pos"], w_o)
-    mx, rel = out_errors(out, rounded)
-    assert rel <= OUT_REL_L2_BF16, (name, "rounded", rel)
-    over = np.abs(out - rounded) > OUT_MAXABS_BF16 + np.abs(rounded) * 2.0 ** -7
-    assert not over.any(), (name, "rounded", mx, int(over.sum()))
+    for kind in ("exact", "rounded"):
+        ref = O.combine(O.expert_outputs(x64, d, W1, W2, bf16=(kind == "rounded"), E=w.E, ids=ids_o,
+                                         act=w.act), d["pos"], w_o)
+        mx, rel = out_errors(out, ref)
+        assert rel <= OUT_REL_L2_BF16, (name, kind, rel)
+        over = np.abs(out - ref) > OUT_MAXABS_BF16 + np.abs(ref) * 2.0 ** -7
+        assert not over.any(), (name, kind, mx, int(over.sum()))
+        if kind == "exact" and np.abs(ref).max() < 4.0:
+            assert mx <= OUT_MAXABS_BF16, (name, kind, mx)
