@@ -178,8 +178,9 @@ Layout layout_of(const moe_desc& d) {
   L.w = take(S * 4);
   L.psum_part = take((size_t)router_partials(s) * E * 4);
   L.psum = take(E * 4);
-  // per-block dispatch tables: the standalone blocking or the router's CTAs
-  const int64_t nblk = dispatch_blocks(s) > router_partials(s) ? dispatch_blocks(s) : router_partials(s);
+  // per-block dispatch tables: the standalone blocking or the router's 128-token tiles
+  const int64_t tiles = (s.T + kRouterTileTokens - 1) / kRouterTileTokens;
+  const int64_t nblk = dispatch_blocks(s) > tiles ? dispatch_blocks(s) : tiles;
   L.blk_hist = take((size_t)nblk * E * 4);
   L.blk_base = take((size_t)nblk * E * 4);
   L.count = take(E * 4);

@@ -29,20 +29,6 @@ namespace {
 constexpr int kDispThreads = 256;
 constexpr int kDispWarps = kDispThreads / 32;
 
-// Slots [s0, s1) of block b: with parts > 0 the blocks are the router's CTAs,
-// block b holding the slots of tokens [b T / parts, (b + 1) T / parts);
-// otherwise blocks of bslots consecutive slots.
-__device__ __forceinline__ void block_slots(int64_t b, int64_t S, int64_t Tn, int K, int bslots, int64_t parts,
-                                            int64_t& s0, int64_t& s1) {
-  if (parts > 0) {
-    s0 = (int64_t)K * (b * Tn / parts);
-    s1 = (int64_t)K * ((b + 1) * Tn / parts);
-  } else {
-    s0 = b * bslots;
-    s1 = min(S, s0 + bslots);
-  }
-}
-
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslots,
                      int32_t* __restrict__ blk_hist, int* err) {
@@ -295,13 +281,13 @@ __device__ __forceinline__ void scatter_slots(const int32_t* __restrict__ ids, i
 }
 
 __global__ void __launch_bounds__(kDispThreads)
-dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots, int64_t parts,
-                        int64_t Tn, int K, const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offs,
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
+                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offs,
                         int32_t* __restrict__ pos, int32_t* __restrict__ src) {
   __shared__ int running[256];
   pdl_enter();
-  int64_t s0, s1;
-  block_slots(blockIdx.x, S, Tn, K, bslots, parts, s0, s1);
+  const int64_t s0 = (int64_t)blockIdx.x * bslots;
+  const int64_t s1 = min(S, s0 + bslots);
   for (int e = threadIdx.x; e < E; e += kDispThreads) running[e] = blk_base[(int64_t)blockIdx.x * E + e];
   scatter_slots(ids, s0, s1, E, C, running, offs, pos, src);
 }
@@ -348,14 +334,14 @@ dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ 
   }
 }
 
-// Scan and scatter in one kernel, when the router has counted the chosen
-// experts of each of its CTAs' tokens: every block reads the whole [nblk, E]
-// table of those counts (eight loads in flight per thread), takes its rank
-// base (the counts of the blocks before it) and the experts' totals and
-// offsets, and places its block's slots.  Block 0 also writes the counts, offsets, dropped slots,
+// Scan and scatter in one kernel, when the router has counted its 128-token
+// tiles: every block reads the whole [nblk, E] table of tile counts (eight
+// loads in flight per thread), takes its rank base (the counts of the tiles
+// before it) and the experts' totals and offsets, and places its tile's
+// slots.  Block 0 also writes the counts, offsets, dropped slots,
 // probability sums (added up exactly as the scan kernel does) and the loss.
 __global__ void __launch_bounds__(kDispThreads)
-dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C,
+dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
                              const int32_t* __restrict__ blk_hist, int64_t nblk, int32_t* __restrict__ count,
                              int32_t* __restrict__ offs, int32_t* __restrict__ dropped,
                              const float* __restrict__ psum_part, int64_t prows, float* __restrict__ psum,
@@ -411,8 +397,8 @@ dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, 
                 leader ? count_copy : nullptr, leader ? dropped_copy : nullptr, leader ? sched : nullptr, s_offs,
                 p_pre);
   __syncthreads();
-  int64_t s0, s1;
-  block_slots(blockIdx.x, S, Tn, K, 0, nblk, s0, s1);
+  const int64_t s0 = (int64_t)blockIdx.x * bslots;
+  const int64_t s1 = min(S, s0 + bslots);
   for (int64_t c0 = s0; c0 < s1; c0 += kDispThreads) {
     const int64_t sl = c0 + threadIdx.x;
     int ex = -1;
@@ -527,7 +513,7 @@ cudaError_t launch_gather(const Shape& s, const void* x, const int32_t* pos, voi
 
 int dispatch_launches(const Shape& s, bool hist_ready) {
   if (dispatch_small(s)) return 1;
-  const int64_t nblk = hist_ready ? router_tc_partials(s) : dispatch_blocks(s);
+  const int64_t nblk = hist_ready ? (s.T + kRouterTileTokens - 1) / kRouterTileTokens : dispatch_blocks(s);
   if (hist_ready && (size_t)nblk * s.E * sizeof(int) <= kFusedScanTable) return 2;   // scan+scatter, gather
   return (hist_ready ? 0 : 1) + 3;                                                   // (hist,) scan, scatter, gather
 }
@@ -552,21 +538,21 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  // blocks of slots: the router's CTAs' tokens when it already counted
+  // blocks of slots: the router's 128-token tiles when it already counted
   // them, else blocks sized for a short scan
-  const int bslots = dispatch_block_slots(s);
-  const int64_t parts = o.hist_ready ? router_tc_partials(s) : 0;
-  const int64_t nblk = o.hist_ready ? parts : dispatch_blocks(s);
+  const int bslots = o.hist_ready ? kRouterTileTokens * s.K : dispatch_block_slots(s);
+  const int64_t nblk = o.hist_ready ? (s.T + kRouterTileTokens - 1) / kRouterTileTokens
+                                    : dispatch_blocks(s);
   cudaError_t e = cudaSuccess;
   const size_t table = (size_t)nblk * s.E * sizeof(int);
   if (o.hist_ready && nblk > 0 && table <= kFusedScanTable) {
-    if (table > 48 * 1024)
-      e = cudaFuncSetAttribute(dispatch_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)table);
+    // the opt-in covers dynamic plus static shared memory above 48 KB
+    e = cudaFuncSetAttribute(dispatch_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)table);
     const int64_t prows = o.psum_part ? router_partial_rows(s) : (int64_t)0;
     if (e == cudaSuccess)
       e = launch_kernel(dispatch_scan_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), table, st, 1, ids,
-                        S, s.E, s.C, (const int32_t*)o.blk_hist, nblk, o.count, o.offs, o.dropped,
+                        S, s.E, s.C, bslots, (const int32_t*)o.blk_hist, nblk, o.count, o.offs, o.dropped,
                         o.psum_part, prows, o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy, o.sched,
                         o.pos, o.src);
     if (e == cudaSuccess && x && x_perm && S > 0) e = launch_gather(s, x, o.pos, x_perm, st);
@@ -582,7 +568,7 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
   const int staged = sm <= 96 * 1024 ? 1 : 0;
   const int staged_p = (o.psum_part && (staged ? sm : 0) + smp <= 192 * 1024) ? 1 : 0;
   const size_t smem = (staged ? sm : 0) + (staged_p ? smp : 0);
-  if (e == cudaSuccess && smem > 48 * 1024)
+  if (e == cudaSuccess && smem > 0)
     e = cudaFuncSetAttribute(dispatch_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = launch_kernel(dispatch_scan_kernel, dim3(1), dim3(256), smem, st, 1, (const int32_t*)o.blk_hist, nblk,
@@ -590,8 +576,7 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
                       o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy, o.sched);
   if (e == cudaSuccess && nblk > 0)
     e = launch_kernel(dispatch_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), 0, st, 1, ids, S, s.E,
-                      s.C, bslots, parts, s.T, s.K, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos,
-                      o.src);
+                      s.C, bslots, (const int32_t*)o.blk_base, (const int32_t*)o.offs, o.pos, o.src);
   if (e == cudaSuccess && x && x_perm && S > 0) e = launch_gather(s, x, o.pos, x_perm, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -67,23 +67,19 @@ void prof_mark(int mark, cudaStream_t st);
 bool tma_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 // ---------------------------------------------------------------- router
-// Upper bound of the rows of per-block probability partial sums (and of the
-// per-block expert counts) the routers write, for any device (workspace
-// sizing), and the rows the chosen router writes on the current device.
+// Upper bound of the rows of per-block probability partial sums the router
+// writes (workspace sizing), and the rows the chosen router writes.
 int64_t router_partials(const Shape& s);
 bool router_small(const Shape& s);   // one-cluster router for decode-sized bf16 batches
 int64_t router_partial_rows(const Shape& s);
 bool router_on_tensor_cores(const Shape& s);
-// The tensor-core router runs G = router_tc_partials(s) CTAs; CTA b owns the
-// tokens [b T / G, (b + 1) T / G) and writes row b of the partial sums and
-// of tile_hist.  router_tc_partials_bound: G's upper bound on any device.
-int64_t router_tc_partials(const Shape& s);
-int64_t router_tc_partials_bound(const Shape& s);
-// tile_hist (nullable): [G, E] count of each CTA's chosen experts, i.e. of
-// the slots K b T / G .. K (b + 1) T / G.
+int router_tc_split(const Shape& s);   // CTAs the tensor-core router splits the hidden dimension over (1 or 2)
+// tile_hist (nullable): [ceil(T/128), E] count of each 128-token tile's
+// chosen experts, in slot order blocks of 128*K slots.
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                              float* logits, int32_t* ids, float* w, float* psum_part,
                              int32_t* tile_hist, int* err, cudaStream_t st);
+constexpr int kRouterTileTokens = 128;
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
                           float* logits, int32_t* ids, float* w, float* psum_part, int* err,
                           cudaStream_t st, int32_t* tile_hist = nullptr);

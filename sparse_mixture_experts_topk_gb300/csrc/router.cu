@@ -185,7 +185,7 @@ router_simt_kernel(const T* __restrict__ x, const T* __restrict__ Wg,
 // piece table over distributed shared memory; after one cluster barrier the
 // leader adds each score's pieces in piece order, adds the bias, finishes
 // each token (top-k, weights), counts the chosen experts as it picks them
-// into tile_hist[0] (the layer's single block of tokens) and sums the
+// into tile_hist[0] (the layer's single 128-token tile) and sums the
 // probabilities per expert in token order into psum_part[0].
 constexpr int kSmallTok = 16;
 constexpr int kSmallChunk = 8;
@@ -322,11 +322,7 @@ __global__ void psum_reduce_kernel(const float* __restrict__ part, int64_t rows,
 
 }  // namespace
 
-int64_t router_partials(const Shape& s) {
-  const int64_t simt = (s.T + kRouterTok - 1) / kRouterTok;
-  const int64_t tc = router_tc_partials_bound(s);
-  return simt > tc ? simt : tc;
-}
+int64_t router_partials(const Shape& s) { return (s.T + kRouterTok - 1) / kRouterTok; }
 
 bool router_small(const Shape& s) {
   // the token rows and the score table fit one CTA's shared memory
@@ -336,7 +332,7 @@ bool router_small(const Shape& s) {
 
 int64_t router_partial_rows(const Shape& s) {
   if (router_small(s)) return 1;
-  return router_on_tensor_cores(s) ? router_tc_partials(s) : (s.T + kRouterTok - 1) / kRouterTok;
+  return router_on_tensor_cores(s) ? (s.T + 127) / 128 * router_tc_split(s) : router_partials(s);
 }
 
 cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const float* gate_bias,
@@ -358,7 +354,7 @@ cudaError_t launch_router(const Shape& s, const void* x, const void* Wg, const f
     return launch_router_tc(s, x, Wg, gate_bias, logits, ids, w, psum_part, tile_hist, err, st);
   const size_t smem = sizeof(float) * (kRouterTok * (kRouterKC + 1) + s.E * (kRouterKC + 1) +
                                        kRouterTok * (s.E + 1));
-  const int64_t grid = (s.T + kRouterTok - 1) / kRouterTok;
+  const int64_t grid = router_partials(s);
   if (s.dtype == MOE_BF16) {
     auto k = router_simt_kernel<bf16>;
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
