@@ -27,6 +27,9 @@ Readings taken where the pages are silent or garbled:
     dropped slots add nothing and the surviving weights are not renormalised;
   * the load-balancing frequency is count_i / (T*k) with counts taken before
     any drop, so the loss is exactly 1 under uniform routing;
+  * with drop_tokens=False the slots the capacity would drop move, one at a
+    time in slot order, to their token's best-scored unused expert with room
+    (``reroute``);
   * GELU is the erf form; on the bf16 path the GELU output h and the expert
     output y are rounded to bf16 (round-to-nearest-even), everything else is
     carried in float64; the fp32 path rounds nowhere.
@@ -152,6 +155,68 @@ def dispatch(ids: np.ndarray, E: int, capacity: int = 0):
                 dropped=int((count - kept).sum()))
 
 
+def reroute(ids: np.ndarray, l: np.ndarray, E: int, capacity: int):
+    """``drop_tokens=False`` ([W] 3.4: with it, slots over an expert's
+    capacity go to the next-best expert instead of being dropped).
+
+    Reading taken where the page stops: the slots the capacity keeps are those
+    ``dispatch`` keeps (each expert's first ``capacity`` slots in (token, rank)
+    order); only the slots it would drop move.  They are taken one at a time in
+    slot order; each goes to its token's best-scored expert (score descending,
+    index ascending) that the token does not already use -- neither among its
+    k choices nor as the target of an earlier move -- and that still has room
+    (``capacity`` minus the slots it already holds); with no such expert the
+    slot is dropped.  A moved slot keeps its routing weight.
+
+    Returns ``(final [T, k], dropped)``: each slot's expert after the moves,
+    -1 for a dropped slot."""
+    T, k = ids.shape
+    d = dispatch(ids, E, capacity)
+    room = (capacity - d["kept"]).astype(np.int64)
+    final = np.asarray(ids, dtype=np.int64).copy()
+    dropped = 0
+    for t in range(T):
+        used = set(int(e) for e in ids[t])
+        for j in range(k):
+            if d["pos"][t * k + j] >= 0:
+                continue
+            best = -1
+            for e in range(E):
+                if e in used or room[e] <= 0:
+                    continue
+                if best < 0 or l[t, e] > l[t, best]:      # equal scores keep the lower index
+                    best = e
+            final[t, j] = best
+            if best < 0:
+                dropped += 1
+            else:
+                room[best] -= 1
+                used.add(best)
+    return final, dropped
+
+
+def dispatch_rerouted(ids: np.ndarray, l: np.ndarray, E: int, capacity: int):
+    """Dispatch with ``drop_tokens=False``: ``reroute`` then group the slots by
+    their final expert, stable in slot order (no expert exceeds its capacity
+    any more).  ``count`` stays the count of the routing's own choices (before
+    any move or drop: the load-balancing frequency); ``dropped`` counts the
+    slots left without an expert."""
+    T, k = ids.shape
+    final, dropped = reroute(ids, l, E, capacity)
+    flat = final.reshape(-1)
+    load = np.bincount(flat[flat >= 0], minlength=E).astype(np.int64)
+    offs = np.zeros(E + 1, dtype=np.int64)
+    offs[1:] = np.cumsum(load)
+    pos = np.full(T * k, -1, dtype=np.int64)
+    src = np.empty(int(offs[E]), dtype=np.int64)
+    for e in range(E):
+        slots = np.nonzero(flat == e)[0]              # ascending slot order
+        pos[slots] = offs[e] + np.arange(slots.size)
+        src[offs[e]:offs[e + 1]] = slots
+    count = np.bincount(np.asarray(ids).reshape(-1), minlength=E).astype(np.int64)
+    return dict(count=count, kept=load, offs=offs, src=src, pos=pos, dropped=dropped, final=final)
+
+
 # ---------------------------------------------------------------------------
 # experts  ([M] 2.2: each expert is Linear - GELU - Linear; [A] 2.2)
 
@@ -257,17 +322,22 @@ def expert_outputs(x, d, W1, W2, b1=None, b2=None, bf16=False, E=None, ids=None,
 
 
 def layer_forward(x, Wg, W1, W2, k, capacity=0, gate_bias=None, b1=None, b2=None,
-                  bf16=False, logits=None, temperature=1.0, act="gelu"):
+                  bf16=False, logits=None, temperature=1.0, act="gelu", reroute_over=False):
     """The full forward pass of [M] 3.2 with the weighted combine of [W] 3.1.
 
     All arrays are float64 values.  If ``logits`` is given (e.g. the GPU's fp32
     router output widened to float64), routing starts from them instead of
-    from ``x Wg^T``.  Returns a dict with every intermediate."""
+    from ``x Wg^T``.  ``reroute_over``: slots over capacity move to the next
+    best expert with room (``dispatch_rerouted``) instead of being dropped.
+    Returns a dict with every intermediate."""
     T = x.shape[0]
     E = Wg.shape[0]
     l = gate_logits(x, Wg, gate_bias) if logits is None else np.asarray(logits, np.float64)
     ids, w, p = route(l, k, temperature)
-    d = dispatch(ids, E, capacity)
+    if reroute_over and capacity > 0:
+        d = dispatch_rerouted(ids, l, E, capacity)
+    else:
+        d = dispatch(ids, E, capacity)
     y_perm = expert_outputs(x, d, W1, W2, b1, b2, bf16, E, ids, act)
     out = combine(y_perm, d["pos"], w)
     return dict(logits=l, ids=ids, w=w, p=p, y_perm=y_perm, out=out,

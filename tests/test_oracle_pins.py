@@ -242,6 +242,158 @@ def test_dispatch_page_capacity_collapse():
     assert d["pos"][: C * E // k * k].min() >= 0 and d["pos"][C * E:].max() == -1
 
 
+# ---------------------------------------------------------------- reroute (drop_tokens=False)
+
+def _check_greedy(ids, l, E, C, final, dropped):
+    """An independent description of the rerouting the walkthrough's 3.4
+    describes (with the reading of the oracle's docstring), checked on a
+    result instead of constructed: kept slots stay; a moved slot's expert was,
+    at that slot's turn, the best-scored expert with room that its token did
+    not use, and every better one was full; a dropped slot had no such expert
+    at all.  "At a slot's turn" an expert holds the slots the capacity kept
+    plus the moves of earlier slots.  These conditions determine the result
+    uniquely, so they pin it."""
+    T, k = ids.shape
+    d = O.dispatch(ids, E, C)
+    kept = d["kept"]
+    assert dropped == int((final < 0).sum())
+    load = np.bincount(final[final >= 0], minlength=E)
+    assert (load <= C).all()
+    for t in range(T):
+        got = [int(e) for e in final[t] if e >= 0]
+        assert len(got) == len(set(got))                   # a token never uses an expert twice
+        for j in range(k):
+            s = t * k + j
+            if d["pos"][s] >= 0:
+                assert final[t, j] == ids[t, j]           # kept slots stay
+                continue
+            e_new = int(final[t, j])
+            assert e_new not in ids[t].tolist()
+            moved_before = [(s2, int(final.reshape(-1)[s2])) for s2 in range(s)
+                            if d["pos"][s2] < 0 and final.reshape(-1)[s2] >= 0]
+            held = kept.copy()
+            for _, e2 in moved_before:
+                held[e2] += 1
+            used = set(ids[t].tolist()) | {e2 for s2, e2 in moved_before if s2 // k == t}
+            free = [e for e in range(E) if e not in used and held[e] < C]
+            if e_new < 0:
+                assert free == []
+            else:
+                assert e_new in free
+                # no free expert ranks above it (score, then lower index)
+                for e in free:
+                    assert (l[t, e], -e) <= (l[t, e_new], -e_new)
+
+
+def test_reroute_hand_example():
+    """Four tokens that all prefer expert 0, capacity 1: token 1 moves to its
+    second-best expert 2, token 2 to its second-best expert 1, token 3 finds
+    both full and is dropped."""
+    l = np.array([[3., 2., 1.], [3., 1., 2.], [3., 2., 1.], [3., 2., 1.]])
+    ids, _, _ = O.route(l, 1)
+    assert ids.reshape(-1).tolist() == [0, 0, 0, 0]
+    final, dropped = O.reroute(ids, l, 3, 1)
+    assert final.reshape(-1).tolist() == [0, 2, 1, -1] and dropped == 1
+    d = O.dispatch_rerouted(ids, l, 3, 1)
+    assert d["offs"].tolist() == [0, 1, 2, 3]
+    assert d["src"].tolist() == [0, 2, 1] and d["pos"].tolist() == [0, 2, 1, -1]
+    assert d["count"].tolist() == [4, 0, 0] and d["dropped"] == 1
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_reroute_tiny_random_satisfies_the_greedy_conditions(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(2, 6))
+    k = int(rng.integers(1, E + 1))
+    T = int(rng.integers(1, 7))
+    C = int(rng.integers(1, 4))
+    # few distinct score values, so ties between experts are common
+    l = rng.integers(-2, 3, size=(T, E)).astype(np.float64)
+    if seed % 2:
+        l[:, 0] += 2.0                                     # crowd the first expert
+    ids, _, _ = O.route(l, k)
+    final, dropped = O.reroute(ids, l, E, C)
+    _check_greedy(ids, l, E, C, final, dropped)
+
+
+def test_reroute_larger_random_satisfies_the_greedy_conditions():
+    rng = np.random.default_rng(5)
+    T, E, k = 60, 8, 3
+    l = rng.standard_normal((T, E)) + np.log(np.arange(1, E + 1) ** -1.5)[None, :]
+    C = O.capacity_ceil(T, E, k) // 2
+    ids, _, _ = O.route(l, k)
+    final, dropped = O.reroute(ids, l, E, C)
+    assert dropped < O.dispatch(ids, E, C)["dropped"]        # rerouting saves slots here
+    _check_greedy(ids, l, E, C, final, dropped)
+
+
+def test_reroute_special_cases():
+    rng = np.random.default_rng(3)
+    l = rng.standard_normal((20, 6))
+    ids, _, _ = O.route(l, 2)
+    # ample capacity: nothing moves
+    final, dropped = O.reroute(ids, l, 6, 40)
+    assert (final == ids).all() and dropped == 0
+    # k = E: no other expert exists, so reroute drops exactly what dispatch drops
+    ids6, _, _ = O.route(l, 6)
+    final, dropped = O.reroute(ids6, l, 6, 10)
+    d = O.dispatch(ids6, 6, 10)
+    assert dropped == d["dropped"]
+    assert ((final.reshape(-1) >= 0) == (d["pos"] >= 0)).all()
+    # total capacity E * C >= T * k: every slot finds an expert
+    final, dropped = O.reroute(ids, l, 6, 7)
+    assert dropped == 0 and (np.bincount(final.reshape(-1), minlength=6) <= 7).all()
+
+
+def test_dispatch_rerouted_groups_final_experts_stably():
+    rng = np.random.default_rng(9)
+    T, E, k = 40, 5, 2
+    l = rng.standard_normal((T, E))
+    l[:, 1] += 1.5
+    ids, _, _ = O.route(l, k)
+    C = 10
+    d = O.dispatch_rerouted(ids, l, E, C)
+    final = d["final"].reshape(-1)
+    R = int(d["offs"][-1])
+    assert R == T * k - d["dropped"]
+    assert sorted(d["src"].tolist()) == sorted(np.nonzero(final >= 0)[0].tolist())
+    for e in range(E):
+        seg = d["src"][d["offs"][e]:d["offs"][e + 1]]
+        assert (final[seg] == e).all() and (np.diff(seg) > 0).all()
+        assert len(seg) <= C
+    for s in range(T * k):
+        assert (d["pos"][s] >= 0) == (final[s] >= 0)
+        if d["pos"][s] >= 0:
+            assert d["src"][d["pos"][s]] == s
+    assert d["count"].tolist() == np.bincount(ids.reshape(-1), minlength=E).tolist()
+
+
+def test_layer_forward_reroute_uses_the_new_experts():
+    """Each token's output is the weighted sum of its slots' final experts,
+    computed here token by token with the routing weights unchanged."""
+    rng = np.random.default_rng(11)
+    T, H, E, k, F = 24, 8, 4, 2, 6
+    x = rng.standard_normal((T, H))
+    Wg = rng.standard_normal((E, H))
+    Wg[0] *= 0.0
+    Wg[0] += 0.5 * x.mean(0) / (np.linalg.norm(x.mean(0)) ** 2)   # tokens lean towards expert 0
+    W1 = rng.standard_normal((E, F, H)) * 0.3
+    W2 = rng.standard_normal((E, H, F)) * 0.3
+    C = 13                                               # 52 places for 48 slots, expert 0 over
+    r = O.layer_forward(x, Wg, W1, W2, k, capacity=C, reroute_over=True)
+    plain = O.layer_forward(x, Wg, W1, W2, k, capacity=C)
+    final, dropped = O.reroute(r["ids"], r["logits"], E, C)
+    assert r["dropped"] == dropped < plain["dropped"]
+    for t in range(T):
+        want = np.zeros(H)
+        for j in range(k):
+            e = int(final[t, j])
+            if e >= 0:
+                want += r["w"][t, j] * O.expert_ffn(x[t:t + 1], W1[e], W2[e])[0]
+        np.testing.assert_allclose(r["out"][t], want, rtol=1e-12, atol=1e-12)
+    assert r["aux"] == plain["aux"]                      # the routing's own counts
+
+
 # ---------------------------------------------------------------- experts
 
 def test_gelu_normal_cdf_values():
