@@ -201,7 +201,7 @@ def oracle_rate(inp: W.LayerInputs, wide, n_tokens: int, reps: int = 1):
     t0 = time.perf_counter()
     for _ in range(reps):
         O.layer_forward(x[:n_tokens], Wg, W1, W2, w.K, capacity=cap, gate_bias=inp.gate_bias,
-                        bf16=(w.dtype == W.BF16))
+                        bf16=(w.dtype == W.BF16), reroute_over=w.reroute, act=w.act, temperature=w.temperature)
     return time.perf_counter() - t0
 
 
@@ -287,7 +287,8 @@ def run_ours(args, w: W.Workload):
     x, Wg, W1, W2 = (to_dev(a, torch) for a in (inp.x, inp.Wg, inp.W1, inp.W2))
     gb = to_dev(inp.gate_bias, torch)
     dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
-    flags = (moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0) | GEMM_FLAGS[args.gemm]
+    flags = (moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0) | (moe.MOE_FLAG_REROUTE if w.reroute else 0) | \
+        GEMM_FLAGS[args.gemm]
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                       moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
     launches_per_step = moe.moe_layer_launches(d)

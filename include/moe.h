@@ -83,6 +83,15 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * activation rows load once every CTA of the expert has stored its share.
  * Same results; for comparing the two (testing). */
 #define MOE_FLAG_FFN_SPLIT   (1u << 9)
+/* drop_tokens = False (the Qwen2-MoE walkthrough, jsqmd.com, section 3.4:
+ * tokens over an expert's capacity go to the next-best expert instead of
+ * being dropped).  With a capacity, moe_layer_forward keeps the slots the
+ * capacity keeps and moves each other slot, in slot order, to the
+ * best-scored expert its token does not use yet that still has room (see
+ * moe_reroute); a moved slot keeps its routing weight.  `count` and the loss
+ * stay those of the routing's own choices; `dropped` counts the slots left
+ * without an expert.  No effect without a capacity. */
+#define MOE_FLAG_REROUTE     (1u << 10)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the
@@ -152,7 +161,8 @@ int moe_router_topk(const moe_desc* desc, const void* x, const void* Wg,
  * 3.4 (tokens over an expert's capacity are dropped).  Slot s = t*K + j.
  * Within an expert, slots keep ascending s order, so with a capacity the
  * earliest tokens are kept.
- *   ids     [T, K] int32 in (each value in [0, E); a token's K ids distinct)
+ *   ids     [T, K] int32 in (each value in [0, E), or -1 for a slot with no
+ *           expert, which is dropped; a token's other ids distinct)
  *   x       [T, H] dtype in, or NULL to skip the gather
  *   count   [E]    int32 out: slots routed to each expert, before dropping
  *   offs    [E+1]  int32 out: first permuted row of each expert; offs[E] = rows
@@ -193,6 +203,31 @@ int moe_dispatch_noalloc(const moe_desc* desc, const int32_t* ids, const void* x
                          int32_t* count, int32_t* offs, int32_t* src, int32_t* pos,
                          void* x_perm, int32_t* dropped, int32_t* device_error,
                          void* stream);
+
+/*
+ * Move the slots a capacity-limited dispatch dropped (drop_tokens = False;
+ * the Qwen2-MoE walkthrough, jsqmd.com, section 3.4: tokens over capacity are
+ * routed to the next-best expert instead of being dropped).  The slots the
+ * capacity kept stay.  The others are taken one at a time in slot order
+ * s = t*K + j; each goes to the expert with the highest score logits[t, e]
+ * (equal scores: the lower index) that token t uses neither among its K
+ * choices nor as the target of an earlier move, and that still has room
+ * (capacity minus the slots it holds so far); if none has, the slot is
+ * dropped.  The result equals that one-at-a-time walk exactly.
+ *   logits  [T, E] fp32 in: the router's scores (moe_router_topk's logits)
+ *   ids     [T, K] int32 in: the routing
+ *   pos     [T*K]  int32 in: moe_dispatch's pos for ids with desc->capacity
+ *                  (pos < 0: over capacity)
+ *   offs    [E+1]  int32 in: moe_dispatch's offs for the same call
+ *   ids_out [T, K] int32 out: each slot's expert after the moves, -1 if dropped
+ *   dropped [1]    int32 out, or NULL: slots left without an expert
+ * Dispatching ids_out again (moe_dispatch accepts -1 as "no expert") groups
+ * the moved routing; no expert exceeds the capacity any more.  One block does
+ * the walk: meant for capacities that drop a minority of the slots.
+ */
+int moe_reroute(const moe_desc* desc, const float* logits, const int32_t* ids, const int32_t* pos,
+                const int32_t* offs, int32_t* ids_out, int32_t* dropped, void* ws, size_t ws_bytes,
+                void* stream);
 
 /*
  * Expert FFN over the permuted rows: for each expert e and each row r in

@@ -18,7 +18,8 @@ import os
 __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU",
-    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "lib", "library_path", "make_desc",
+    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "MOE_FLAG_REROUTE", "lib",
+    "library_path", "make_desc", "moe_reroute",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "moe_ffn_kernel",
@@ -37,6 +38,7 @@ MOE_FLAG_SWIGLU = 1 << 6
 MOE_FLAG_TEST_WAIT_TIMEOUT = 1 << 7
 MOE_FLAG_GEMM_ROWS = 1 << 8
 MOE_FLAG_FFN_SPLIT = 1 << 9
+MOE_FLAG_REROUTE = 1 << 10
 # moe_ffn_kernel results
 MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED, MOE_FFN_STREAM_SPLIT = 0, 1, 2, 3, 4, 5
 
@@ -67,6 +69,7 @@ _SIGS = {
     "moe_router_topk": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 8 + [ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 10),
+    "moe_reroute": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 7 + [ctypes.c_size_t, _P]),
     "moe_expert_ffn": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 5),
     "moe_aux_loss": (ctypes.c_int, [ctypes.POINTER(MoeDesc)] + [_P] * 4),
@@ -169,6 +172,12 @@ def moe_dispatch_noalloc(desc, ids, x, count, offs, src, pos, x_perm, dropped, d
     _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(
         ctypes.byref(desc), _ptr(ids), _ptr(x), _ptr(count), _ptr(offs), _ptr(src), _ptr(pos),
         _ptr(x_perm), _ptr(dropped), _ptr(device_error), _stream(stream)))
+
+
+def moe_reroute(desc, logits, ids, pos, offs, ids_out, dropped, ws, stream=None):
+    _check("moe_reroute", lib().moe_reroute(
+        ctypes.byref(desc), _ptr(logits), _ptr(ids), _ptr(pos), _ptr(offs), _ptr(ids_out), _ptr(dropped),
+        _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def moe_expert_ffn(desc, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, ws, stream=None):

@@ -134,6 +134,7 @@ namespace {
 
 struct Layout {
   size_t err, sched, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
+  size_t pend, choice, scores, fin;
   size_t x_perm, h_perm, x_stage, out_stage, total;
   int64_t rows;
 };
@@ -189,6 +190,13 @@ Layout layout_of(const moe_desc& d) {
   L.aux = take(4);
   L.src = take((size_t)L.rows * 4);
   L.pos = take(S * 4);
+  L.pend = take(S * 4);          // moving over-capacity slots (drop_tokens=False)
+  L.choice = take(S * 4);
+  L.scores = L.fin = 0;
+  if (d.flags & MOE_FLAG_REROUTE) {
+    L.scores = take((size_t)s.T * E * 4);
+    L.fin = take(S * 4);
+  }
   L.x_perm = take((size_t)L.rows * s.H * es);   // also holds y_perm in the layer call
   L.h_perm = take((size_t)L.rows * s.F * es);
   L.x_stage = L.out_stage = 0;
@@ -286,6 +294,18 @@ int moe_dispatch(const moe_desc* desc, const int32_t* ids, const void* x, int32_
   return cuda_status(launch_dispatch(s, ids, x, x_perm, o, at<int>(ws, L.err), (cudaStream_t)stream));
 }
 
+int moe_reroute(const moe_desc* desc, const float* logits, const int32_t* ids, const int32_t* pos,
+                const int32_t* offs, int32_t* ids_out, int32_t* dropped, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const moe_desc& d = *desc;
+  if ((rc = check_ws(d, ws, ws_bytes))) return rc;
+  if (d.T > 0 && (!logits || !ids || !pos || !offs || !ids_out)) return MOE_ERR_INVALID;
+  const Layout L = layout_of(d);
+  return cuda_status(launch_reroute(shape_of(d), logits, ids, pos, offs, ids_out, at<int32_t>(ws, L.pend),
+                                    at<int32_t>(ws, L.choice), dropped, nullptr, (cudaStream_t)stream));
+}
+
 int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs, const void* W1,
                    const float* b1, const void* W2, const float* b2, void* h_perm, void* y_perm,
                    void* ws, size_t ws_bytes, void* stream) {
@@ -329,6 +349,15 @@ namespace moe {
 // In the layer call the router counts its 128-token tiles' chosen experts
 // (the dispatch histogram) when the multi-block dispatch will read them.
 bool layer_fused_hist(const Shape& s) { return router_on_tensor_cores(s) && !dispatch_small(s); }
+// drop_tokens=False in the layer call: a capacity-limited dispatch without
+// the gather, the move of the over-capacity slots, then a dispatch of the
+// moved routing (no capacity cut: no expert is over any more).
+bool layer_reroutes(const Shape& s) { return (s.flags & MOE_FLAG_REROUTE) && s.C > 0 && s.T > 0; }
+Shape final_shape(const Shape& s) {
+  Shape f = s;
+  f.C = 0;
+  return f;
+}
 }  // namespace moe
 
 int moe_layer_launches(const moe_desc* desc) {
@@ -338,6 +367,10 @@ int moe_layer_launches(const moe_desc* desc) {
   int n = 0;
   if (s.T > 0) n += 1;                                  // router
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
+  if (layer_reroutes(s)) {
+    if (!dispatch_small(s)) n -= 1;                     // the first dispatch gathers nothing
+    n += 1 + dispatch_launches(final_shape(s), false);  // the move, then the dispatch of the moved routing
+  }
   if (s.T > 0) {                                        // expert FFN, combine
     const int k = ffn_kernel(s, rows_for(*desc));
     n += (k == MOE_FFN_TC_FUSED || k == MOE_FFN_STREAM ? 1 : 2) + 1;
@@ -382,8 +415,10 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   float* w = at<float>(ws, L.w);
   float* part = at<float>(ws, L.psum_part);
   const bool fused_hist = layer_fused_hist(s);
+  const bool rr = layer_reroutes(s);
+  float* scores = rr ? at<float>(ws, L.scores) : nullptr;
   if (e == cudaSuccess)
-    e = launch_router(s, xd, Wg, gate_bias, nullptr, ids, w, part, err, st,
+    e = launch_router(s, xd, Wg, gate_bias, scores, ids, w, part, err, st,
                       fused_hist ? at<int32_t>(ws, L.blk_hist) : nullptr);
   prof_mark(kMarkRouter, st);
   if (e == cudaSuccess) {
@@ -394,16 +429,36 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
     o.offs = at<int32_t>(ws, L.offs);
     o.src = at<int32_t>(ws, L.src);
     o.pos = at<int32_t>(ws, L.pos);
-    o.dropped = at<int32_t>(ws, L.dropped);
     o.blk_hist = at<int32_t>(ws, L.blk_hist);
     o.blk_base = at<int32_t>(ws, L.blk_base);
     o.psum_part = part;
     o.psum = at<float>(ws, L.psum);
     o.aux = aux;
     o.count_copy = count;
-    o.dropped_copy = dropped;
-    o.sched = at<int32_t>(ws, L.sched);
-    e = launch_dispatch(s, ids, xd, at<void>(ws, L.x_perm), o, err, st);
+    if (!rr) {
+      o.dropped = at<int32_t>(ws, L.dropped);
+      o.dropped_copy = dropped;
+      o.sched = at<int32_t>(ws, L.sched);
+    }
+    e = launch_dispatch(s, ids, rr ? nullptr : xd, rr ? nullptr : at<void>(ws, L.x_perm), o, err, st);
+  }
+  if (e == cudaSuccess && rr) {
+    // the routing's own counts (the loss) are in; now move the slots the
+    // capacity dropped, and group the moved routing
+    int32_t* fin = at<int32_t>(ws, L.fin);
+    e = launch_reroute(s, scores, ids, at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offs), fin,
+                       at<int32_t>(ws, L.pend), at<int32_t>(ws, L.choice), at<int32_t>(ws, L.dropped), dropped, st);
+    if (e == cudaSuccess) {
+      DispatchOut o;
+      memset(&o, 0, sizeof(o));
+      o.offs = at<int32_t>(ws, L.offs);
+      o.src = at<int32_t>(ws, L.src);
+      o.pos = at<int32_t>(ws, L.pos);
+      o.blk_hist = at<int32_t>(ws, L.blk_hist);
+      o.blk_base = at<int32_t>(ws, L.blk_base);
+      o.sched = at<int32_t>(ws, L.sched);
+      e = launch_dispatch(final_shape(s), fin, xd, at<void>(ws, L.x_perm), o, err, st);
+    }
   }
   prof_mark(kMarkDispatch, st);
   void* x_perm = at<void>(ws, L.x_perm);

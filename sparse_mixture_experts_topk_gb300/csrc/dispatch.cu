@@ -41,7 +41,7 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int bslo
   for (int64_t s = s0 + threadIdx.x; s < s1; s += kDispThreads) {
     const int e = ids[s];
     if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-    else set_error(err, kDevBadIndex);
+    else if (e != -1) set_error(err, kDevBadIndex);   // -1: the slot has no expert
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kDispThreads) blk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
@@ -450,7 +450,7 @@ dispatch_small_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, 
     const int64_t s = (int64_t)c * kDispThreads + threadIdx.x;
     if (s < S) {
       if (my[c] >= 0 && my[c] < E) atomicAdd(&hist[my[c]], 1);
-      else set_error(err, kDevBadIndex);
+      else if (my[c] != -1) set_error(err, kDevBadIndex);   // -1: the slot has no expert
     }
     if (my[c] < 0 || my[c] >= E) my[c] = -1;
   }

@@ -111,6 +111,15 @@ struct DispatchOut {
 cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, void* x_perm,
                             const DispatchOut& o, int* err, cudaStream_t st);
 
+// drop_tokens=False: fin [S] = each slot's expert after the over-capacity
+// slots (pos < 0 in the capacity-limited dispatch with row offsets offs) have
+// moved to their token's next-best expert with room, or -1; scores [T, E] are
+// the router's; pend, choice: [S] scratch.  dropped (nullable): slots left
+// without an expert.
+cudaError_t launch_reroute(const Shape& s, const float* scores, const int32_t* ids, const int32_t* pos,
+                           const int32_t* offs, int32_t* fin, int32_t* pend, int32_t* choice, int32_t* dropped,
+                           int32_t* dropped_copy, cudaStream_t st);
+
 // ---------------------------------------------------------------- expert FFN
 // The SM-pair expert GEMMs' counters: two tile counters, then one ready
 // counter per 256-row block of the kept rows (at most rows / 256 + E + 1).

@@ -45,6 +45,7 @@ class Workload:
     ffn_bias: bool = False
     temperature: float = 1.0      # router softmax temperature
     act: str = "gelu"             # "gelu" (Linear-GELU-Linear) | "swiglu" (W2 (SiLU(W1 x) * W3 x))
+    reroute: bool = False         # drop_tokens=False: over-capacity slots move to the next-best expert
     seed: int = 0
 
     @property
@@ -71,6 +72,9 @@ WORKLOADS = {
     # top-4 with a Zipf(1.2) gate bias and capacity ceil(T/E)*k = 2048
     "zipf_cap": Workload("zipf_cap", T=16384, H=3584, E=32, K=4, F=2560,
                          capacity=capacity_ceil(16384, 32, 4), gate_bias="zipf"),
+    # the same with drop_tokens=False: the slots over capacity move to the next-best expert with room
+    "zipf_reroute": Workload("zipf_reroute", T=16384, H=3584, E=32, K=4, F=2560,
+                             capacity=capacity_ceil(16384, 32, 4), gate_bias="zipf", reroute=True),
     # long prefill with wide hidden and many narrow experts
     "wide": Workload("wide", T=32768, H=4096, E=64, K=2, F=1408),
     # the prefill layer with SwiGLU experts (W1, W2, W3)

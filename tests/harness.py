@@ -48,6 +48,8 @@ def tdtype(w: W.Workload):
 def desc_of(w: W.Workload, flags: int = 0):
     if w.act == "swiglu":
         flags |= moe.MOE_FLAG_SWIGLU
+    if w.reroute:
+        flags |= moe.MOE_FLAG_REROUTE
     return moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                          moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
 
@@ -99,6 +101,14 @@ def run_stages(dev: Dev, flags: int = 0):
     r["dropped"] = t.empty((1,), dtype=t.int32, device="cuda")
     moe.moe_dispatch(d, r["ids"], dev.x, r["count"], r["offs"], r["src"], r["pos"], r["x_perm"],
                      r["dropped"], ws)
+    if w.reroute and w.capacity > 0:
+        # drop_tokens=False: move the slots the capacity dropped, then group
+        # the moved routing (the routing's own counts stay in r["count"])
+        r["ids_final"] = t.empty((T, K), dtype=t.int32, device="cuda")
+        moe.moe_reroute(d, r["logits"], r["ids"], r["pos"], r["offs"], r["ids_final"], r["dropped"], ws)
+        r["count_final"] = t.empty((E,), dtype=t.int32, device="cuda")
+        moe.moe_dispatch(d, r["ids_final"], dev.x, r["count_final"], r["offs"], r["src"], r["pos"],
+                         r["x_perm"], None, ws)
     r["h_perm"] = t.zeros((R, F), dtype=dt, device="cuda")
     r["y_perm"] = t.zeros((R, H), dtype=dt, device="cuda")
     moe.moe_expert_ffn(d, r["x_perm"], r["offs"], dev.W1, dev.b1, dev.W2, dev.b2, r["h_perm"],
@@ -171,3 +181,11 @@ PSUM_REL = 2e-5            # fp32 sums of T probabilities
 OUT_MAXABS_BF16 = 2e-2     # layer output vs the bf16-rounded oracle
 OUT_REL_L2_BF16 = 1e-2
 OUT_REL_L2_F32 = 1e-4
+
+
+def oracle_dispatch(w: W.Workload, ids_o, scores):
+    """The oracle's dispatch of the routing ids_o (from the GPU's scores):
+    with drop_tokens=False the rerouted one."""
+    if w.reroute and w.capacity > 0:
+        return O.dispatch_rerouted(ids_o, scores, w.E, w.capacity)
+    return O.dispatch(ids_o, w.E, w.capacity)

@@ -34,7 +34,7 @@ import sparse_mixture_experts_topk_gb300 as moe
 from oracle import moe_oracle as O
 
 from harness import (Dev, run_stages, run_layer, to_np, as_f64, logits_rel_err, out_errors, product_tol,
-                     GELU_SLOPE, LOGITS_REL, W_ABS, PSUM_REL, OUT_MAXABS_BF16, OUT_REL_L2_BF16)
+                     oracle_dispatch, GELU_SLOPE, LOGITS_REL, W_ABS, PSUM_REL, OUT_MAXABS_BF16, OUT_REL_L2_BF16)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +61,8 @@ class _PerExpert:
         return O.widen(self.a[e], self.dtype)
 
 
-@pytest.mark.parametrize("name", ["decode1", "decode8", "decode16r", "prefill", "zipf_cap", "wide",
-                                  "prefill_swiglu"])
+@pytest.mark.parametrize("name", ["decode1", "decode8", "decode16r", "prefill", "zipf_cap", "zipf_reroute",
+                                  "wide", "prefill_swiglu"])
 def test_full_size(name):
     w = W.WORKLOADS[name]
     inp = W.generate(w)
@@ -84,7 +84,10 @@ def test_full_size(name):
     np.testing.assert_allclose(to_np(r["psum"]), p_o.sum(0), rtol=PSUM_REL, atol=1e-5)
 
     # dispatch, in full
-    d = O.dispatch(ids_o, w.E, w.capacity)
+    d = oracle_dispatch(w, ids_o, gl)
+    if w.reroute:
+        np.testing.assert_array_equal(to_np(r["ids_final"]), d["final"])
+        assert d["dropped"] < O.dispatch(ids_o, w.E, w.capacity)["dropped"]   # the move saves slots
     for k_ in ("count", "offs", "pos"):
         np.testing.assert_array_equal(to_np(r[k_]), d[k_])
     R = int(d["offs"][-1])
@@ -95,6 +98,8 @@ def test_full_size(name):
     assert w.capacity > 0 or d["dropped"] == 0
     if name == "zipf_cap":
         assert d["dropped"] > 0           # the Zipf prior overfills the first experts
+    if name == "zipf_reroute":
+        assert (d["kept"] <= w.capacity).all() and d["kept"].sum() > O.dispatch(ids_o, w.E, w.capacity)["kept"].sum()
     if w.x_kind == "decode_distinct":
         assert sorted(ids_o.reshape(-1).tolist()) == list(range(2 * w.T))
     if name == "decode16r":

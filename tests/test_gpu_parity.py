@@ -19,7 +19,7 @@ from sparse_mixture_experts_topk_gb300 import workloads as W
 import sparse_mixture_experts_topk_gb300 as moe
 from oracle import moe_oracle as O
 
-from harness import (Dev, run_stages, run_layer, to_np, as_f64, logits_rel_err, out_errors,
+from harness import (Dev, run_stages, run_layer, to_np, as_f64, logits_rel_err, out_errors, oracle_dispatch,
                      LOGITS_REL, W_ABS, PSUM_REL, OUT_MAXABS_BF16, OUT_REL_L2_BF16, OUT_REL_L2_F32)
 
 pytestmark = pytest.mark.gpu
@@ -67,6 +67,18 @@ SMALL = {
     # expert product's last k-block is partly zero-filled
     "h_ragged": W.small("h_ragged", T=300, H=200, E=8, K=2, F=264),
     "h_ragged_decode": W.small("h_ragged_decode", T=5, H=200, E=8, K=2, F=264),
+    # drop_tokens=False: the slots over capacity move to the next-best expert with room
+    "reroute_k4": W.small("reroute_k4", T=300, H=256, E=8, K=4, F=384,
+                          capacity=W.capacity_ceil(300, 8, 4) // 2, gate_bias="zipf", reroute=True),
+    # every token prefers experts 0 and 1: most slots move, in score order, to the other experts
+    "reroute_hot2": W.small("reroute_hot2", T=700, H=256, E=8, K=2, F=384, gate_bias="hot",
+                            capacity=W.capacity_ceil(700, 8, 2), reroute=True),
+    # one-block dispatch on both sides of the move
+    "reroute_small": W.small("reroute_small", T=100, H=128, E=8, K=2, F=64,
+                             capacity=W.capacity_ceil(100, 8, 2) // 2, gate_bias="zipf", reroute=True),
+    # many experts, top-8: many epochs of the move
+    "reroute_e64_k8": W.small("reroute_e64_k8", T=700, H=128, E=64, K=8, F=64, gate_bias="zipf",
+                              capacity=W.capacity_ceil(700, 64, 8) // 2, reroute=True),
 }
 
 
@@ -97,8 +109,10 @@ def _check_routing(w, inp, r, x64, Wg64):
     return gl, ids_o, w_o, p_o
 
 
-def _check_dispatch(w, r, ids_o, x_bytes):
-    d = O.dispatch(ids_o, w.E, w.capacity)
+def _check_dispatch(w, r, ids_o, x_bytes, scores):
+    d = oracle_dispatch(w, ids_o, scores)
+    if "ids_final" in r:
+        np.testing.assert_array_equal(to_np(r["ids_final"]), d["final"])
     np.testing.assert_array_equal(to_np(r["count"]), d["count"])
     np.testing.assert_array_equal(to_np(r["offs"]), d["offs"])
     R = int(d["offs"][-1])
@@ -121,7 +135,7 @@ def test_stages_and_layer_small(name):
     r = run_stages(dev)
     assert r["device_error"] == 0
     gl, ids_o, w_o, p_o = _check_routing(w, inp, r, x64, Wg64)
-    d = _check_dispatch(w, r, ids_o, inp.x)
+    d = _check_dispatch(w, r, ids_o, inp.x, gl)
     R = int(d["offs"][-1])
 
     # expert FFN, one product at a time
@@ -164,7 +178,8 @@ def test_stages_and_layer_small(name):
     ref = O.layer_forward(x64, Wg64, W164, W264, w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
                           b1=None if inp.b1 is None else inp.b1.astype(np.float64),
                           b2=None if inp.b2 is None else inp.b2.astype(np.float64),
-                          bf16=bf, logits=gl, temperature=w.temperature, act=w.act)
+                          bf16=bf, logits=gl, temperature=w.temperature, act=w.act,
+                          reroute_over=w.reroute)
     mx, rel = out_errors(out_gpu, ref["out"])
     if bf:
         assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
@@ -228,7 +243,7 @@ def test_cuda_core_router_and_ffn_match_oracle(name):
     r = run_stages(dev, flags=moe.MOE_FLAG_SIMT_ROUTER | moe.MOE_FLAG_SIMT_FFN)
     assert r["device_error"] == 0
     gl, ids_o, w_o, p_o = _check_routing(w, inp, r, x64, Wg64)
-    d = _check_dispatch(w, r, ids_o, inp.x)
+    d = _check_dispatch(w, r, ids_o, inp.x, gl)
     ref = O.layer_forward(x64, Wg64, O.widen(inp.W1, w.dtype), O.widen(inp.W2, w.dtype), w.K,
                           capacity=w.capacity, gate_bias=inp.gate_bias, bf16=True, logits=gl)
     mx, rel = out_errors(as_f64(r["out"]), ref["out"])
@@ -280,7 +295,7 @@ def test_expert_gemm_kernels_match_oracle(name, kind):
     assert r["device_error"] == 0
     x64, Wg64 = O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype)
     gl, ids_o, w_o, p_o = _check_routing(w, inp, r, x64, Wg64)
-    d = _check_dispatch(w, r, ids_o, inp.x)
+    d = _check_dispatch(w, r, ids_o, inp.x, gl)
     R = int(d["offs"][-1])
     W164, W264 = O.widen(inp.W1, w.dtype), O.widen(inp.W2, w.dtype)
     xp, h_gpu, y_gpu = as_f64(r["x_perm"])[:R], as_f64(r["h_perm"])[:R], as_f64(r["y_perm"])[:R]
