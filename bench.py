@@ -319,8 +319,8 @@ def run_ours(args, w: W.Workload):
     if moe.moe_get_device_error(ws) != 0:
         raise RuntimeError("device error flag set during warm-up")
     c = count.cpu().numpy()
-    rows = int(np.minimum(c, w.capacity).sum()) if w.capacity > 0 else int(c.sum())
-    used = int((c > 0).sum())
+    rows = w.S - int(dropped.item())         # kept rows (moved ones included under drop_tokens=False)
+    used = int((c > 0).sum()) if not w.reroute else w.E
 
     # Timed region.  Loop A (the headline): CUDA events around each whole layer
     # call only, so the library's kernels chain with programmatic dependent

@@ -279,8 +279,14 @@ int moe_aux_loss(const moe_desc* desc, const float* psum, const int32_t* count,
  * enqueued on one stream with no host synchronisation (mlqm.cn section 3.2).
  *   x [T, H], out [T, H] dtype: device pointers, or host pointers if
  *     desc->flags has MOE_FLAG_HOST_IO (then the call copies x in and out
- *     through the workspace on `stream`; pinned host memory is fastest, and
- *     `out` is valid once the stream has been synchronised)
+ *     through the workspace; pinned host memory is fastest, and `out` is
+ *     valid once `stream` has been synchronised).  With host pointers, no
+ *     capacity and T >= 2048, the batch runs as two halves of tokens whose
+ *     copies overlap the other half's layer: the copies go on two internal
+ *     streams (created on the first such call of each host thread on each
+ *     device, kept until the process exits) joined to `stream` by events,
+ *     the outputs are the same bits, and count and the loss are the whole
+ *     batch's.
  *   aux [1] fp32 out or NULL; count [E] int32 out or NULL; dropped [1] int32
  *     out or NULL (device pointers)
  */

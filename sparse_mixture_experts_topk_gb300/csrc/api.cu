@@ -134,7 +134,7 @@ namespace {
 
 struct Layout {
   size_t err, sched, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
-  size_t pend, choice, scores, fin;
+  size_t pend, choice, alts, scores, fin, count_chunks, psum_chunks;
   size_t x_perm, h_perm, x_stage, out_stage, total;
   int64_t rows;
 };
@@ -192,6 +192,7 @@ Layout layout_of(const moe_desc& d) {
   L.pos = take(S * 4);
   L.pend = take(S * 4);          // moving over-capacity slots (drop_tokens=False)
   L.choice = take(S * 4);
+  L.alts = take((size_t)s.T * E);
   L.scores = L.fin = 0;
   if (d.flags & MOE_FLAG_REROUTE) {
     L.scores = take((size_t)s.T * E * 4);
@@ -199,6 +200,8 @@ Layout layout_of(const moe_desc& d) {
   }
   L.x_perm = take((size_t)L.rows * s.H * es);   // also holds y_perm in the layer call
   L.h_perm = take((size_t)L.rows * s.F * es);
+  L.count_chunks = take(2 * E * 4);   // per-piece counts and sums of the chunked host-I/O path
+  L.psum_chunks = take(2 * E * 4);
   L.x_stage = L.out_stage = 0;
   if (d.flags & MOE_FLAG_HOST_IO) {
     L.x_stage = take((size_t)s.T * s.H * es);
@@ -303,7 +306,8 @@ int moe_reroute(const moe_desc* desc, const float* logits, const int32_t* ids, c
   if (d.T > 0 && (!logits || !ids || !pos || !offs || !ids_out)) return MOE_ERR_INVALID;
   const Layout L = layout_of(d);
   return cuda_status(launch_reroute(shape_of(d), logits, ids, pos, offs, ids_out, at<int32_t>(ws, L.pend),
-                                    at<int32_t>(ws, L.choice), dropped, nullptr, (cudaStream_t)stream));
+                                    at<int32_t>(ws, L.choice), at<uint8_t>(ws, L.alts), dropped, nullptr,
+                                    (cudaStream_t)stream));
 }
 
 int moe_expert_ffn(const moe_desc* desc, const void* x_perm, const int32_t* offs, const void* W1,
@@ -358,6 +362,18 @@ Shape final_shape(const Shape& s) {
   f.C = 0;
   return f;
 }
+// Host-I/O layers without a capacity are split into kIoChunks pieces of
+// tokens: a token's output depends only on its own row then, so the pieces
+// give the same outputs, and the copy of one piece overlaps the layer on
+// another.  Every piece reads all the expert weights again, so the pieces
+// stay few.
+constexpr int kIoChunks = 2;
+constexpr int64_t kIoMinChunkTokens = 1024;
+
+bool io_chunked(const Shape& s) {
+  return (s.flags & MOE_FLAG_HOST_IO) && s.C <= 0 && s.T >= kIoChunks * kIoMinChunkTokens;
+}
+int64_t io_chunk_begin(const Shape& s, int c) { return s.T * c / kIoChunks; }
 }  // namespace moe
 
 int moe_layer_launches(const moe_desc* desc) {
@@ -369,7 +385,16 @@ int moe_layer_launches(const moe_desc* desc) {
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
   if (layer_reroutes(s)) {
     if (!dispatch_small(s)) n -= 1;                     // the first dispatch gathers nothing
-    n += 1 + dispatch_launches(final_shape(s), false);  // the move, then the dispatch of the moved routing
+    n += 2 + dispatch_launches(final_shape(s), false);  // the move (2), then the dispatch of the moved routing
+  }
+  if (s.T > 0 && io_chunked(s)) {                       // two pieces of tokens, then the statistics
+    n = 1;
+    for (int c = 0; c < kIoChunks; ++c) {
+      moe_desc dc = *desc;
+      dc.T = io_chunk_begin(s, c + 1) - io_chunk_begin(s, c);
+      dc.flags &= ~MOE_FLAG_HOST_IO;
+      n += moe_layer_launches(&dc);
+    }
   }
   if (s.T > 0) {                                        // expert FFN, combine
     const int k = ffn_kernel(s, rows_for(*desc));
@@ -383,6 +408,121 @@ int moe_ffn_kernel(const moe_desc* desc) {
   if (rc) return rc;
   return ffn_kernel(shape_of(*desc), rows_for(*desc));
 }
+
+namespace moe {
+namespace {
+
+// Where one pass of the layer puts its statistics.
+struct LayerStats {
+  int32_t* count;         // [E] routing counts (workspace)
+  float* psum;            // [E] probability sums (workspace)
+  float* aux;             // [1] loss, or null
+  int32_t* count_copy;    // [E] caller's count, or null
+  int32_t* dropped_copy;  // [1] caller's dropped, or null
+};
+
+// The layer on device buffers xd -> outd (T = s.T tokens), on stream st.
+cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, const void* xd, const void* Wg,
+                      const float* gate_bias, const void* W1, const float* b1, const void* W2, const float* b2,
+                      void* outd, const LayerStats& ls, bool marks, cudaStream_t st) {
+  int* err = at<int>(ws, L.err);
+  cudaError_t e = cudaSuccess;
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  float* part = at<float>(ws, L.psum_part);
+  const bool fused_hist = layer_fused_hist(s);
+  const bool rr = layer_reroutes(s);
+  float* scores = rr ? at<float>(ws, L.scores) : nullptr;
+  e = launch_router(s, xd, Wg, gate_bias, scores, ids, w, part, err, st,
+                    fused_hist ? at<int32_t>(ws, L.blk_hist) : nullptr);
+  if (marks) prof_mark(kMarkRouter, st);
+  if (e == cudaSuccess) {
+    DispatchOut o;
+    memset(&o, 0, sizeof(o));
+    o.hist_ready = fused_hist;
+    o.count = ls.count;
+    o.offs = at<int32_t>(ws, L.offs);
+    o.src = at<int32_t>(ws, L.src);
+    o.pos = at<int32_t>(ws, L.pos);
+    o.blk_hist = at<int32_t>(ws, L.blk_hist);
+    o.blk_base = at<int32_t>(ws, L.blk_base);
+    o.psum_part = part;
+    o.psum = ls.psum;
+    o.aux = ls.aux;
+    o.count_copy = ls.count_copy;
+    if (!rr) {
+      o.dropped = at<int32_t>(ws, L.dropped);
+      o.dropped_copy = ls.dropped_copy;
+      o.sched = at<int32_t>(ws, L.sched);
+    }
+    e = launch_dispatch(s, ids, rr ? nullptr : xd, rr ? nullptr : at<void>(ws, L.x_perm), o, err, st);
+  }
+  if (e == cudaSuccess && rr) {
+    // the routing's own counts (the loss) are in; now move the slots the
+    // capacity dropped, and group the moved routing
+    int32_t* fin = at<int32_t>(ws, L.fin);
+    e = launch_reroute(s, scores, ids, at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offs), fin,
+                       at<int32_t>(ws, L.pend), at<int32_t>(ws, L.choice), at<uint8_t>(ws, L.alts),
+                       at<int32_t>(ws, L.dropped), ls.dropped_copy, st);
+    if (e == cudaSuccess) {
+      DispatchOut o;
+      memset(&o, 0, sizeof(o));
+      o.offs = at<int32_t>(ws, L.offs);
+      o.src = at<int32_t>(ws, L.src);
+      o.pos = at<int32_t>(ws, L.pos);
+      o.blk_hist = at<int32_t>(ws, L.blk_hist);
+      o.blk_base = at<int32_t>(ws, L.blk_base);
+      o.sched = at<int32_t>(ws, L.sched);
+      e = launch_dispatch(final_shape(s), fin, xd, at<void>(ws, L.x_perm), o, err, st);
+    }
+  }
+  if (marks) prof_mark(kMarkDispatch, st);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h_perm = at<void>(ws, L.h_perm);
+  void* y_perm = x_perm;   // x_perm is dead once the first product has run
+  if (e == cudaSuccess)
+    e = launch_ffn(s, rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
+                   at<int32_t>(ws, L.sched), st);
+  if (marks) prof_mark(kMarkSecond, st);
+  if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
+  if (marks) prof_mark(kMarkCombine, st);
+  return e;
+}
+
+// The copy streams and events of the chunked host-I/O path, created once per
+// host thread and device.
+struct IoRes {
+  bool ok = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, in[kIoChunks] = {}, done[kIoChunks] = {}, end = nullptr;
+};
+constexpr int kMaxIoDevices = 64;
+thread_local IoRes g_io[kMaxIoDevices];
+
+cudaError_t io_resources(IoRes** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxIoDevices) return cudaErrorInvalidDevice;
+  IoRes& r = g_io[dev];
+  if (!r.ok) {
+    const unsigned ef = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&r.h2d, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&r.d2h, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&r.start, ef)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&r.end, ef)) != cudaSuccess) return e;
+    for (int c = 0; c < kIoChunks; ++c) {
+      if ((e = cudaEventCreateWithFlags(&r.in[c], ef)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&r.done[c], ef)) != cudaSuccess) return e;
+    }
+    r.ok = true;
+  }
+  *out = &r;
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
 
 int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const float* gate_bias,
                       const void* W1, const float* b1, const void* W2, const float* b2, void* out,
@@ -400,76 +540,64 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
   const Layout L = layout_of(d);
   const Shape s = shape_of(d);
   cudaStream_t st = (cudaStream_t)stream;
-  int* err = at<int>(ws, L.err);
-  const size_t xbytes = (size_t)s.T * s.H * s.esize();
+  const size_t row_bytes = (size_t)s.H * s.esize();
+  cudaError_t e = cudaSuccess;
+  if (host_io && io_chunked(s)) {
+    // two pieces of tokens: the H2D of the second overlaps the layer on the
+    // first, the D2H of the first the layer on the second
+    IoRes* io = nullptr;
+    if ((e = io_resources(&io)) != cudaSuccess) return cuda_status(e);
+    char* xs = at<char>(ws, L.x_stage);
+    char* os = at<char>(ws, L.out_stage);
+    e = cudaEventRecord(io->start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(io->h2d, io->start, 0);
+    for (int c = 0; c < kIoChunks && e == cudaSuccess; ++c) {
+      const int64_t t0 = io_chunk_begin(s, c), t1 = io_chunk_begin(s, c + 1);
+      e = cudaMemcpyAsync(xs + t0 * row_bytes, (const char*)x + t0 * row_bytes, (size_t)(t1 - t0) * row_bytes,
+                          cudaMemcpyHostToDevice, io->h2d);
+      if (e == cudaSuccess) e = cudaEventRecord(io->in[c], io->h2d);
+    }
+    for (int c = 0; c < kIoChunks && e == cudaSuccess; ++c) {
+      const int64_t t0 = io_chunk_begin(s, c), t1 = io_chunk_begin(s, c + 1);
+      Shape sc = s;
+      sc.T = t1 - t0;
+      moe_desc dc = d;
+      dc.T = sc.T;
+      const LayerStats ls{at<int32_t>(ws, L.count_chunks) + (size_t)c * s.E,
+                          at<float>(ws, L.psum_chunks) + (size_t)c * s.E, nullptr, nullptr, nullptr};
+      e = cudaStreamWaitEvent(st, io->in[c], 0);
+      if (e == cudaSuccess)
+        e = run_layer(sc, rows_for(dc), L, ws, xs + t0 * row_bytes, Wg, gate_bias, W1, b1, W2, b2,
+                      os + t0 * row_bytes, ls, false, st);
+      if (e == cudaSuccess) e = cudaEventRecord(io->done[c], st);
+    }
+    for (int c = 0; c < kIoChunks && e == cudaSuccess; ++c) {
+      const int64_t t0 = io_chunk_begin(s, c), t1 = io_chunk_begin(s, c + 1);
+      e = cudaStreamWaitEvent(io->d2h, io->done[c], 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync((char*)out + t0 * row_bytes, os + t0 * row_bytes, (size_t)(t1 - t0) * row_bytes,
+                            cudaMemcpyDeviceToHost, io->d2h);
+    }
+    // the whole batch's counts and loss from the pieces' sums
+    if (e == cudaSuccess)
+      e = launch_merge_stats(s, at<int32_t>(ws, L.count_chunks), at<float>(ws, L.psum_chunks), kIoChunks,
+                             at<int32_t>(ws, L.count), at<float>(ws, L.psum), count, aux, dropped, st);
+    if (e == cudaSuccess) e = cudaEventRecord(io->end, io->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, io->end, 0);   // the caller's stream covers it all
+    return cuda_status(e);
+  }
+  const size_t xbytes = (size_t)s.T * row_bytes;
   const void* xd = x;
   void* outd = out;
-  cudaError_t e = cudaSuccess;
   prof_mark(kMarkStart, st);
   if (host_io && s.T > 0) {
     xd = at<void>(ws, L.x_stage);
     outd = at<void>(ws, L.out_stage);
     e = cudaMemcpyAsync((void*)xd, x, xbytes, cudaMemcpyHostToDevice, st);
   }
-  int32_t* ids = at<int32_t>(ws, L.ids);
-  float* w = at<float>(ws, L.w);
-  float* part = at<float>(ws, L.psum_part);
-  const bool fused_hist = layer_fused_hist(s);
-  const bool rr = layer_reroutes(s);
-  float* scores = rr ? at<float>(ws, L.scores) : nullptr;
+  const LayerStats ls{at<int32_t>(ws, L.count), at<float>(ws, L.psum), aux, count, dropped};
   if (e == cudaSuccess)
-    e = launch_router(s, xd, Wg, gate_bias, scores, ids, w, part, err, st,
-                      fused_hist ? at<int32_t>(ws, L.blk_hist) : nullptr);
-  prof_mark(kMarkRouter, st);
-  if (e == cudaSuccess) {
-    DispatchOut o;
-    memset(&o, 0, sizeof(o));
-    o.hist_ready = fused_hist;
-    o.count = at<int32_t>(ws, L.count);
-    o.offs = at<int32_t>(ws, L.offs);
-    o.src = at<int32_t>(ws, L.src);
-    o.pos = at<int32_t>(ws, L.pos);
-    o.blk_hist = at<int32_t>(ws, L.blk_hist);
-    o.blk_base = at<int32_t>(ws, L.blk_base);
-    o.psum_part = part;
-    o.psum = at<float>(ws, L.psum);
-    o.aux = aux;
-    o.count_copy = count;
-    if (!rr) {
-      o.dropped = at<int32_t>(ws, L.dropped);
-      o.dropped_copy = dropped;
-      o.sched = at<int32_t>(ws, L.sched);
-    }
-    e = launch_dispatch(s, ids, rr ? nullptr : xd, rr ? nullptr : at<void>(ws, L.x_perm), o, err, st);
-  }
-  if (e == cudaSuccess && rr) {
-    // the routing's own counts (the loss) are in; now move the slots the
-    // capacity dropped, and group the moved routing
-    int32_t* fin = at<int32_t>(ws, L.fin);
-    e = launch_reroute(s, scores, ids, at<int32_t>(ws, L.pos), at<int32_t>(ws, L.offs), fin,
-                       at<int32_t>(ws, L.pend), at<int32_t>(ws, L.choice), at<int32_t>(ws, L.dropped), dropped, st);
-    if (e == cudaSuccess) {
-      DispatchOut o;
-      memset(&o, 0, sizeof(o));
-      o.offs = at<int32_t>(ws, L.offs);
-      o.src = at<int32_t>(ws, L.src);
-      o.pos = at<int32_t>(ws, L.pos);
-      o.blk_hist = at<int32_t>(ws, L.blk_hist);
-      o.blk_base = at<int32_t>(ws, L.blk_base);
-      o.sched = at<int32_t>(ws, L.sched);
-      e = launch_dispatch(final_shape(s), fin, xd, at<void>(ws, L.x_perm), o, err, st);
-    }
-  }
-  prof_mark(kMarkDispatch, st);
-  void* x_perm = at<void>(ws, L.x_perm);
-  void* h_perm = at<void>(ws, L.h_perm);
-  void* y_perm = x_perm;   // x_perm is dead once the first product has run
-  if (e == cudaSuccess)
-    e = launch_ffn(s, L.rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
-                   at<int32_t>(ws, L.sched), st);
-  prof_mark(kMarkSecond, st);
-  if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
-  prof_mark(kMarkCombine, st);
+    e = run_layer(s, L.rows, L, ws, xd, Wg, gate_bias, W1, b1, W2, b2, outd, ls, true, st);
   if (e == cudaSuccess && host_io && s.T > 0)
     e = cudaMemcpyAsync(out, outd, xbytes, cudaMemcpyDeviceToHost, st);
   return cuda_status(e);

@@ -41,7 +41,44 @@ __global__ void aux_kernel(const float* __restrict__ psum, const int32_t* __rest
   if (e == 0) *loss = (float)E * sa[0];
 }
 
+__global__ void merge_stats_kernel(const int32_t* __restrict__ count_parts, const float* __restrict__ psum_parts,
+                                   int n, int E, int64_t Tn, int K, int32_t* __restrict__ count,
+                                   float* __restrict__ psum, int32_t* __restrict__ count_copy,
+                                   float* __restrict__ aux, int32_t* __restrict__ dropped) {
+  __shared__ float sa[256];
+  pdl_enter();
+  const int e = threadIdx.x;
+  int c = 0;
+  float p = 0.f;
+  if (e < E) {
+    for (int i = 0; i < n; ++i) {
+      c += count_parts[(int64_t)i * E + e];
+      p += psum_parts[(int64_t)i * E + e];
+    }
+    count[e] = c;
+    psum[e] = p;
+    if (count_copy) count_copy[e] = c;
+  }
+  sa[e] = (e < E && Tn > 0) ? ((float)c / (float)(Tn * K)) * (p / (float)Tn) : 0.f;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (e < o) sa[e] += sa[e + o];
+    __syncthreads();
+  }
+  if (e == 0) {
+    if (aux) *aux = (float)E * sa[0];
+    if (dropped) *dropped = 0;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_merge_stats(const Shape& s, const int32_t* count_parts, const float* psum_parts, int n,
+                               int32_t* count, float* psum, int32_t* count_copy, float* aux, int32_t* dropped,
+                               cudaStream_t st) {
+  return launch_kernel(merge_stats_kernel, dim3(1), dim3(256), 0, st, 1, count_parts, psum_parts, n, s.E, s.T, s.K,
+                       count, psum, count_copy, aux, dropped);
+}
 
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* pos, const float* w,
                            void* out, cudaStream_t st) {

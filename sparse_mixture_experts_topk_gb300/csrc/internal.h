@@ -114,11 +114,11 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
 // drop_tokens=False: fin [S] = each slot's expert after the over-capacity
 // slots (pos < 0 in the capacity-limited dispatch with row offsets offs) have
 // moved to their token's next-best expert with room, or -1; scores [T, E] are
-// the router's; pend, choice: [S] scratch.  dropped (nullable): slots left
-// without an expert.
+// the router's; pend, choice: [S] and alts: [T, E] scratch.  dropped
+// (nullable): slots left without an expert.  Two launches.
 cudaError_t launch_reroute(const Shape& s, const float* scores, const int32_t* ids, const int32_t* pos,
-                           const int32_t* offs, int32_t* fin, int32_t* pend, int32_t* choice, int32_t* dropped,
-                           int32_t* dropped_copy, cudaStream_t st);
+                           const int32_t* offs, int32_t* fin, int32_t* pend, int32_t* choice, uint8_t* alts,
+                           int32_t* dropped, int32_t* dropped_copy, cudaStream_t st);
 
 // ---------------------------------------------------------------- expert FFN
 // The SM-pair expert GEMMs' counters: two tile counters, then one ready
@@ -139,5 +139,11 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* po
                            void* out, cudaStream_t st);
 cudaError_t launch_aux(const Shape& s, const float* psum, const int32_t* count, float* loss,
                        cudaStream_t st);
+// The statistics of a layer run in pieces of tokens: count[e] and psum[e]
+// summed over the n pieces in order, then the loss of the whole batch (s.T
+// tokens); count_copy, aux and dropped (0: no capacity) are nullable.
+cudaError_t launch_merge_stats(const Shape& s, const int32_t* count_parts, const float* psum_parts, int n,
+                               int32_t* count, float* psum, int32_t* count_copy, float* aux, int32_t* dropped,
+                               cudaStream_t st);
 
 }  // namespace moe

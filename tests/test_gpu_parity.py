@@ -232,6 +232,36 @@ def test_host_io_layer_matches_device_layer():
     assert torch.equal(outh.view(torch.int16), ref["out"].cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("T", [2048, 2501])
+def test_chunked_host_io_layer_matches_device_layer(T):
+    """With host buffers and no capacity the call runs the batch in two
+    pieces of tokens, each piece's copies overlapping the other's layer: the
+    output is the device layer's bit for bit (a token's output depends on its
+    own row only), the counts are equal and the loss is the whole batch's."""
+    torch = pytest.importorskip("torch")
+    w = W.small("io_chunks", T=T, H=256, E=8, K=2, F=384)
+    dev = Dev(W.generate(w))
+    ref = run_layer(dev)
+    d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, 0, moe.MOE_BF16, moe.MOE_FLAG_HOST_IO)
+    ws = moe.workspace(d)
+    xh = dev.x.cpu().pin_memory()
+    outh = torch.full_like(xh, 7.0).pin_memory()
+    aux = torch.full((1,), -1.0, device="cuda")
+    count = torch.full((w.E,), -1, dtype=torch.int32, device="cuda")
+    dropped = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    moe.moe_layer_forward(d, xh, dev.Wg, None, dev.W1, None, dev.W2, None, outh, aux, count, dropped, ws)
+    torch.cuda.current_stream().synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    assert torch.equal(outh.view(torch.int16), ref["out"].cpu().view(torch.int16))
+    assert torch.equal(count, ref["count"]) and int(dropped.item()) == 0
+    assert float(aux.item()) == pytest.approx(float(ref["aux"].item()), rel=2e-6)
+    # a second call on the same workspace and streams gives the same bits
+    outh2 = torch.empty_like(xh).pin_memory()
+    moe.moe_layer_forward(d, xh, dev.Wg, None, dev.W1, None, dev.W2, None, outh2, None, None, None, ws)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(outh2.view(torch.int16), outh.view(torch.int16))
+
+
 @pytest.mark.parametrize("name", ["ragged_bf16", "e64_k8", "cap_zipf_k4"])
 def test_cuda_core_router_and_ffn_match_oracle(name):
     """The CUDA-core router and expert FFN (kept for fp32 layers and as a
