@@ -83,6 +83,10 @@ def config_of(w: W.Workload, world: int, rows: int, used: int, gemm: str):
             "parallelism": f"replicas x{world}", "kept_rows": rows, "used_experts": used, "gemm": gemm}
 
 
+def gemm_desc(args) -> str:
+    return args.gemm + ("+fused-combine" if getattr(args, "fused_combine", False) else "")
+
+
 def describe(w: W.Workload) -> str:
     cap = f" capacity={w.capacity}" if w.capacity > 0 else ""
     return f"{w.name}: T={w.T} H={w.H} E={w.E} k={w.K} F={w.F} {w.dtype}{cap}"
@@ -231,7 +235,8 @@ def run_reference(args, w: W.Workload):
     wide = widen_inputs(inp)
     # the whole batch's routing (cheap) for the kept rows and used experts
     ids, _, _ = O.route(O.gate_logits(wide[0], wide[1], inp.gate_bias), w.K, w.temperature)
-    dd = O.dispatch(ids, w.E, w.capacity)
+    dd = O.dispatch_rerouted(ids, O.gate_logits(wide[0], wide[1], inp.gate_bias), w.E, w.capacity) \
+        if (w.reroute and w.capacity > 0) else O.dispatch(ids, w.E, w.capacity)
     budget = 150.0 / max(1, args.steps + args.warmup)     # seconds per step
     n = min(16, w.T)
     while n < w.T and oracle_rate(inp, wide, n) < budget / 2.5:
@@ -245,7 +250,7 @@ def run_reference(args, w: W.Workload):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": config_of(w, world, int(dd["offs"][-1]), int((dd["count"] > 0).sum()), args.gemm),
+            "config": config_of(w, world, int(dd["offs"][-1]), int((dd["count"] > 0).sum()), gemm_desc(args)),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
                              "sample": f"fp64 numpy oracle, whole layer on the first {n} of {w.T} "
                                        f"tokens per step ({n} tokens timed per step)"},
@@ -288,7 +293,7 @@ def run_ours(args, w: W.Workload):
     gb = to_dev(inp.gate_bias, torch)
     dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
     flags = (moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0) | (moe.MOE_FLAG_REROUTE if w.reroute else 0) | \
-        GEMM_FLAGS[args.gemm]
+        (moe.MOE_FLAG_FUSED_COMBINE if args.fused_combine else 0) | GEMM_FLAGS[args.gemm]
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                       moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
     launches_per_step = moe.moe_layer_launches(d)
@@ -320,7 +325,7 @@ def run_ours(args, w: W.Workload):
         raise RuntimeError("device error flag set during warm-up")
     c = count.cpu().numpy()
     rows = w.S - int(dropped.item())         # kept rows (moved ones included under drop_tokens=False)
-    used = int((c > 0).sum()) if not w.reroute else w.E
+    used = int((c > 0).sum())
 
     # Timed region.  Loop A (the headline): CUDA events around each whole layer
     # call only, so the library's kernels chain with programmatic dependent
@@ -423,7 +428,7 @@ def run_ours(args, w: W.Workload):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
         "data": "synthetic",
-        "config": config_of(w, world, rows, used, args.gemm),
+        "config": config_of(w, world, rows, used, gemm_desc(args)),
         "roofline": roof,
         "stages": stages,
         "stage_timing": {"ms_per_step_with_stage_events": staged_step_ms,
@@ -500,6 +505,8 @@ def main():
     ap.add_argument("--min-warmup-s", type=float, default=1.5)
     ap.add_argument("--gemm", default="auto", choices=sorted(GEMM_FLAGS),
                     help="expert GEMM kernel for bf16 prefill: the library's choice, or one forced")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="fold the weighted combine into the second expert product's epilogue")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -92,6 +92,15 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * stay those of the routing's own choices; `dropped` counts the slots left
  * without an expert.  No effect without a capacity. */
 #define MOE_FLAG_REROUTE     (1u << 10)
+/* bf16, K <= 2, SM-pair expert GEMMs: moe_layer_forward folds the weighted
+ * combine into the second expert product's epilogue (each output row adds
+ * w * y, with y rounded to bf16 as stored, to an fp32 copy of out in the
+ * workspace with vector reductions; two additions onto zero give the same
+ * sum in either order, so the result is deterministic), then converts it to
+ * out.  y_perm is not written.  Ignored where it does not apply.  For
+ * comparing the two (the MoE sparse-activation article, wmrh.cn, section
+ * 4.3, on the dispatcher's memory traffic). */
+#define MOE_FLAG_FUSED_COMBINE (1u << 11)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the

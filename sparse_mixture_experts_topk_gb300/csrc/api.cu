@@ -24,7 +24,8 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
                           void* h_perm, void* y_perm, int* err, cudaStream_t st);
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
-                               void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st);
+                               void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
+                               const CombineInto* comb);
 
 // SM-pair tiles move a third less data per SM for the same MMA work.  The
 // single-SM kernel pads each expert's rows to 128; the pair kernel runs its
@@ -105,9 +106,20 @@ int ffn_kernel(const Shape& s, int64_t max_rows) {
   return MOE_FFN_SIMT;
 }
 
+// The combine runs in the second product's epilogue when asked for, with
+// at most two slots per token (two fp32 additions onto zero give the same
+// sum in either order, so the result does not depend on which tile comes
+// first) and on the SM-pair kernels.
+bool combine_fusable(const Shape& s, int64_t max_rows) {
+  if (!(s.flags & MOE_FLAG_FUSED_COMBINE) || s.K > 2 || s.T == 0) return false;
+  const int k = ffn_kernel(s, max_rows);
+  return k == MOE_FFN_TC_FUSED || k == MOE_FFN_TC_PAIRS;
+}
+
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
-                       void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
+                       void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
+                       const CombineInto* comb) {
   if (s.T == 0 || max_rows == 0) return cudaSuccess;
   if (stream_ffn_eligible(s))
     return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
@@ -115,7 +127,7 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
   // unsupported shape or a missing tensor-map entry point is an error)
   if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
     if (use_pair_gemm(s, max_rows))
-      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
+      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st, comb);
     return launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
   }
   return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
@@ -134,7 +146,7 @@ namespace {
 
 struct Layout {
   size_t err, sched, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
-  size_t pend, choice, alts, scores, fin, count_chunks, psum_chunks;
+  size_t pend, choice, alts, scores, fin, count_chunks, psum_chunks, acc;
   size_t x_perm, h_perm, x_stage, out_stage, total;
   int64_t rows;
 };
@@ -200,6 +212,8 @@ Layout layout_of(const moe_desc& d) {
   }
   L.x_perm = take((size_t)L.rows * s.H * es);   // also holds y_perm in the layer call
   L.h_perm = take((size_t)L.rows * s.F * es);
+  L.acc = 0;
+  if (d.flags & MOE_FLAG_FUSED_COMBINE) L.acc = take((size_t)s.T * s.H * 4);   // fp32 combine target
   L.count_chunks = take(2 * E * 4);   // per-piece counts and sums of the chunked host-I/O path
   L.psum_chunks = take(2 * E * 4);
   L.x_stage = L.out_stage = 0;
@@ -383,6 +397,7 @@ int moe_layer_launches(const moe_desc* desc) {
   int n = 0;
   if (s.T > 0) n += 1;                                  // router
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
+  if (s.T > 0 && combine_fusable(s, rows_for(*desc))) n += 1;   // zeroing the fp32 combine target
   if (layer_reroutes(s)) {
     if (!dispatch_small(s)) n -= 1;                     // the first dispatch gathers nothing
     n += 2 + dispatch_launches(final_shape(s), false);  // the move (2), then the dispatch of the moved routing
@@ -476,15 +491,20 @@ cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, c
       e = launch_dispatch(final_shape(s), fin, xd, at<void>(ws, L.x_perm), o, err, st);
     }
   }
+  const bool fuse = combine_fusable(s, rows);
+  float* acc = fuse ? at<float>(ws, L.acc) : nullptr;
+  if (e == cudaSuccess && fuse) e = launch_zero_acc(s, acc, st);
   if (marks) prof_mark(kMarkDispatch, st);
   void* x_perm = at<void>(ws, L.x_perm);
   void* h_perm = at<void>(ws, L.h_perm);
   void* y_perm = x_perm;   // x_perm is dead once the first product has run
+  const CombineInto ci{at<int32_t>(ws, L.src), w, acc};
   if (e == cudaSuccess)
     e = launch_ffn(s, rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
-                   at<int32_t>(ws, L.sched), st);
+                   at<int32_t>(ws, L.sched), st, fuse ? &ci : nullptr);
   if (marks) prof_mark(kMarkSecond, st);
-  if (e == cudaSuccess) e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
+  if (e == cudaSuccess)
+    e = fuse ? launch_acc_to_out(s, acc, outd, st) : launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
   if (marks) prof_mark(kMarkCombine, st);
   return e;
 }

@@ -71,7 +71,38 @@ __global__ void merge_stats_kernel(const int32_t* __restrict__ count_parts, cons
   }
 }
 
+__global__ void __launch_bounds__(256) zero_acc_kernel(float4* __restrict__ acc, int64_t n4) {
+  pdl_enter();
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+    __stcg(acc + i, z);
+}
+
+// out = bf16(acc), 8 elements per thread step
+__global__ void __launch_bounds__(256) acc_to_out_kernel(const float4* __restrict__ acc, uint4* __restrict__ out,
+                                                         int64_t n8) {
+  pdl_enter();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = __ldcs(acc + 2 * i), b = __ldcs(acc + 2 * i + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    __stcs(out + i, Vec<bf16>::pack(v));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_zero_acc(const Shape& s, float* acc, cudaStream_t st) {
+  const int64_t n4 = s.T * (int64_t)s.H / 4;
+  const int64_t grid = (int64_t)sm_count() * 8;
+  return launch_kernel(zero_acc_kernel, dim3((unsigned)grid), dim3(256), 0, st, 1, (float4*)acc, n4);
+}
+
+cudaError_t launch_acc_to_out(const Shape& s, const float* acc, void* out, cudaStream_t st) {
+  const int64_t n8 = s.T * (int64_t)s.H / 8;
+  const int64_t grid = (int64_t)sm_count() * 8;
+  return launch_kernel(acc_to_out_kernel, dim3((unsigned)grid), dim3(256), 0, st, 1, (const float4*)acc, (uint4*)out,
+                       n8);
+}
 
 cudaError_t launch_merge_stats(const Shape& s, const int32_t* count_parts, const float* psum_parts, int n,
                                int32_t* count, float* psum, int32_t* count_copy, float* aux, int32_t* dropped,

@@ -82,12 +82,29 @@ static_assert(kTQ > kStages + 3, "tile queue shorter than the pipeline");
 constexpr int kTqAbort = -2;
 
 // One product of a launch: output columns N, reduction length K, the
-// nullable per-expert bias and the output rows C [rows, N].
+// nullable per-expert bias and the output rows C [rows, N].  With acc set
+// (the second product only) the rows are not stored: row r, the slot
+// s = src[r] of token t = s / topk, adds wts[s] * bf16(y) to acc[t, :] (fp32,
+// zeroed beforehand) -- the weighted combine done in the epilogue.
 struct PairProduct {
   int N, K;
   const float* bias;
   bf16* C;
+  const int32_t* src;
+  const float* wts;
+  float* acc;
+  int topk;
 };
+
+// acc[0..7] += w * v[0..7] with two 16-byte vector reductions (addr 32-byte aligned)
+__device__ __forceinline__ void red_add8(float* addr, float w, const float* v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(w * v[0]), "f"(w * v[1]),
+               "f"(w * v[2]), "f"(w * v[3])
+               : "memory");
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr + 4), "f"(w * v[4]), "f"(w * v[5]),
+               "f"(w * v[6]), "f"(w * v[7])
+               : "memory");
+}
 
 // Wait (bounded) until the counter reaches `need`, with acquire semantics at
 // GPU scope; then order those observed writes before this thread's later
@@ -145,15 +162,28 @@ __device__ __forceinline__ void tile_epilogue(uint32_t tbase, bool swap, int e, 
       for (int i = 0; i < 4; ++i) {
         const int jj = (lane >> 2) + 8 * i;
         const int row = row_base + c * 32 + jj;
-        if (row < row_end && fv < N)
-          *reinterpret_cast<uint4*>(C + (int64_t)row * N + fv) =
-              *reinterpret_cast<const uint4*>(xb + jj * 32 + 8 * (lane & 3));
+        if (row < row_end && fv < N) {
+          const uint4 u = *reinterpret_cast<const uint4*>(xb + jj * 32 + 8 * (lane & 3));
+          if (kEpi == kEpiPlain && P.acc) {
+            const int sl = P.src[row];
+            float v[8];
+            Vec<bf16>::unpack(u, v);
+            red_add8(P.acc + (int64_t)(sl / P.topk) * N + fv, P.wts[sl], v);
+          } else {
+            *reinterpret_cast<uint4*>(C + (int64_t)row * N + fv) = u;
+          }
+        }
       }
       __syncwarp();
     }
   } else {
     const int row = row_base + (int)rank * kBM + q * 32 + lane;
     const bool row_ok = row < row_end;
+    // fused combine: this row's token and routing weight
+    const bool comb = kEpi == kEpiPlain && P.acc != nullptr;
+    const int sl = (comb && row_ok) ? P.src[row] : 0;
+    const float wt = (comb && row_ok) ? P.wts[sl] : 0.f;
+    float* acc_row = comb ? P.acc + (int64_t)(sl / P.topk) * N : nullptr;
 #pragma unroll 1
     for (int c = 0; c < kOut / 32; ++c) {
       const int col0 = n0 + c * 32;
@@ -163,7 +193,7 @@ __device__ __forceinline__ void tile_epilogue(uint32_t tbase, bool swap, int e, 
       if (kSwi) tc::tmem_ld_32x32b_x32(tbase + kOut + c * 32, u);
       tc::tmem_wait_ld();
       if (row_ok) {
-        bf16* dst = C + (int64_t)row * N + col0;
+        bf16* dst = comb ? nullptr : C + (int64_t)row * N + col0;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           if (col0 + g * 8 < N) {
@@ -182,7 +212,14 @@ __device__ __forceinline__ void tile_epilogue(uint32_t tbase, bool swap, int e, 
                 v[j] = a;
               }
             }
-            *reinterpret_cast<uint4*>(dst + g * 8) = Vec<bf16>::pack(v);
+            const uint4 pk = Vec<bf16>::pack(v);
+            if (comb) {
+              float y[8];
+              Vec<bf16>::unpack(pk, y);                  // y rounded to bf16, as stored
+              red_add8(acc_row + col0 + g * 8, wt, y);
+            } else {
+              *reinterpret_cast<uint4*>(dst + g * 8) = pk;
+            }
           }
         }
       }
@@ -583,7 +620,8 @@ cudaError_t launch_pair(const CUtensorMap (&m)[6], const int32_t* offs, int E, c
 // counters (rows / 256 + E + 1 of them), all zero on entry.
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
-                               void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st) {
+                               void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
+                               const CombineInto* comb) {
   if (!sched) return cudaErrorInvalidValue;
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
@@ -595,8 +633,9 @@ cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_p
   if (!pair_maps(&m1[0], &m1[1], &m1[2], x_perm, max_rows, W1, (int64_t)s.E * s.F * (swi ? 2 : 1), s.H) ||
       !pair_maps(&m2[0], &m2[1], &m2[2], h_perm, max_rows, W2, (int64_t)s.E * s.H, s.F))
     return cudaErrorNotSupported;
-  const PairProduct P1{s.F, s.H, b1, (bf16*)h_perm};
-  const PairProduct P2{s.H, s.F, b2, (bf16*)y_perm};
+  const PairProduct P1{s.F, s.H, b1, (bf16*)h_perm, nullptr, nullptr, nullptr, s.K};
+  const PairProduct P2{s.H, s.F, b2, (bf16*)y_perm, comb ? comb->src : nullptr, comb ? comb->w : nullptr,
+                       comb ? comb->acc : nullptr, s.K};
   if (!(s.flags & MOE_FLAG_FFN_SPLIT)) {
     // both products in one launch: the second's tiles start on row blocks the first has finished
     const CUtensorMap m[6] = {m1[0], m1[1], m1[2], m2[0], m2[1], m2[2]};

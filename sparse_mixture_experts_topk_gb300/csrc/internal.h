@@ -129,16 +129,29 @@ inline int64_t sched_words(int64_t rows, int E) { return 2 + rows / 256 + E + 1;
 // sched[2 .. 2 + E)).
 bool stream_ffn_eligible(const Shape& s);
 bool stream_fused(const Shape& s);
+// The weighted combine folded into the second product's epilogue (K <= 2,
+// SM-pair kernels): row r adds w[src[r]] * y to acc[src[r] / K] (fp32,
+// zeroed beforehand) instead of storing y.
+struct CombineInto {
+  const int32_t* src;
+  const float* w;
+  float* acc;
+};
+bool combine_fusable(const Shape& s, int64_t max_rows);
 // sched: sched_words(max_rows, E) zeroed ints (the SM-pair kernel's counters)
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
-                       void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st);
+                       void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
+                       const CombineInto* comb = nullptr);
 
 // ---------------------------------------------------------------- combine / aux
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* pos, const float* w,
                            void* out, cudaStream_t st);
 cudaError_t launch_aux(const Shape& s, const float* psum, const int32_t* count, float* loss,
                        cudaStream_t st);
+// acc [T, H] fp32 = 0, and out [T, H] = bf16(acc) (the fused combine's two ends)
+cudaError_t launch_zero_acc(const Shape& s, float* acc, cudaStream_t st);
+cudaError_t launch_acc_to_out(const Shape& s, const float* acc, void* out, cudaStream_t st);
 // The statistics of a layer run in pieces of tokens: count[e] and psum[e]
 // summed over the n pieces in order, then the loss of the whole batch (s.T
 // tokens); count_copy, aux and dropped (0: no capacity) are nullable.

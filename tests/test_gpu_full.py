@@ -153,3 +153,31 @@ def test_full_size(name):
         assert not over.any(), (name, kind, mx, int(over.sum()))
         if kind == "exact" and np.abs(ref).max() < 4.0:
             assert mx <= OUT_MAXABS_BF16, (name, kind, mx)
+
+
+def test_full_size_fused_combine():
+    """The prefill layer with the combine folded into the second product's
+    epilogue: every output element against the exact and the rounded oracle
+    (as above), and within one bf16 ulp of the plain layer's."""
+    w = W.WORKLOADS["prefill"]
+    inp = W.generate(w)
+    dev = Dev(inp)
+    plain = run_layer(dev)
+    fused = run_layer(dev, flags=moe.MOE_FLAG_FUSED_COMBINE)
+    assert plain["device_error"] == 0 and fused["device_error"] == 0
+    out, b = as_f64(fused["out"]), as_f64(plain["out"])
+    # one bf16 ulp, or the fp32 rounding of the two products (terms below 4) where they cancel
+    assert (np.abs(out - b) <= np.abs(b) * 2.0 ** -7 + 1e-6).all()
+    assert (out != b).mean() < 0.01
+    r = run_stages(dev)
+    gl = to_np(r["logits"]).astype(np.float64)
+    ids_o, w_o, _ = O.route(gl, w.K)
+    d = O.dispatch(ids_o, w.E, w.capacity)
+    W1 = _PerExpert(inp.W1, w.dtype)
+    W2 = _PerExpert(inp.W2, w.dtype)
+    x64 = O.widen(inp.x, w.dtype)
+    for kind in ("exact", "rounded"):
+        ref = O.combine(O.expert_outputs(x64, d, W1, W2, bf16=(kind == "rounded"), E=w.E, ids=ids_o), d["pos"], w_o)
+        mx, rel = out_errors(out, ref)
+        assert rel <= OUT_REL_L2_BF16, (kind, rel)
+        assert not (np.abs(out - ref) > OUT_MAXABS_BF16 + np.abs(ref) * 2.0 ** -7).any(), (kind, mx)

@@ -232,6 +232,36 @@ def test_host_io_layer_matches_device_layer():
     assert torch.equal(outh.view(torch.int16), ref["out"].cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["ragged_bf16", "hot2_cap", "swiglu_ragged", "e64_k8", "cap_zipf_k4", "h_ragged"])
+def test_fused_combine_matches_oracle(name):
+    """MOE_FLAG_FUSED_COMBINE: the weighted combine in the second product's
+    epilogue (fp32 vector reductions onto a zeroed copy of out), for K <= 2 on
+    the SM-pair kernels; other layers ignore the flag.  Against the oracle
+    like the plain layer, and within one bf16 ulp of it (the two add the same
+    rounded products in fp32, one with a fused multiply-add)."""
+    w = SMALL[name]
+    inp = W.generate(w)
+    dev = Dev(inp)
+    plain = run_layer(dev, flags=moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_NO_DECODE)
+    fused = run_layer(dev, flags=moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_NO_DECODE | moe.MOE_FLAG_FUSED_COMBINE)
+    assert plain["device_error"] == 0 and fused["device_error"] == 0
+    a, b = as_f64(fused["out"]), as_f64(plain["out"])
+    # one bf16 ulp, or the fp32 rounding of the two products where they cancel
+    assert (np.abs(a - b) <= np.abs(b) * 2.0 ** -7 + 1e-6).all()
+    if w.K > 2:
+        np.testing.assert_array_equal(to_np(fused["out"]), to_np(plain["out"]))   # not fused: same path
+    np.testing.assert_array_equal(to_np(fused["count"]), to_np(plain["count"]))
+    r = run_stages(dev, flags=moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_NO_DECODE)
+    gl = to_np(r["logits"]).astype(np.float64)
+    ref = O.layer_forward(O.widen(inp.x, w.dtype), O.widen(inp.Wg, w.dtype), O.widen(inp.W1, w.dtype),
+                          O.widen(inp.W2, w.dtype), w.K, capacity=w.capacity, gate_bias=inp.gate_bias,
+                          b1=None if inp.b1 is None else inp.b1.astype(np.float64),
+                          b2=None if inp.b2 is None else inp.b2.astype(np.float64),
+                          bf16=True, logits=gl, act=w.act)
+    mx, rel = out_errors(a, ref["out"])
+    assert mx <= OUT_MAXABS_BF16 and rel <= OUT_REL_L2_BF16, (mx, rel)
+
+
 @pytest.mark.parametrize("T", [2048, 2501])
 def test_chunked_host_io_layer_matches_device_layer(T):
     """With host buffers and no capacity the call runs the batch in two
