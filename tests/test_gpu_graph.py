@@ -23,7 +23,12 @@ CASES = {
     # SwiGLU experts with capacity drops
     "swiglu_cap": W.small("swiglu_cap", T=300, H=256, E=8, K=2, F=384, act="swiglu",
                           capacity=W.capacity_ceil(300, 8, 2) // 2, gate_bias="zipf"),
+    # drop_tokens=False: capacity-limited dispatch, the move, the dispatch of the moved routing
+    "reroute": W.small("reroute", T=700, H=256, E=8, K=2, F=384, gate_bias="hot",
+                       capacity=W.capacity_ceil(700, 8, 2), reroute=True),
 }
+# the combine folded into the second product's epilogue (flags on top of the case)
+FLAGGED = {"fused_combine": ("ragged_bf16", moe.MOE_FLAG_FUSED_COMBINE)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,16 +41,17 @@ def _built():
     moe.lib()
 
 
-@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("name", list(CASES) + list(FLAGGED))
 def test_captured_layer_replays_bit_exactly(name):
     import torch
-    w = CASES[name]
+    case, flags = FLAGGED.get(name, (name, 0))
+    w = CASES[case]
     inp = W.generate(w)
     dev = Dev(inp)
-    eager = run_layer(dev)
+    eager = run_layer(dev, flags=flags)
     assert eager["device_error"] == 0
 
-    d = desc_of(w, 0)
+    d = desc_of(w, flags)
     ws = moe.workspace(d)
     out = torch.empty((w.T, w.H), dtype=tdtype(w), device="cuda")
     aux = torch.empty((1,), dtype=torch.float32, device="cuda")
@@ -82,5 +88,5 @@ def test_captured_layer_replays_bit_exactly(name):
     dev.x.copy_(dev2.x)
     g.replay()
     torch.cuda.synchronize()
-    eager2 = run_layer(dev)
+    eager2 = run_layer(dev, flags=flags)
     np.testing.assert_array_equal(to_np(out), to_np(eager2["out"]))
