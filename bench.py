@@ -84,7 +84,8 @@ def config_of(w: W.Workload, world: int, rows: int, used: int, gemm: str):
 
 
 def gemm_desc(args) -> str:
-    return args.gemm + ("+fused-combine" if getattr(args, "fused_combine", False) else "")
+    return args.gemm + ("+fused-combine" if getattr(args, "fused_combine", False) else "") + \
+        ("+decode-split" if getattr(args, "decode_split", False) else "")
 
 
 def describe(w: W.Workload) -> str:
@@ -106,6 +107,8 @@ def work_counts(w: W.Workload, rows: int, used_experts: int):
         "combine": rows * w.H * es + w.T * w.H * es + S * 8,               # y_perm, out; pos + w
         "ffn_first_bytes": used_experts * up * w.F * w.H * es + rows * (w.H + w.F) * es,
         "ffn_second_bytes": used_experts * w.F * w.H * es + rows * (w.H + w.F) * es,
+        # the whole layer in one launch: x and Wg in, the used experts' weights, out
+        "layer_bytes": 2 * w.T * w.H * es + w.E * w.H * es + used_experts * (up + 1) * w.F * w.H * es,
     }
 
 
@@ -163,7 +166,9 @@ class Clocks:
 
 
 GEMM_SOURCES = ("ffn_tc.cu", "ffn_tc2.cu", "tc_ptx.cuh", "common.cuh")
-STREAM_SOURCES = ("ffn_stream.cu", "bf16_dot.cuh", "tc_ptx.cuh", "common.cuh")
+STREAM_SOURCES = ("ffn_stream.cu", "stream_body.cuh", "bf16_dot.cuh", "tc_ptx.cuh", "common.cuh")
+DECODE_SOURCES = ("decode_layer.cu", "stream_body.cuh", "router_body.cuh", "combine.cuh", "bf16_dot.cuh",
+                  "tc_ptx.cuh", "common.cuh")
 
 
 def source_hash(files=GEMM_SOURCES) -> str:
@@ -293,12 +298,14 @@ def run_ours(args, w: W.Workload):
     gb = to_dev(inp.gate_bias, torch)
     dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
     flags = (moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0) | (moe.MOE_FLAG_REROUTE if w.reroute else 0) | \
-        (moe.MOE_FLAG_FUSED_COMBINE if args.fused_combine else 0) | GEMM_FLAGS[args.gemm]
+        (moe.MOE_FLAG_FUSED_COMBINE if args.fused_combine else 0) | \
+        (moe.MOE_FLAG_DECODE_SPLIT if args.decode_split else 0) | GEMM_FLAGS[args.gemm]
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                       moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
     launches_per_step = moe.moe_layer_launches(d)
     ffn_kind = moe.moe_ffn_kernel(d)
     fused = ffn_kind in (moe.MOE_FFN_TC_FUSED, moe.MOE_FFN_STREAM)   # both products in one launch
+    one_launch = moe.moe_layer_decode_fused(d)                        # the whole decode layer in one launch
     ws = moe.workspace(d)
     out = torch.empty((w.T, w.H), dtype=dt, device="cuda")
     aux = torch.empty(1, device="cuda")
@@ -384,7 +391,11 @@ def run_ours(args, w: W.Workload):
     flops = {"ffn_first": work["ffn_flops_first"], "ffn_second": work["ffn_flops_second"],
              "ffn": work["ffn_flops_first"] + work["ffn_flops_second"]}
     work["ffn_bytes"] = work["ffn_first_bytes"] + work["ffn_second_bytes"]
-    if fused:
+    if one_launch:
+        # one launch runs the whole layer (after a one-block counter reset):
+        # its time is the headline's, events around each whole call
+        dom, dom_ms = "layer", total_ms / args.steps
+    elif fused:
         # one launch runs both products: its time is the whole span between the
         # dispatch and the combine marks (the second mark follows it directly)
         dom, dom_ms = "ffn", f1 + f2
@@ -392,7 +403,14 @@ def run_ours(args, w: W.Workload):
         dom, dom_ms = ("ffn_first", f1) if f1 >= f2 else ("ffn_second", f2)
     # decode-sized batches run the weight-streaming kernel: bound by HBM
     streaming = ffn_kind in (moe.MOE_FFN_STREAM, moe.MOE_FFN_STREAM_SPLIT)
-    if streaming:
+    if one_launch:
+        achieved = work["layer_bytes"] / (dom_ms / 1e3) / 1e9
+        roof = {"kernel": "one-launch decode layer (gate scores, routing, both expert products, combine; "
+                          "timed with its counter reset)", "bound": "hbm", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_source": f"{src} HBM copy",
+                "traffic": (ncu_traffic(w.name, DECODE_SOURCES) or {}).get(dom),
+                "algorithmic_bytes_per_launch": work["layer_bytes"]}
+    elif streaming:
         achieved = work[dom + "_bytes"] / (dom_ms / 1e3) / 1e9
         roof = {"kernel": "weight-streaming expert kernel (both products, one launch)" if fused
                 else f"weight-streaming expert kernel ({dom})", "bound": "hbm", "achieved": achieved,
@@ -413,6 +431,9 @@ def run_ours(args, w: W.Workload):
     stage_names = ["router", "dispatch", "ffn", "combine"] if fused else STAGES
     if fused:
         stage_ms = dict(stage_ms, ffn=f1 + f2)
+    if one_launch:
+        stage_names = []
+        stages["layer"] = {"ms": dom_ms, "gbs": achieved, "frac_hbm": achieved / hbm}
     for name in stage_names:
         ms = stage_ms[name]
         if name.startswith("ffn"):
@@ -507,6 +528,8 @@ def main():
                     help="expert GEMM kernel for bf16 prefill: the library's choice, or one forced")
     ap.add_argument("--fused-combine", action="store_true",
                     help="fold the weighted combine into the second expert product's epilogue")
+    ap.add_argument("--decode-split", action="store_true",
+                    help="decode-sized batches: the layer's separate steps instead of the one-launch layer")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":

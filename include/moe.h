@@ -101,6 +101,15 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * comparing the two (the MoE sparse-activation article, wmrh.cn, section
  * 4.3, on the dispatcher's memory traffic). */
 #define MOE_FLAG_FUSED_COMBINE (1u << 11)
+/* bf16 batches of at most 16 tokens: moe_layer_forward runs the layer as
+ * its separate steps (router, dispatch, weight-streaming expert products,
+ * combine: four launches) instead of the default one-launch decode layer,
+ * in which one grid with every CTA resident computes the gate scores,
+ * routes and places every token in each CTA, spreads the used experts'
+ * weight rows evenly over the CTAs and combines, with counters in the
+ * workspace between the steps.  Same results, bit for bit; for comparing
+ * the two (testing). */
+#define MOE_FLAG_DECODE_SPLIT  (1u << 12)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the
@@ -328,6 +337,15 @@ int moe_layer_launches(const moe_desc* desc);
 #define MOE_FFN_TC_FUSED  4 /* tensor cores on SM pairs, both products in 1 launch */
 #define MOE_FFN_STREAM_SPLIT 5 /* weight streaming, one launch per product: 2 launches */
 int moe_ffn_kernel(const moe_desc* desc);
+
+/*
+ * Whether moe_layer_forward runs this description as the one-launch decode
+ * layer (see MOE_FLAG_DECODE_SPLIT): 1 if it does (two launches: its
+ * counters zeroed, then the layer), 0 if it runs the separate steps, or a
+ * negative MOE_ERR_* for an invalid desc.  No counterpart on the pages; it
+ * lets a benchmark attribute the time.  Depends on the shape and flags only.
+ */
+int moe_layer_decode_fused(const moe_desc* desc);
 
 /*
  * Stage timing for moe_layer_forward on the calling host thread (no

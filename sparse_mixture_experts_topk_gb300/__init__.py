@@ -18,11 +18,11 @@ import os
 __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU",
-    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "MOE_FLAG_REROUTE", "MOE_FLAG_FUSED_COMBINE", "lib",
+    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "MOE_FLAG_REROUTE", "MOE_FLAG_FUSED_COMBINE", "MOE_FLAG_DECODE_SPLIT", "lib",
     "library_path", "make_desc", "moe_reroute",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
-    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "moe_ffn_kernel",
+    "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "moe_ffn_kernel", "moe_layer_decode_fused",
     "MOE_FFN_STREAM", "MOE_FFN_SIMT", "MOE_FFN_TC_SINGLE", "MOE_FFN_TC_PAIRS", "MOE_FFN_TC_FUSED",
     "MOE_FFN_STREAM_SPLIT", "workspace",
 ]
@@ -40,6 +40,7 @@ MOE_FLAG_GEMM_ROWS = 1 << 8
 MOE_FLAG_FFN_SPLIT = 1 << 9
 MOE_FLAG_REROUTE = 1 << 10
 MOE_FLAG_FUSED_COMBINE = 1 << 11
+MOE_FLAG_DECODE_SPLIT = 1 << 12
 # moe_ffn_kernel results
 MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED, MOE_FFN_STREAM_SPLIT = 0, 1, 2, 3, 4, 5
 
@@ -79,6 +80,7 @@ _SIGS = {
     "moe_profile_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     "moe_layer_launches": (ctypes.c_int, [ctypes.POINTER(MoeDesc)]),
     "moe_ffn_kernel": (ctypes.c_int, [ctypes.POINTER(MoeDesc)]),
+    "moe_layer_decode_fused": (ctypes.c_int, [ctypes.POINTER(MoeDesc)]),
 }
 
 _lib = None
@@ -219,6 +221,14 @@ def moe_ffn_kernel(desc: MoeDesc) -> int:
     if k < 0:
         _check("moe_ffn_kernel", k)
     return k
+
+
+def moe_layer_decode_fused(desc: MoeDesc) -> bool:
+    """Whether ``moe_layer_forward`` runs ``desc`` as the one-launch decode layer."""
+    k = int(lib().moe_layer_decode_fused(ctypes.byref(desc)))
+    if k < 0:
+        _check("moe_layer_decode_fused", k)
+    return k == 1
 
 
 def moe_get_device_error(ws, stream=None) -> int:

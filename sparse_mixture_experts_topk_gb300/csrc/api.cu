@@ -146,7 +146,7 @@ namespace {
 
 struct Layout {
   size_t err, sched, ids, w, psum_part, psum, blk_hist, blk_base, count, offs, dropped, aux, src, pos;
-  size_t pend, choice, alts, scores, fin, count_chunks, psum_chunks, acc;
+  size_t pend, choice, alts, scores, fin, count_chunks, psum_chunks, acc, dec_part, dec_ctr;
   size_t x_perm, h_perm, x_stage, out_stage, total;
   int64_t rows;
 };
@@ -214,6 +214,11 @@ Layout layout_of(const moe_desc& d) {
   L.h_perm = take((size_t)L.rows * s.F * es);
   L.acc = 0;
   if (d.flags & MOE_FLAG_FUSED_COMBINE) L.acc = take((size_t)s.T * s.H * 4);   // fp32 combine target
+  L.dec_part = L.dec_ctr = 0;
+  if (s.T >= 1 && s.T <= 16) {           // the one-launch decode layer's score pieces and counters
+    L.dec_part = take(decode_part_floats(s) * 4);
+    L.dec_ctr = take((size_t)decode_ctr_words(s) * 4);
+  }
   L.count_chunks = take(2 * E * 4);   // per-piece counts and sums of the chunked host-I/O path
   L.psum_chunks = take(2 * E * 4);
   L.x_stage = L.out_stage = 0;
@@ -394,6 +399,7 @@ int moe_layer_launches(const moe_desc* desc) {
   int rc = check_desc(desc);
   if (rc) return rc;
   const Shape s = shape_of(*desc);
+  if (s.T > 0 && decode_layer_eligible(s)) return 2;   // counters zeroed, the one-launch layer
   int n = 0;
   if (s.T > 0) n += 1;                                  // router
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
@@ -416,6 +422,13 @@ int moe_layer_launches(const moe_desc* desc) {
     n += (k == MOE_FFN_TC_FUSED || k == MOE_FFN_STREAM ? 1 : 2) + 1;
   }
   return n;
+}
+
+int moe_layer_decode_fused(const moe_desc* desc) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  const Shape s = shape_of(*desc);
+  return s.T > 0 && decode_layer_eligible(s) ? 1 : 0;
 }
 
 int moe_ffn_kernel(const moe_desc* desc) {
@@ -441,6 +454,32 @@ cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, c
                       const float* gate_bias, const void* W1, const float* b1, const void* W2, const float* b2,
                       void* outd, const LayerStats& ls, bool marks, cudaStream_t st) {
   int* err = at<int>(ws, L.err);
+  if (decode_layer_eligible(s)) {
+    DecodeIO io;
+    io.x = xd;
+    io.Wg = Wg;
+    io.gate_bias = gate_bias;
+    io.W1 = W1;
+    io.b1 = b1;
+    io.W2 = W2;
+    io.b2 = b2;
+    io.out = outd;
+    io.part = at<float>(ws, L.dec_part);
+    io.ctr = at<int>(ws, L.dec_ctr);
+    io.h = at<void>(ws, L.h_perm);
+    io.y = at<void>(ws, L.x_perm);
+    io.count = ls.count;
+    io.count_copy = ls.count_copy;
+    io.dropped = at<int32_t>(ws, L.dropped);
+    io.dropped_copy = ls.dropped_copy;
+    io.psum = ls.psum;
+    io.aux = ls.aux;
+    io.err = err;
+    const cudaError_t e = launch_decode_layer(s, io, st);
+    if (marks)   // one launch: every stage ends with it
+      for (int m = kMarkRouter; m <= kMarkCombine; ++m) prof_mark(m, st);
+    return e;
+  }
   cudaError_t e = cudaSuccess;
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* w = at<float>(ws, L.w);

@@ -29,81 +29,27 @@
 #include <algorithm>
 #include <type_traits>
 
-#include "bf16_dot.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "stream_body.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 
 namespace {
 
+using stream::kConsumers;
+using stream::kWaitNs;
+using stream::stage_row;
+using stream::stage_row_of_warp;
+using stream::wait_count;
+
 constexpr int kMaxRows = 16;
-constexpr int kConsumers = 8;                    // consumer warps; a stage holds <= 8 rows
 constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
 constexpr int kMaxStages = 6;
 constexpr size_t kSmemBudget = 220 * 1024;
-constexpr uint64_t kWaitNs = 2000000000ull;
 
 __host__ __device__ inline size_t act_bytes(int mcap, int K, int esize) { return ((size_t)mcap * K * esize + 127) / 128 * 128; }
-
-// One weight row (SwiGLU: gate row w and up row u) against the m <= MR
-// staged activation rows: lane l takes vectors l, l + 32, ...; fp32 sums,
-// reduced across the warp; lane 0 adds the bias, applies the activation and
-// writes out[r * N] for r < m.  bf16 rows are multiplied without widening
-// (fma8_bf16); fp32 rows element by element.
-template <typename T, int kEpi, int MR>
-__device__ __forceinline__ void dot_rows(const uint4* w, const uint4* u, const uint4* act, int kv, int m,
-                                         const float* be, int n, int N, T* out) {
-  constexpr bool kSwi = kEpi == kEpiSwiglu;
-  constexpr int V = Vec<T>::N;
-  const int lane = threadIdx.x & 31;
-  float acc[MR], accu[MR];
-#pragma unroll
-  for (int r = 0; r < MR; ++r) acc[r] = accu[r] = 0.f;
-#pragma unroll 2
-  for (int v = lane; v < kv; v += 32) {
-    const uint4 wq = w[v];
-    const uint4 uq = kSwi ? u[v] : wq;
-#pragma unroll
-    for (int r = 0; r < MR; ++r) {
-      if (r < m) {
-        const uint4 xq = act[r * kv + v];
-        if constexpr (std::is_same<T, bf16>::value) {
-          acc[r] = fma8_bf16(xq, wq, acc[r]);
-          if (kSwi) accu[r] = fma8_bf16(xq, uq, accu[r]);
-        } else {
-          float x[V], b[V], bu[V];
-          Vec<T>::unpack(xq, x);
-          Vec<T>::unpack(wq, b);
-          if (kSwi) Vec<T>::unpack(uq, bu);
-#pragma unroll
-          for (int i = 0; i < V; ++i) {
-            acc[r] = fmaf(x[i], b[i], acc[r]);
-            if (kSwi) accu[r] = fmaf(x[i], bu[i], accu[r]);
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < MR; ++r) {
-    if (r < m) {
-      float sg = acc[r], su = accu[r];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sg += __shfl_xor_sync(0xffffffffu, sg, o);
-        if (kSwi) su += __shfl_xor_sync(0xffffffffu, su, o);
-      }
-      if (lane == 0) {
-        float v = sg + (be ? be[n] : 0.f);
-        if (kEpi == kEpiGelu) v = gelu_erf(v);
-        if (kSwi) v = silu_f(v) * (su + (be ? be[N + n] : 0.f));
-        out[(int64_t)r * N] = from_f32<T>(v);
-      }
-    }
-  }
-}
 
 // One product of a launch: activation rows A [rows, K], weights B
 // [E, N, K] (SwiGLU: [E, 2N, K]), nullable bias, output rows C [rows, N],
@@ -130,50 +76,6 @@ __device__ __forceinline__ StreamRange stream_range(int N, int rps, int nblk, in
   r.n_end = min(N, r.n_begin + per);
   r.groups = r.n_begin < r.n_end ? (r.n_end - r.n_begin + rps - 1) / rps : 0;
   return r;
-}
-
-// Dot weight row j of a staged ring stage with the staged activation rows
-// (a body sized for the segment, so the hot loop stays small; kMR bounds the
-// segment, and with it the registers the bodies take).
-template <typename T, int kEpi, int kMR>
-__device__ __forceinline__ void stage_row(const uint8_t* st, int j, int rps, uint32_t row_bytes, const uint4* act,
-                                          int kv, int m, const float* be, int n, int N, T* out) {
-  const uint4* wv = reinterpret_cast<const uint4*>(st + (size_t)j * row_bytes);
-  const uint4* uv = reinterpret_cast<const uint4*>(st + (size_t)(rps + j) * row_bytes);
-  if (m <= 1) dot_rows<T, kEpi, 1>(wv, uv, act, kv, m, be, n, N, out);
-  else if (kMR <= 2 || m <= 2) dot_rows<T, kEpi, 2>(wv, uv, act, kv, m, be, n, N, out);
-  else if (kMR <= 4 || m <= 4) dot_rows<T, kEpi, (kMR < 4 ? kMR : 4)>(wv, uv, act, kv, m, be, n, N, out);
-  else if (kMR <= 8 || m <= 8) dot_rows<T, kEpi, (kMR < 8 ? kMR : 8)>(wv, uv, act, kv, m, be, n, N, out);
-  else dot_rows<T, kEpi, kMR>(wv, uv, act, kv, m, be, n, N, out);
-}
-
-// Row j of stage g (rps rows a stage) is the CTA's row g rps + j of the
-// product, and goes to consumer warp (g rps + j) mod kConsumers: with fewer
-// rows than warps in a stage, the idle warps work on the next stage.
-__device__ __forceinline__ int stage_row_of_warp(int g, int rps, int warp) {
-  return ((warp - g * rps) % kConsumers + kConsumers) % kConsumers;
-}
-
-// Wait (bounded) until *p reaches `need`, acquire at GPU scope, then order
-// the observed writes before this thread's later bulk copies (which read
-// global memory through the async proxy).  False on timeout or abort.
-__device__ __forceinline__ bool wait_count(const int* p, int need, const volatile int* abort) {
-  uint64_t t0 = 0;
-  for (int i = 0;; ++i) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= need) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      return true;
-    }
-    if (*abort) return false;
-    if ((i & 63) == 63) {
-      const uint64_t now = tc::globaltimer();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > kWaitNs) return false;
-    }
-    __nanosleep(64);
-  }
 }
 
 // nphase = 1: the product P0 (activation kEpi).  nphase = 2: P0, then the

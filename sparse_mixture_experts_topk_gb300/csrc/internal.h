@@ -144,6 +144,37 @@ cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, con
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
                        const CombineInto* comb = nullptr);
 
+// ---------------------------------------------------------------- one-launch decode layer
+// bf16 batches of at most 16 tokens whose rows, score table and weight ring
+// fit one CTA's shared memory, unless the flags ask for the separate steps.
+bool decode_layer_eligible(const Shape& s);
+// workspace: [pieces][T][E] fp32 partial gate scores, and the counters
+size_t decode_part_floats(const Shape& s);
+int decode_ctr_words(const Shape& s);
+struct DecodeIO {
+  const void* x;
+  const void* Wg;
+  const float* gate_bias;
+  const void* W1;
+  const float* b1;
+  const void* W2;
+  const float* b2;
+  void* out;
+  float* part;
+  int* ctr;
+  void* h;      // [kept rows, F]
+  void* y;      // [kept rows, H]
+  int32_t* count;
+  int32_t* count_copy;
+  int32_t* dropped;
+  int32_t* dropped_copy;
+  float* psum;
+  float* aux;
+  int* err;
+};
+// Two launches: the counters zeroed, then the layer.
+cudaError_t launch_decode_layer(const Shape& s, const DecodeIO& io, cudaStream_t st);
+
 // ---------------------------------------------------------------- combine / aux
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* pos, const float* w,
                            void* out, cudaStream_t st);

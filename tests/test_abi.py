@@ -77,10 +77,22 @@ def test_layer_launch_count(lib):
     assert moe.moe_layer_launches(f32) == 1 + 4 + 2 + 1
     decode = moe.make_desc(8, 3584, 32, 2, 2560)
     assert moe.moe_ffn_kernel(decode) == moe.MOE_FFN_STREAM
-    assert moe.moe_layer_launches(decode) == 1 + 1 + 1 + 1
+    assert moe.moe_layer_decode_fused(decode)
+    assert moe.moe_layer_launches(decode) == 2            # counters zeroed, the one-launch layer
+    steps = moe.make_desc(8, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_DECODE_SPLIT)
+    assert not moe.moe_layer_decode_fused(steps)
+    assert moe.moe_layer_launches(steps) == 1 + 1 + 1 + 1
     decode_split = moe.make_desc(8, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_FFN_SPLIT)
     assert moe.moe_ffn_kernel(decode_split) == moe.MOE_FFN_STREAM_SPLIT
+    assert not moe.moe_layer_decode_fused(decode_split)
     assert moe.moe_layer_launches(decode_split) == 1 + 1 + 2 + 1
+    # fp32, more than 16 tokens, drop_tokens=False with a capacity: the separate steps
+    assert not moe.moe_layer_decode_fused(moe.make_desc(8, 256, 8, 2, 256, dtype=moe.MOE_F32))
+    assert not moe.moe_layer_decode_fused(moe.make_desc(17, 3584, 32, 2, 2560))
+    assert not moe.moe_layer_decode_fused(moe.make_desc(8, 3584, 32, 2, 2560, capacity=1,
+                                                        flags=moe.MOE_FLAG_REROUTE))
+    assert moe.moe_layer_decode_fused(moe.make_desc(16, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_SWIGLU))
+    assert moe.moe_layer_decode_fused(moe.make_desc(1, 3584, 32, 2, 2560))
     assert moe.moe_layer_launches(moe.make_desc(0, 3584, 32, 2, 2560)) == 1
     with pytest.raises(moe.MoeError):
         moe.moe_layer_launches(moe.make_desc(8, 3584, 32, 9, 2560))
