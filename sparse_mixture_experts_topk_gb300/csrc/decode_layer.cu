@@ -17,17 +17,19 @@
 //   2. every CTA waits for the counter, sums the pieces and finishes every
 //      token itself (top-k, weights, probabilities) in shared memory, then
 //      places the slots: per expert in slot order, the first C kept;
-//   3. the experts' weight rows are cut into units of one ring stage (rps
-//      rows), first product then second, in expert order; CTA b takes the
-//      b-th equal share of each product's units, so every CTA streams the
-//      same bytes whatever the experts' row counts, and a share may span
-//      several experts.  A producer warp moves the weight stages through a
-//      ring of bulk copies; an activation warp moves each expert's rows (x
-//      rows for the first product, h rows for the second, the latter once
-//      the expert's first-product units are all counted) into one of two
-//      buffers; eight consumer warps dot them;
-//   4. once every CTA has counted its second-product units, the CTAs that own
-//      output items combine them.
+//   3. the used experts' weight rows, first product then second, in expert
+//      order: CTA b takes the b-th share of each product's rows, the shares
+//      cut at equal sums of a per-row cost that grows with the expert's
+//      token rows (the dots of experts with many rows are compute-bound), a
+//      share possibly spanning several experts, and streams it in ring
+//      stages of at most rps rows of one expert.  A producer warp moves the
+//      stages through a ring of bulk copies; an activation warp moves each
+//      expert's rows (x rows for the first product, h rows for the second,
+//      the latter once all F columns of the expert's first product are
+//      counted) into one of two buffers; eight consumer warps dot them, two
+//      weight rows a warp for experts of one to four rows;
+//   4. once every CTA has counted itself done with the second product, the
+//      CTAs that own output items combine them.
 // Counter waits need every CTA resident: the grid is one or two CTAs per SM
 // and the host checks that many fit.  Every wait is bounded; on expiry the
 // kernel records a timeout in the error word, skips the remaining work,
@@ -156,6 +158,28 @@ struct StageWalk {
   }
 };
 
+// Relative time per weight row of an expert with m rows, as measured on
+// the layer: the dots of one and two rows keep up with HBM, more rows make
+// a CTA's stages compute-bound.  The shares of the weight rows follow it.
+__device__ __forceinline__ int row_cost(int m) { return m <= 1 ? 8 : m == 2 ? 9 : m == 3 ? 12 : m == 4 ? 14 : 3 * m; }
+
+// The first row of the b-th of nb shares of the A experts' N-row weight
+// matrices (rows of expert a are a N .. a N + N - 1), the shares cut at
+// equal sums of row_cost over their rows.
+__device__ __forceinline__ int share_start(int b, int nb, int A, int N, const int* ue, const int* offs) {
+  int64_t total = 0;
+  for (int a = 0; a < A; ++a) total += (int64_t)N * row_cost(offs[ue[a] + 1] - offs[ue[a]]);
+  const int64_t x = total * b / nb;
+  int64_t c = 0;
+  for (int a = 0; a < A; ++a) {
+    const int w = row_cost(offs[ue[a] + 1] - offs[ue[a]]);
+    const int64_t span = (int64_t)N * w;
+    if (x < c + span) return a * N + (int)((x - c) / w);
+    c += span;
+  }
+  return A * N;
+}
+
 __device__ __forceinline__ void bar_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
 
 // Tokens per gate-score unit: a unit is (gate row, piece, group of up to
@@ -209,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1) decode_layer_kerne
   __shared__ int s_ue[256];
   __shared__ float s_sa[256];
   __shared__ int s_A, s_mmax, s_drop, s_abort;
+  __shared__ int s_rows[4];   // this CTA's rows [r1a, r1b) and [r2a, r2b)
   __shared__ __align__(8) uint64_t s_bar[2 * kMaxStages + 5];
   constexpr bool kSwi = kEpi == kEpiSwiglu;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -381,6 +406,11 @@ __global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1) decode_layer_kerne
       s_mmax = mx;
     }
     __syncwarp();
+    // this CTA's shares of the two products' weight rows
+    if (lane < 4) {
+      const int N = lane < 2 ? F : H;
+      s_rows[lane] = share_start(b + (lane & 1), nb, s_A, N, s_ue, s_offs);
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < S; c0 += 32) {
       const int s = c0 + lane;
@@ -420,13 +450,11 @@ __global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1) decode_layer_kerne
   DecodePlan pl{};
   const bool planned = routed && decode_plan(a.dyn_bytes, s_mmax, H, F, kSwi, &pl);
   if (routed && !planned && tid == 0) set_error(a.err, kDevBadIndex);
-  const int A = planned ? s_A : 0;
   const uint32_t row0 = (uint32_t)H * 2u, row1 = (uint32_t)F * 2u;
-  // this CTA's weight rows: the b-th of nb equal shares of the A * F rows of
-  // the first product and of the A * H rows of the second
-  const int64_t R1 = (int64_t)A * F, R2 = (int64_t)A * H;
-  const int r1a = (int)(R1 * b / nb), r1b = (int)(R1 * (b + 1) / nb);
-  const int r2a = (int)(R2 * b / nb), r2b = (int)(R2 * (b + 1) / nb);
+  // this CTA's weight rows: the b-th of nb shares of the A * F rows of the
+  // first product and of the A * H rows of the second, cut at equal cost
+  const int r1a = planned ? s_rows[0] : 0, r1b = planned ? s_rows[1] : 0;
+  const int r2a = planned ? s_rows[2] : 0, r2b = planned ? s_rows[3] : 0;
   const StageWalk walk0{r1a, r1b, r2a, r2b, F, H, pl.rps0, pl.rps1};
   const uint32_t s_act = tc::smem_u32(smem), s_ring = s_act + (uint32_t)pl.nab * pl.slot;
   const uint8_t* ring = smem + (size_t)pl.nab * pl.slot;
@@ -559,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, kMR <= 2 ? 2 : 1) decode_layer_kerne
       const uint8_t* st = ring + (size_t)s * pl.stage_bytes;
       // a segment of 2-4 rows dots two weight rows per warp (twice the
       // independent sums, half the activation reads); else one
-      const bool pairs = m >= 2 && m <= (kMR < 4 ? kMR : 4);
+      const bool pairs = m >= 1 && m <= (kMR < 4 ? kMR : 4);
       const int rps = sg.second ? pl.rps1 : pl.rps0;
       const int j = stage_row_of_warp(sg.gl, pairs ? (rps + 1) / 2 : rps, warp) * (pairs ? 2 : 1);
       if (j < sg.rows) {

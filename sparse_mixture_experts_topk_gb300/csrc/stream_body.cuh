@@ -159,7 +159,8 @@ __device__ __forceinline__ void stage_pair(const uint8_t* st, int j, int rps, ui
   const uint4* u0 = reinterpret_cast<const uint4*>(st + (size_t)(rps + j) * row_bytes);
   const uint4* w1 = reinterpret_cast<const uint4*>(st + (size_t)(j + 1) * row_bytes);
   const uint4* u1 = reinterpret_cast<const uint4*>(st + (size_t)(rps + j + 1) * row_bytes);
-  if (kMR <= 2 || m <= 2) dot_rows2<kEpi, 2>(w0, u0, w1, u1, act, kv, m, be, n, N, out);
+  if (m <= 1) dot_rows2<kEpi, 1>(w0, u0, w1, u1, act, kv, m, be, n, N, out);
+  else if (kMR <= 2 || m <= 2) dot_rows2<kEpi, 2>(w0, u0, w1, u1, act, kv, m, be, n, N, out);
   else dot_rows2<kEpi, 4>(w0, u0, w1, u1, act, kv, m, be, n, N, out);
 }
 
