@@ -40,6 +40,9 @@ CASES = {
     "temp_zipf": W.small("temp_zipf", T=7, H=128, E=16, K=4, F=96, temperature=0.7, gate_bias="zipf"),
     # four score pieces per gate row, 14 KB token rows
     "wide_h": W.small("wide_h", T=4, H=7168, E=16, K=2, F=512),
+    # all kept h rows (128 x 2 KB) do not fit beside the ring: the second
+    # product runs expert by expert and the combine reads y back
+    "t16_k8_wide_f": W.small("t16_k8_wide_f", T=16, H=256, E=64, K=8, F=1024),
 }
 
 
