@@ -21,7 +21,13 @@
 // only the 32-row boxes of token rows its half needs; the accumulator holds
 // the transposed tile (TMEM lane = output column, column = token row), and
 // each epilogue warp transposes its 32 x 32 blocks through 2 KB of shared
-// memory so that global stores stay 16-byte vectors along the row.  Full
+// memory so that global stores stay 16-byte vectors along the row.  A
+// swapped block of at most 32 rows runs wide: each stage brings the weight
+// rows of two n-tiles (in the stage's A and B slots) and the block's token
+// rows (a third, 2 KB slot), and the MMA issuer writes two accumulators,
+// 128 columns apart.  Such a block's tiles are bound by how fast the ring
+// turns over, not by the MMAs, so twice the weight bytes per stage halves
+// their count (measured: a 32-row tail tile took as long as a full one).  Full
 // blocks stay in row orientation because that transpose costs shared-memory
 // bandwidth the tensor cores need (measured: 15% slower for full tiles).
 // The SwiGLU first product keeps the row orientation for every block (N =
@@ -62,16 +68,19 @@ constexpr int kBM = 128;             // A rows per CTA (the pair covers M = 256)
 constexpr int kBNh = 128;            // B rows per CTA at most (the pair covers N <= 256)
 constexpr int kBK = 64;
 constexpr int kBoxB = 32;            // swapped: token rows per B box
+constexpr int kBoxT = 16;            // wide swapped tiles: token rows per box (a stage's T region)
+constexpr int kWideRows = 32;        // a tail block of at most this many rows runs wide
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 8;         // epilogue warps per pair (4 per CTA)
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBNh * kBK * 2;
 constexpr int kBoxBytes = kBoxB * kBK * 2;
+constexpr int kTBytes = kBoxT * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kStages = 6;
 constexpr int kTmemCols = 512;       // two 256-column accumulators
 constexpr int kXposeBytes = 4 * 32 * 32 * 2;   // epilogue transpose blocks, one per warp
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kXposeBytes;
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kStageBytes + kTBytes) + kXposeBytes;
 constexpr uint64_t kWaitNs = 2000000000ull;
 // Tile queue: the leader's producer takes tiles from a global counter and
 // publishes them here, in both CTAs, for every other role.  No role can be
@@ -127,6 +136,23 @@ __device__ __forceinline__ bool wait_count(const int* p, int need, const volatil
     }
     __nanosleep(64);
   }
+}
+
+// An expert of `rows` token rows has a wide tail when its last 256-row block
+// holds at most kWideRows rows and runs swapped (ok): that block's tiles then
+// cover two n-tiles each, the weight rows of both in one stage (the A and B
+// slots) with its few token rows in the stage's T slot, so a stage carries
+// 34 KB per CTA instead of 20 KB.
+__device__ __forceinline__ bool wide_tail(int rows, bool ok) {
+  if (!ok || rows <= 0) return false;
+  const int mt = (rows + 2 * kBM - 1) / (2 * kBM);
+  return rows - (mt - 1) * 2 * kBM <= kWideRows;
+}
+// The expert's pair tiles in one product of nt n-tiles.
+__device__ __forceinline__ int expert_tiles(int rows, int nt, bool ok) {
+  const int mt = (rows + 2 * kBM - 1) / (2 * kBM);
+  if (!(wide_tail(rows, ok) && nt >= 2)) return mt * nt;
+  return (nt / 2) * (2 * (mt - 1) + 1) + (nt % 2) * mt;
 }
 
 // One tile's epilogue: this warp's 32 accumulator lanes (TMEM lane quarter
@@ -240,15 +266,17 @@ __device__ __forceinline__ void tile_epilogue(uint32_t tbase, bool swap, int e, 
 //
 // Tensor maps, per product p: tmX = token rows [rows, K] in 128-row boxes
 // (row-orientation A), tmXs = the same rows in 32-row boxes (swapped B), tmW
-// = weight rows [E N, K] in 128-row boxes (row-orientation B, swapped A).
+// = weight rows [E N, K] in 128-row boxes (row-orientation B, swapped A),
+// tmXt = the token rows in 16-row boxes (wide swapped tiles).
 // kEpiA = kEpiSwiglu: tmW0 covers [W1; W3] stacked per expert ([E, 2N, K]);
 // the leader loads 128 gate rows and the peer the matching 128 up rows.
 // swap_tail = 0 keeps every block in row orientation.
 template <int kEpiA>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmXs0,
-                         const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmX1,
-                         const __grid_constant__ CUtensorMap tmXs1, const __grid_constant__ CUtensorMap tmW1,
+                         const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmXt0,
+                         const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmXs1,
+                         const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmXt1,
                          const int32_t* __restrict__ offs, int E, PairProduct P0, PairProduct P1, int nphase,
                          int swap_tail, int* __restrict__ next_tile, int* __restrict__ ready, int* err) {
   constexpr int S = kStages;
@@ -263,7 +291,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA = tc::smem_u32(smem);
   const uint32_t sB = sA + S * kABytes;
-  bf16* xpose = reinterpret_cast<bf16*>(smem + (size_t)S * kStageBytes);   // [4][32][32]
+  const uint32_t sT = sB + S * kBBytes;   // wide swapped tiles' token rows, kTBytes a stage
+  bf16* xpose = reinterpret_cast<bf16*>(smem + (size_t)S * (kStageBytes + kTBytes));   // [4][32][32]
   auto full = [&](int s) { return tc::smem_u32(&s_bar[s]); };
   auto empty = [&](int s) { return tc::smem_u32(&s_bar[S + s]); };
   auto tfull = [&](int a) { return tc::smem_u32(&s_bar[2 * S + a]); };
@@ -279,24 +308,27 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
   const int nt1 = (P1.N + kOutB - 1) / kOutB;
   const int nk0 = (P0.K + kBK - 1) / kBK;
   const int nk1 = (P1.K + kBK - 1) / kBK;
+  // wide tails: swapped blocks only (the SwiGLU first product never swaps)
+  auto wide_ok = [&](int p, int st) { return st != 0 && !(p == 0 && kSwiA); };
 
   if (warp == 0) {
     pdl_enter();   // the tile table reads offs, written by the previous kernel
-    // per-expert pair-tile counts (256-row blocks x n-tiles) of both products and their prefixes
+    // per-expert pair-tile counts (256-row blocks x n-tiles, a wide tail
+    // covering two n-tiles) of both products and their prefixes
     int loc0[8], loc1[8];
     int sum0 = 0, sum1 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane * 8 + i;
-      int mt = 0;
+      int rows = 0;
       if (e < E) {
         const int o0 = offs[e], o1 = offs[e + 1];
-        mt = (o1 - o0 + 2 * kBM - 1) / (2 * kBM);
+        rows = o1 - o0;
         s_offs[e] = o0;
         if (e == E - 1) s_offs[E] = o1;
       }
-      loc0[i] = mt * nt0;
-      loc1[i] = nphase > 1 ? mt * nt1 : 0;
+      loc0[i] = expert_tiles(rows, nt0, wide_ok(0, swap_tail));
+      loc1[i] = nphase > 1 ? expert_tiles(rows, nt1, wide_ok(1, swap_tail)) : 0;
       sum0 += loc0[i];
       sum1 += loc1[i];
     }
@@ -342,10 +374,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
       tc::prefetch_tmap(&tmX0);
       tc::prefetch_tmap(&tmXs0);
       tc::prefetch_tmap(&tmW0);
+      tc::prefetch_tmap(&tmXt0);
       if (nphase > 1) {
         tc::prefetch_tmap(&tmX1);
         tc::prefetch_tmap(&tmXs1);
         tc::prefetch_tmap(&tmW1);
+        tc::prefetch_tmap(&tmXt1);
       }
     }
   } else if (warp == 1) {
@@ -390,9 +424,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
   // rows of that block (<= 256), the MMA N (swapped: rows rounded up to 16;
   // else 256), the first output column and the block's ready counter.  Tiles
   // run product by product, expert by expert, row blocks inner.
+  // With a wide tail (at most kWideRows rows) an expert's n-tiles go in
+  // pairs: the full blocks of n-tile 2c, those of n-tile 2c + 1, then the
+  // one tail tile of both (so both weight slabs are still in L2); an odd
+  // last n-tile keeps its own tail.  Otherwise n-tiles outer, row blocks inner.
   struct Tile {
     int p, e, row_base, nrows, row_end, mma_n, n0, block;
-    bool swap;
+    bool swap, wide;
   };
   auto decode = [&](int t) {
     Tile d;
@@ -407,14 +445,39 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
     d.e = lo;
     const int rows = s_offs[d.e + 1] - s_offs[d.e];
     const int mt = (rows + 2 * kBM - 1) / (2 * kBM);
+    const int nt = d.p ? nt1 : nt0;
     const int local = tl - ts[d.e];
-    const int rb = local % mt;
+    int rb, col;
+    d.wide = false;
+    if (wide_tail(rows, wide_ok(d.p, swap_tail)) && nt >= 2) {
+      const int per = 2 * (mt - 1) + 1;   // tiles of an n-tile pair
+      if (local < (nt / 2) * per) {
+        const int c2 = local / per, w = local % per;
+        if (w < mt - 1) {
+          col = 2 * c2;
+          rb = w;
+        } else if (w < 2 * (mt - 1)) {
+          col = 2 * c2 + 1;
+          rb = w - (mt - 1);
+        } else {
+          col = 2 * c2;
+          rb = mt - 1;
+          d.wide = true;
+        }
+      } else {
+        col = nt - 1;
+        rb = local - (nt / 2) * per;
+      }
+    } else {
+      rb = local % mt;
+      col = local / mt;
+    }
     d.row_base = s_offs[d.e] + rb * (2 * kBM);
     d.row_end = s_offs[d.e + 1];
     d.nrows = min(2 * kBM, d.row_end - d.row_base);
     d.swap = !(d.p == 0 && kSwiA) && swap_tail && d.nrows < 2 * kBM;
     d.mma_n = d.swap ? (d.nrows + 15) / 16 * 16 : 2 * kBNh;
-    d.n0 = (local / mt) * (d.p ? kOutB : kOutA);
+    d.n0 = col * (d.p ? kOutB : kOutA);
     d.block = (s_offs[d.e] >> 8) + d.e + rb;
     return d;
   };
@@ -451,12 +514,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
         // swapped: this CTA's token rows start half the MMA N into the block
         const int half = d.mma_n / 2;
         const int nbox = (half + kBoxB - 1) / kBoxB;
-        const uint32_t tx = d.swap ? 2u * (uint32_t)(kABytes + nbox * kBoxBytes) : 2u * kStageBytes;
+        const uint32_t tx = d.wide ? 2u * (uint32_t)(kABytes + kBBytes + kTBytes)
+                                   : d.swap ? 2u * (uint32_t)(kABytes + nbox * kBoxBytes) : 2u * kStageBytes;
+        const CUtensorMap* mXt = d.p ? &tmXt1 : &tmXt0;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
           const uint32_t fbar = tc::map_peer(full(stage), 0);
           if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), tx);
-          if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
+          if (d.wide) {   // A, B = the weight rows of n-tiles n0 and n0 + 256, T = this CTA's token rows
+            tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+            tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
+                                 d.e * N + d.n0 + 2 * kBM + (int)rank * kBM);
+            tc::tma_load_2d_pair(sT + stage * kTBytes, mXt, fbar, kb * kBK, d.row_base + (int)rank * half);
+          } else if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
             tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
             for (int i = 0; i < nbox; ++i)
               tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, mXs, fbar, kb * kBK,
@@ -500,10 +570,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
           if (!tc::mbar_wait(full(stage), phase, &s_abort, kWaitNs)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t a0 = sA + stage * kABytes, b0 = sB + stage * kBBytes;
+          if (dt.wide) {
+            // two weight groups against the same token rows, into columns 0 and 128
+            const uint32_t t0 = sT + stage * kTBytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            tc::mma_bf16_pair(d, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(b0 + k * 32), idesc,
-                              (kb | k) != 0);
+            for (int k = 0; k < kBK / 16; ++k) {
+              tc::mma_bf16_pair(d, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(t0 + k * 32), idesc, (kb | k) != 0);
+              tc::mma_bf16_pair(d + kBM, tc::sdesc_k128(b0 + k * 32), tc::sdesc_k128(t0 + k * 32), idesc,
+                                (kb | k) != 0);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              tc::mma_bf16_pair(d, tc::sdesc_k128(a0 + k * 32), tc::sdesc_k128(b0 + k * 32), idesc,
+                                (kb | k) != 0);
+          }
           tc::tc_commit_pair_mc(empty(stage), 0x3);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -544,16 +625,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
       }
       tc::tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kBNh);
+      // a wide tile holds n-tile n0 in columns 0.. and n-tile n0 + 256 in columns 128..
+      const int groups = d.wide ? 2 : 1;
       if (d.p == 0) {
-        tile_epilogue<kEpiA>(tbase, d.swap, d.e, d.row_base, d.nrows, d.row_end, d.n0, rank, q, lane, xb, P0);
+        for (int g = 0; g < groups; ++g)
+          tile_epilogue<kEpiA>(tbase + g * kBM, d.swap, d.e, d.row_base, d.nrows, d.row_end, d.n0 + g * 2 * kBM,
+                               rank, q, lane, xb, P0);
         if (nphase > 1) {
-          // this warp's stores are visible GPU-wide before the block's counter moves
+          // this warp's stores are visible GPU-wide before the block's counter
+          // moves (by one per n-tile written)
           __threadfence();
           __syncwarp();
-          if (lane == 0) atomicAdd(ready + d.block, 1);
+          if (lane == 0) atomicAdd(ready + d.block, groups);
         }
       } else {
-        tile_epilogue<kEpiPlain>(tbase, d.swap, d.e, d.row_base, d.nrows, d.row_end, d.n0, rank, q, lane, xb, P1);
+        for (int g = 0; g < groups; ++g)
+          tile_epilogue<kEpiPlain>(tbase + g * kBM, d.swap, d.e, d.row_base, d.nrows, d.row_end, d.n0 + g * 2 * kBM,
+                                   rank, q, lane, xb, P1);
       }
       tc::tc_fence_before();
       if (rank == 0) tc::mbar_arrive(tempty(acc));
@@ -577,19 +665,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
   }
 }
 
-// The three tensor maps of one product: token rows A [rows, K] in 128- and
-// 32-row boxes, weight rows [wrows, K] in 128-row boxes.
-bool pair_maps(CUtensorMap* mx, CUtensorMap* mxs, CUtensorMap* mw, const void* A, int64_t rows, const void* B,
-               int64_t wrows, int K) {
+// The four tensor maps of one product: token rows A [rows, K] in 128-, 32-
+// and 16-row boxes, weight rows [wrows, K] in 128-row boxes.
+bool pair_maps(CUtensorMap* mx, CUtensorMap* mxs, CUtensorMap* mw, CUtensorMap* mxt, const void* A, int64_t rows,
+               const void* B, int64_t wrows, int K) {
   return tma_map_bf16(mx, A, (uint64_t)rows, (uint64_t)K, kBM) &&
          tma_map_bf16(mxs, A, (uint64_t)rows, (uint64_t)K, kBoxB) &&
-         tma_map_bf16(mw, B, (uint64_t)wrows, (uint64_t)K, kBNh);
+         tma_map_bf16(mw, B, (uint64_t)wrows, (uint64_t)K, kBNh) &&
+         tma_map_bf16(mxt, A, (uint64_t)rows, (uint64_t)K, kBoxT);
 }
 
 // One persistent launch: one resident pair per two SMs, never more pairs
 // than fit at once.
 template <int kEpiA>
-cudaError_t launch_pair(const CUtensorMap (&m)[6], const int32_t* offs, int E, const PairProduct& P0,
+cudaError_t launch_pair(const CUtensorMap (&m)[8], const int32_t* offs, int E, const PairProduct& P0,
                         const PairProduct& P1, int nphase, int swap_tail, int* next_tile, int* ready, int* err,
                         cudaStream_t st) {
   auto kern = grouped_gemm_pair_kernel<kEpiA>;
@@ -611,7 +700,7 @@ cudaError_t launch_pair(const CUtensorMap (&m)[6], const int32_t* offs, int E, c
   int fit = 0;
   if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) == cudaSuccess && fit > 0 && fit < pairs) pairs = fit;
   return launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), kSmem, st, 2, m[0], m[1], m[2], m[3], m[4],
-                       m[5], offs, E, P0, P1, nphase, swap_tail, next_tile, ready, err);
+                       m[5], m[6], m[7], offs, E, P0, P1, nphase, swap_tail, next_tile, ready, err);
 }
 
 }  // namespace
@@ -629,28 +718,28 @@ cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_p
   const bool swi = (s.flags & MOE_FLAG_SWIGLU) != 0;
   // each expert's last, short row block runs swapped unless all are forced to rows
   const int swap_tail = (s.flags & MOE_FLAG_GEMM_ROWS) ? 0 : 1;
-  CUtensorMap m1[6], m2[6];
-  if (!pair_maps(&m1[0], &m1[1], &m1[2], x_perm, max_rows, W1, (int64_t)s.E * s.F * (swi ? 2 : 1), s.H) ||
-      !pair_maps(&m2[0], &m2[1], &m2[2], h_perm, max_rows, W2, (int64_t)s.E * s.H, s.F))
+  CUtensorMap m1[4], m2[4];
+  if (!pair_maps(&m1[0], &m1[1], &m1[2], &m1[3], x_perm, max_rows, W1, (int64_t)s.E * s.F * (swi ? 2 : 1), s.H) ||
+      !pair_maps(&m2[0], &m2[1], &m2[2], &m2[3], h_perm, max_rows, W2, (int64_t)s.E * s.H, s.F))
     return cudaErrorNotSupported;
   const PairProduct P1{s.F, s.H, b1, (bf16*)h_perm, nullptr, nullptr, nullptr, s.K};
   const PairProduct P2{s.H, s.F, b2, (bf16*)y_perm, comb ? comb->src : nullptr, comb ? comb->w : nullptr,
                        comb ? comb->acc : nullptr, s.K};
   if (!(s.flags & MOE_FLAG_FFN_SPLIT)) {
     // both products in one launch: the second's tiles start on row blocks the first has finished
-    const CUtensorMap m[6] = {m1[0], m1[1], m1[2], m2[0], m2[1], m2[2]};
+    const CUtensorMap m[8] = {m1[0], m1[1], m1[2], m1[3], m2[0], m2[1], m2[2], m2[3]};
     cudaError_t r = swi ? launch_pair<kEpiSwiglu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st)
                         : launch_pair<kEpiGelu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st);
     if (r != cudaSuccess) return r;
     prof_mark(kMarkFirst, st);
     return cudaSuccess;
   }
-  const CUtensorMap ma[6] = {m1[0], m1[1], m1[2], m1[0], m1[1], m1[2]};
+  const CUtensorMap ma[8] = {m1[0], m1[1], m1[2], m1[3], m1[0], m1[1], m1[2], m1[3]};
   cudaError_t r = swi ? launch_pair<kEpiSwiglu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st)
                       : launch_pair<kEpiGelu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st);
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
-  const CUtensorMap mb[6] = {m2[0], m2[1], m2[2], m2[0], m2[1], m2[2]};
+  const CUtensorMap mb[8] = {m2[0], m2[1], m2[2], m2[3], m2[0], m2[1], m2[2], m2[3]};
   return launch_pair<kEpiPlain>(mb, offs, s.E, P2, P2, 1, swap_tail, sched + 1, nullptr, err, st);
 }
 
