@@ -22,9 +22,9 @@
 // the transposed tile (TMEM lane = output column, column = token row), and
 // each epilogue warp transposes its 32 x 32 blocks through 2 KB of shared
 // memory so that global stores stay 16-byte vectors along the row.  A
-// swapped block of at most 32 rows runs wide: each stage brings the weight
+// swapped block of at most 48 rows runs wide: each stage brings the weight
 // rows of two n-tiles (in the stage's A and B slots) and the block's token
-// rows (a third, 2 KB slot), and the MMA issuer writes two accumulators,
+// rows (a third, 3 KB slot), and the MMA issuer writes two accumulators,
 // 128 columns apart.  Such a block's tiles are bound by how fast the ring
 // turns over, not by the MMAs, so twice the weight bytes per stage halves
 // their count (measured: a 32-row tail tile took as long as a full one).  Full
@@ -68,8 +68,8 @@ constexpr int kBM = 128;             // A rows per CTA (the pair covers M = 256)
 constexpr int kBNh = 128;            // B rows per CTA at most (the pair covers N <= 256)
 constexpr int kBK = 64;
 constexpr int kBoxB = 32;            // swapped: token rows per B box
-constexpr int kBoxT = 16;            // wide swapped tiles: token rows per box (a stage's T region)
-constexpr int kWideRows = 32;        // a tail block of at most this many rows runs wide
+constexpr int kBoxT = 24;            // wide swapped tiles: token rows per box (a stage's T region)
+constexpr int kWideRows = 48;        // a tail block of at most this many rows runs wide
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 8;         // epilogue warps per pair (4 per CTA)
 constexpr int kABytes = kBM * kBK * 2;
@@ -142,7 +142,7 @@ __device__ __forceinline__ bool wait_count(const int* p, int need, const volatil
 // holds at most kWideRows rows and runs swapped (ok): that block's tiles then
 // cover two n-tiles each, the weight rows of both in one stage (the A and B
 // slots) with its few token rows in the stage's T slot, so a stage carries
-// 34 KB per CTA instead of 20 KB.
+// 35 KB per CTA instead of 19-22 KB.
 __device__ __forceinline__ bool wide_tail(int rows, bool ok) {
   if (!ok || rows <= 0) return false;
   const int mt = (rows + 2 * kBM - 1) / (2 * kBM);
