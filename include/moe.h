@@ -300,7 +300,9 @@ int moe_aux_loss(const moe_desc* desc, const float* psum, const int32_t* count,
  *     through the workspace; pinned host memory is fastest, and `out` is
  *     valid once `stream` has been synchronised).  With host pointers, no
  *     capacity and T >= 2048, the batch runs as two halves of tokens whose
- *     copies overlap the other half's layer: the copies go on two internal
+ *     copies overlap the other half's layer (the second half's output is
+ *     combined and copied back in two parts, the copy of the first part
+ *     overlapping the combine of the second): the copies go on two internal
  *     streams (created on the first such call of each host thread on each
  *     device, kept until the process exits) joined to `stream` by events,
  *     the outputs are the same bits, and count and the loss are the whole

@@ -387,6 +387,9 @@ Shape final_shape(const Shape& s) {
 // another.  Every piece reads all the expert weights again, so the pieces
 // stay few.
 constexpr int kIoChunks = 2;
+// The last piece's combine runs as this many launches, so that the copy of
+// each part of its output overlaps the combine of the next.
+constexpr int kLastParts = 2;
 constexpr int64_t kIoMinChunkTokens = 1024;
 
 bool io_chunked(const Shape& s) {
@@ -415,6 +418,8 @@ int moe_layer_launches(const moe_desc* desc) {
       dc.T = io_chunk_begin(s, c + 1) - io_chunk_begin(s, c);
       dc.flags &= ~MOE_FLAG_HOST_IO;
       n += moe_layer_launches(&dc);
+      // the last piece's combine as kLastParts launches
+      if (c == kIoChunks - 1 && !combine_fusable(shape_of(dc), rows_for(dc))) n += kLastParts - 1;
     }
   }
   if (s.T > 0) {                                        // expert FFN, combine
@@ -449,10 +454,20 @@ struct LayerStats {
   int32_t* dropped_copy;  // [1] caller's dropped, or null
 };
 
+// The combine of a layer pass run as `parts` launches over consecutive
+// ranges of its tokens, each followed by its event (so a copy of that range
+// of out can start while the rest is combined).  Same outputs: a token's
+// output depends on its own slots only.
+struct CombineParts {
+  int parts;
+  cudaEvent_t* done;
+};
+
 // The layer on device buffers xd -> outd (T = s.T tokens), on stream st.
 cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, const void* xd, const void* Wg,
                       const float* gate_bias, const void* W1, const float* b1, const void* W2, const float* b2,
-                      void* outd, const LayerStats& ls, bool marks, cudaStream_t st) {
+                      void* outd, const LayerStats& ls, bool marks, cudaStream_t st,
+                      const CombineParts* cparts = nullptr) {
   int* err = at<int>(ws, L.err);
   if (decode_layer_eligible(s)) {
     DecodeIO io;
@@ -542,8 +557,23 @@ cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, c
     e = launch_ffn(s, rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
                    at<int32_t>(ws, L.sched), st, fuse ? &ci : nullptr);
   if (marks) prof_mark(kMarkSecond, st);
-  if (e == cudaSuccess)
-    e = fuse ? launch_acc_to_out(s, acc, outd, st) : launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
+  if (e == cudaSuccess) {
+    if (fuse) {
+      e = launch_acc_to_out(s, acc, outd, st);
+    } else if (cparts && cparts->parts > 1) {
+      const size_t row_bytes = (size_t)s.H * s.esize();
+      for (int p = 0; p < cparts->parts && e == cudaSuccess; ++p) {
+        const int64_t t0 = s.T * p / cparts->parts, t1 = s.T * (p + 1) / cparts->parts;
+        Shape sp = s;
+        sp.T = t1 - t0;
+        e = launch_combine(sp, y_perm, at<int32_t>(ws, L.pos) + t0 * s.K, w + t0 * s.K,
+                           (char*)outd + t0 * row_bytes, st);
+        if (e == cudaSuccess) e = cudaEventRecord(cparts->done[p], st);
+      }
+    } else {
+      e = launch_combine(s, y_perm, at<int32_t>(ws, L.pos), w, outd, st);
+    }
+  }
   if (marks) prof_mark(kMarkCombine, st);
   return e;
 }
@@ -554,6 +584,7 @@ struct IoRes {
   bool ok = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t start = nullptr, in[kIoChunks] = {}, done[kIoChunks] = {}, end = nullptr;
+  cudaEvent_t part[kLastParts] = {};   // the last piece's combine, by parts
 };
 constexpr int kMaxIoDevices = 64;
 thread_local IoRes g_io[kMaxIoDevices];
@@ -574,6 +605,8 @@ cudaError_t io_resources(IoRes** out) {
       if ((e = cudaEventCreateWithFlags(&r.in[c], ef)) != cudaSuccess) return e;
       if ((e = cudaEventCreateWithFlags(&r.done[c], ef)) != cudaSuccess) return e;
     }
+    for (int p = 0; p < kLastParts; ++p)
+      if ((e = cudaEventCreateWithFlags(&r.part[p], ef)) != cudaSuccess) return e;
     r.ok = true;
   }
   *out = &r;
@@ -624,14 +657,31 @@ int moe_layer_forward(const moe_desc* desc, const void* x, const void* Wg, const
       dc.T = sc.T;
       const LayerStats ls{at<int32_t>(ws, L.count_chunks) + (size_t)c * s.E,
                           at<float>(ws, L.psum_chunks) + (size_t)c * s.E, nullptr, nullptr, nullptr};
+      const bool last = c == kIoChunks - 1;
+      const CombineParts cp{kLastParts, io->part};
       e = cudaStreamWaitEvent(st, io->in[c], 0);
       if (e == cudaSuccess)
         e = run_layer(sc, rows_for(dc), L, ws, xs + t0 * row_bytes, Wg, gate_bias, W1, b1, W2, b2,
-                      os + t0 * row_bytes, ls, false, st);
+                      os + t0 * row_bytes, ls, false, st, last && !combine_fusable(sc, rows_for(dc)) ? &cp : nullptr);
       if (e == cudaSuccess) e = cudaEventRecord(io->done[c], st);
     }
     for (int c = 0; c < kIoChunks && e == cudaSuccess; ++c) {
       const int64_t t0 = io_chunk_begin(s, c), t1 = io_chunk_begin(s, c + 1);
+      Shape sc = s;
+      sc.T = t1 - t0;
+      moe_desc dc = d;
+      dc.T = sc.T;
+      if (c == kIoChunks - 1 && !combine_fusable(sc, rows_for(dc))) {
+        // the last piece's output in parts, each as soon as its combine is done
+        for (int p = 0; p < kLastParts && e == cudaSuccess; ++p) {
+          const int64_t a = t0 + sc.T * p / kLastParts, b = t0 + sc.T * (p + 1) / kLastParts;
+          e = cudaStreamWaitEvent(io->d2h, io->part[p], 0);
+          if (e == cudaSuccess)
+            e = cudaMemcpyAsync((char*)out + a * row_bytes, os + a * row_bytes, (size_t)(b - a) * row_bytes,
+                                cudaMemcpyDeviceToHost, io->d2h);
+        }
+        continue;
+      }
       e = cudaStreamWaitEvent(io->d2h, io->done[c], 0);
       if (e == cudaSuccess)
         e = cudaMemcpyAsync((char*)out + t0 * row_bytes, os + t0 * row_bytes, (size_t)(t1 - t0) * row_bytes,
