@@ -20,11 +20,11 @@ from harness import to_dev, to_np, as_f64, product_tol, GELU_SLOPE
 pytestmark = pytest.mark.gpu
 
 H, F = 512, 768
-# rows per expert: 0 (empty), wide tails (1, 16, 32, 33, 48), swapped (49,
-# 128), row orientation (129, 255), a full block (256), full blocks with wide
-# or swapped tails (256 + 48, 256 + 49), and two full blocks with tails either
-# side of the swap limit (512 + 128, 512 + 129)
-COUNTS = [1, 16, 0, 32, 33, 48, 49, 128, 129, 255, 256, 304, 305, 640, 641]
+# rows per expert: 0 (empty), wide tails alone (1, 16, 32, 33, 48), swapped
+# (49, 128), row orientation (129, 255), a full block (256), full blocks with
+# a wide tail (256 + 1, 256 + 48, 512 + 48) or a swapped one (256 + 49), and
+# two full blocks with tails either side of the swap limit (512 + 128, 512 + 129)
+COUNTS = [1, 16, 0, 32, 33, 48, 49, 128, 129, 255, 256, 257, 304, 305, 560, 640, 641]
 E = len(COUNTS)
 
 KINDS = {
