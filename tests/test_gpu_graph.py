@@ -18,8 +18,9 @@ pytestmark = pytest.mark.gpu
 CASES = {
     # tensor-core router with tile counts, scan+scatter, SM-pair GEMM
     "ragged_bf16": W.small("ragged_bf16", T=333, H=512, E=8, K=2, F=768),
-    # small-batch router, one-block dispatch, weight streaming
+    # the one-launch decode layer: one CTA per SM (4 tokens), two per SM (1 token)
     "decode4": W.small("decode4", T=4, H=512, E=16, K=2, F=256, x_kind="decode_distinct"),
+    "decode1": W.small("decode1", T=1, H=512, E=32, K=2, F=256),
     # SwiGLU experts with capacity drops
     "swiglu_cap": W.small("swiglu_cap", T=300, H=256, E=8, K=2, F=384, act="swiglu",
                           capacity=W.capacity_ceil(300, 8, 2) // 2, gate_bias="zipf"),

@@ -217,9 +217,12 @@ def test_empty_batch():
     assert L["out"].numel() == 0 and int(to_np(L["dropped"])[0]) == 0
 
 
-def test_host_io_layer_matches_device_layer():
+@pytest.mark.parametrize("name", ["ragged_bf16", "one_token", "decode4"])
+def test_host_io_layer_matches_device_layer(name):
+    """Host x and out, copied through the workspace: the device layer's bits
+    (the multi-block path, and decode-sized batches on the one-launch layer)."""
     torch = pytest.importorskip("torch")
-    w = SMALL["ragged_bf16"]
+    w = SMALL[name]
     dev = Dev(W.generate(w))
     ref = run_layer(dev)
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity, moe.MOE_BF16, moe.MOE_FLAG_HOST_IO)
