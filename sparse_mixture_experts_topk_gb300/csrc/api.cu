@@ -421,6 +421,7 @@ int moe_layer_launches(const moe_desc* desc) {
       // the last piece's combine as kLastParts launches
       if (c == kIoChunks - 1 && !combine_fusable(shape_of(dc), rows_for(dc))) n += kLastParts - 1;
     }
+    return n;
   }
   if (s.T > 0) {                                        // expert FFN, combine
     const int k = ffn_kernel(s, rows_for(*desc));

@@ -94,6 +94,14 @@ def test_layer_launch_count(lib):
     assert moe.moe_layer_decode_fused(moe.make_desc(16, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_SWIGLU))
     assert moe.moe_layer_decode_fused(moe.make_desc(1, 3584, 32, 2, 2560))
     assert moe.moe_layer_launches(moe.make_desc(0, 3584, 32, 2, 2560)) == 1
+    # host buffers, no capacity: two halves of 4096 tokens (each router, scan+scatter, gather,
+    # expert FFN, combine; the second half's combine in two launches), then the statistics merge
+    host = moe.make_desc(8192, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_HOST_IO)
+    assert moe.moe_layer_launches(host) == 1 + 2 * (1 + 2 + 1 + 1) + 1
+    # with a capacity the whole batch runs once between its two copies
+    host_cap = moe.make_desc(8192, 3584, 32, 2, 2560, capacity=512, flags=moe.MOE_FLAG_HOST_IO)
+    assert moe.moe_layer_launches(host_cap) == moe.moe_layer_launches(
+        moe.make_desc(8192, 3584, 32, 2, 2560, capacity=512))
     with pytest.raises(moe.MoeError):
         moe.moe_layer_launches(moe.make_desc(8, 3584, 32, 9, 2560))
     with pytest.raises(moe.MoeError):
