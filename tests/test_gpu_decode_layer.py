@@ -43,6 +43,12 @@ CASES = {
     # all kept h rows (128 x 2 KB) do not fit beside the ring: the second
     # product runs expert by expert and the combine reads y back
     "t16_k8_wide_f": W.small("t16_k8_wide_f", T=16, H=256, E=64, K=8, F=1024),
+    # top-1 routing (weights all 1), the smallest expert count, one token on both experts
+    "t3_k1": W.small("t3_k1", T=3, H=256, E=4, K=1, F=128),
+    "t1_e2": W.small("t1_e2", T=1, H=256, E=2, K=2, F=128),
+    "t16_e256_k1": W.small("t16_e256_k1", T=16, H=128, E=256, K=1, F=64),
+    # capacity 1 with every token preferring the same two experts: most slots dropped
+    "t9_hot_cap1": W.small("t9_hot_cap1", T=9, H=128, E=8, K=2, F=96, gate_bias="hot", capacity=1),
 }
 
 
