@@ -85,7 +85,8 @@ def config_of(w: W.Workload, world: int, rows: int, used: int, gemm: str):
 
 def gemm_desc(args) -> str:
     return args.gemm + ("+fused-combine" if getattr(args, "fused_combine", False) else "") + \
-        ("+decode-split" if getattr(args, "decode_split", False) else "")
+        ("+decode-split" if getattr(args, "decode_split", False) else "") + \
+        ("+gather-gemm" if getattr(args, "gather_gemm", False) else "")
 
 
 def describe(w: W.Workload) -> str:
@@ -299,7 +300,8 @@ def run_ours(args, w: W.Workload):
     dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
     flags = (moe.MOE_FLAG_SWIGLU if w.act == "swiglu" else 0) | (moe.MOE_FLAG_REROUTE if w.reroute else 0) | \
         (moe.MOE_FLAG_FUSED_COMBINE if args.fused_combine else 0) | \
-        (moe.MOE_FLAG_DECODE_SPLIT if args.decode_split else 0) | GEMM_FLAGS[args.gemm]
+        (moe.MOE_FLAG_DECODE_SPLIT if args.decode_split else 0) | \
+        (moe.MOE_FLAG_GATHER_GEMM if args.gather_gemm else 0) | GEMM_FLAGS[args.gemm]
     d = moe.make_desc(w.T, w.H, w.E, w.K, w.F, w.capacity,
                       moe.MOE_BF16 if w.dtype == W.BF16 else moe.MOE_F32, flags, w.temperature)
     launches_per_step = moe.moe_layer_launches(d)
@@ -530,6 +532,8 @@ def main():
                     help="fold the weighted combine into the second expert product's epilogue")
     ap.add_argument("--decode-split", action="store_true",
                     help="decode-sized batches: the layer's separate steps instead of the one-launch layer")
+    ap.add_argument("--gather-gemm", action="store_true",
+                    help="the first expert product reads its token rows from x (no gather kernel, no x_perm)")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":

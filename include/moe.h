@@ -110,6 +110,13 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * workspace between the steps.  Same results, bit for bit; for comparing
  * the two (testing). */
 #define MOE_FLAG_DECODE_SPLIT  (1u << 12)
+/* bf16 layers on the SM-pair expert GEMMs, without MOE_FLAG_REROUTE:
+ * moe_layer_forward runs no gather of x rows; the first expert product
+ * copies each kept row's token row from x itself (slot s = src[r] of kept
+ * row r is token s / K; Qwen2-MoE walkthrough, jsqmd.com, section 3.1 item
+ * 3, grouping without a host-side sort), so x_perm is never written.  Same
+ * results, bit for bit.  Ignored where it does not apply. */
+#define MOE_FLAG_GATHER_GEMM   (1u << 13)
 
 /*
  * Layer description.  Field names follow the Qwen2MoEConfig fields of the

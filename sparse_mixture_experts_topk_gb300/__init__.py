@@ -18,7 +18,7 @@ import os
 __all__ = [
     "MoeDesc", "MoeError", "MOE_F32", "MOE_BF16", "MOE_FLAG_HOST_IO", "MOE_FLAG_SIMT_FFN",
     "MOE_FLAG_NO_DECODE", "MOE_FLAG_SIMT_ROUTER", "MOE_FLAG_GEMM_SINGLE", "MOE_FLAG_GEMM_PAIR", "MOE_FLAG_SWIGLU",
-    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "MOE_FLAG_REROUTE", "MOE_FLAG_FUSED_COMBINE", "MOE_FLAG_DECODE_SPLIT", "lib",
+    "MOE_FLAG_TEST_WAIT_TIMEOUT", "MOE_FLAG_GEMM_ROWS", "MOE_FLAG_FFN_SPLIT", "MOE_FLAG_REROUTE", "MOE_FLAG_FUSED_COMBINE", "MOE_FLAG_DECODE_SPLIT", "MOE_FLAG_GATHER_GEMM", "lib",
     "library_path", "make_desc", "moe_reroute",
     "moe_status_string", "moe_capacity_default", "moe_max_rows", "moe_workspace_size",
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
@@ -41,6 +41,7 @@ MOE_FLAG_FFN_SPLIT = 1 << 9
 MOE_FLAG_REROUTE = 1 << 10
 MOE_FLAG_FUSED_COMBINE = 1 << 11
 MOE_FLAG_DECODE_SPLIT = 1 << 12
+MOE_FLAG_GATHER_GEMM = 1 << 13
 # moe_ffn_kernel results
 MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED, MOE_FFN_STREAM_SPLIT = 0, 1, 2, 3, 4, 5
 

@@ -25,7 +25,7 @@ cudaError_t launch_ffn_tc(const Shape& s, int64_t max_rows, const void* x_perm, 
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
                                void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
-                               const CombineInto* comb);
+                               const CombineInto* comb, const GatherRows* gather);
 
 // SM-pair tiles move a third less data per SM for the same MMA work.  The
 // single-SM kernel pads each expert's rows to 128; the pair kernel runs its
@@ -119,15 +119,19 @@ bool combine_fusable(const Shape& s, int64_t max_rows) {
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
-                       const CombineInto* comb) {
+                       const CombineInto* comb, const GatherRows* gather) {
   if (s.T == 0 || max_rows == 0) return cudaSuccess;
+  if (gather && !(s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN) && !stream_ffn_eligible(s) &&
+                  use_pair_gemm(s, max_rows)))
+    return cudaErrorNotSupported;
   if (stream_ffn_eligible(s))
     return launch_ffn_stream(s, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st);
   // bf16 runs on the tensor cores; there is no silent fallback (an
   // unsupported shape or a missing tensor-map entry point is an error)
   if (s.dtype == MOE_BF16 && !(s.flags & MOE_FLAG_SIMT_FFN)) {
     if (use_pair_gemm(s, max_rows))
-      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st, comb);
+      return launch_ffn_tc_pair(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, sched, st, comb,
+                                gather);
     return launch_ffn_tc(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, err, st);
   }
   return launch_ffn_simt(s, max_rows, x_perm, offs, W1, b1, W2, b2, h_perm, y_perm, st);
@@ -376,6 +380,14 @@ bool layer_fused_hist(const Shape& s) { return router_on_tensor_cores(s) && !dis
 // the gather, the move of the over-capacity slots, then a dispatch of the
 // moved routing (no capacity cut: no expert is over any more).
 bool layer_reroutes(const Shape& s) { return (s.flags & MOE_FLAG_REROUTE) && s.C > 0 && s.T > 0; }
+// The first product gathers its token rows from x when asked for, on the
+// SM-pair kernels, except where the over-capacity slots are moved (that
+// path dispatches twice).
+bool layer_gathers(const Shape& s, int64_t max_rows) {
+  if (!(s.flags & MOE_FLAG_GATHER_GEMM) || s.T == 0 || layer_reroutes(s)) return false;
+  const int k = ffn_kernel(s, max_rows);
+  return k == MOE_FFN_TC_FUSED || k == MOE_FFN_TC_PAIRS;
+}
 Shape final_shape(const Shape& s) {
   Shape f = s;
   f.C = 0;
@@ -407,6 +419,7 @@ int moe_layer_launches(const moe_desc* desc) {
   if (s.T > 0) n += 1;                                  // router
   n += dispatch_launches(s, layer_fused_hist(s));       // one block, or (histogram,) scan, scatter, gather
   if (s.T > 0 && combine_fusable(s, rows_for(*desc))) n += 1;   // zeroing the fp32 combine target
+  if (layer_gathers(s, rows_for(*desc)) && !dispatch_small(s)) n -= 1;   // the first product gathers
   if (layer_reroutes(s)) {
     if (!dispatch_small(s)) n -= 1;                     // the first dispatch gathers nothing
     n += 2 + dispatch_launches(final_shape(s), false);  // the move (2), then the dispatch of the moved routing
@@ -502,6 +515,7 @@ cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, c
   float* part = at<float>(ws, L.psum_part);
   const bool fused_hist = layer_fused_hist(s);
   const bool rr = layer_reroutes(s);
+  const bool gat = layer_gathers(s, rows);   // no gather kernel: the first product reads x itself
   float* scores = rr ? at<float>(ws, L.scores) : nullptr;
   e = launch_router(s, xd, Wg, gate_bias, scores, ids, w, part, err, st,
                     fused_hist ? at<int32_t>(ws, L.blk_hist) : nullptr);
@@ -525,7 +539,8 @@ cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, c
       o.dropped_copy = ls.dropped_copy;
       o.sched = at<int32_t>(ws, L.sched);
     }
-    e = launch_dispatch(s, ids, rr ? nullptr : xd, rr ? nullptr : at<void>(ws, L.x_perm), o, err, st);
+    e = launch_dispatch(s, ids, rr || gat ? nullptr : xd, rr || gat ? nullptr : at<void>(ws, L.x_perm), o, err,
+                        st);
   }
   if (e == cudaSuccess && rr) {
     // the routing's own counts (the loss) are in; now move the slots the
@@ -554,9 +569,10 @@ cudaError_t run_layer(const Shape& s, int64_t rows, const Layout& L, void* ws, c
   void* h_perm = at<void>(ws, L.h_perm);
   void* y_perm = x_perm;   // x_perm is dead once the first product has run
   const CombineInto ci{at<int32_t>(ws, L.src), w, acc};
+  const GatherRows gr{xd, at<int32_t>(ws, L.src)};
   if (e == cudaSuccess)
     e = launch_ffn(s, rows, x_perm, at<int32_t>(ws, L.offs), W1, b1, W2, b2, h_perm, y_perm, err,
-                   at<int32_t>(ws, L.sched), st, fuse ? &ci : nullptr);
+                   at<int32_t>(ws, L.sched), st, fuse ? &ci : nullptr, gat ? &gr : nullptr);
   if (marks) prof_mark(kMarkSecond, st);
   if (e == cudaSuccess) {
     if (fuse) {

@@ -58,6 +58,15 @@
 // All waits are bounded (timeout -> error word + abort flag); the CTAs meet
 // in cluster barriers after set-up and before exit so neither can touch the
 // other's shared memory once it has left.
+//
+// Gathering instantiation (kGather): the first product's token rows are read
+// from x by the slot list instead of from x_perm, so the layer runs no
+// gather kernel (Qwen2-MoE walkthrough, jsqmd.com, section 3.1 item 3).  The
+// whole of warp 0 copies them with 16-byte cp.async copies into the stage,
+// in the 128-byte swizzle; a stage counts as full once both CTAs' warps have
+// waited for their copies, fenced them for the async proxy and arrived.  It
+// gives the same bits as x_perm and is measured about 4x slower (the small
+// copies do not keep up with the MMAs), so it is not the default.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -90,6 +99,12 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // more than kStages + 2 tiles behind the producer (its ring and the two
 // accumulators hold it back), so 16 entries never overwrite one still unread.
 constexpr int kTQ = 16;
+// gathered token rows: each lane copies one 16-byte chunk of rows
+// lane / 8 + 4 i of the CTA's (at most 128) rows
+constexpr int kGatherPer = kBM / 4;
+// a gathered stage is signalled once at most this many newer ones are still copying
+constexpr int kGatherLag = 4;
+static_assert(kGatherLag < kStages, "gathered stages signalled too late");
 static_assert(kTQ > kStages + 3, "tile queue shorter than the pipeline");
 constexpr int kTqAbort = -2;
 
@@ -98,6 +113,9 @@ constexpr int kTqAbort = -2;
 // (the second product only) the rows are not stored: row r, the slot
 // s = src[r] of token t = s / topk, adds wts[s] * bf16(y) to acc[t, :] (fp32,
 // zeroed beforehand) -- the weighted combine done in the epilogue.
+// With gx set (the first product only) the token rows are not read from the
+// tensor maps: kept row r is row gsrc[r] / topk of gx [gtok, K], copied by
+// the producer warp.
 struct PairProduct {
   int N, K;
   const float* bias;
@@ -106,6 +124,9 @@ struct PairProduct {
   const float* wts;
   float* acc;
   int topk;
+  const bf16* gx;
+  const int32_t* gsrc;
+  int gtok;
 };
 
 // acc[0..7] += w * v[0..7] with two 16-byte vector reductions (addr 32-byte aligned)
@@ -274,7 +295,9 @@ __device__ __forceinline__ void tile_epilogue(uint32_t tbase, bool swap, int e, 
 // kEpiA = kEpiSwiglu: tmW0 covers [W1; W3] stacked per expert ([E, 2N, K]);
 // the leader loads 128 gate rows and the peer the matching 128 up rows.
 // swap_tail = 0 keeps every block in row orientation.
-template <int kEpiA>
+// kGather: the first product's token rows come from P0.gx by P0.gsrc (the
+// producer warp copies them), not from tmX0 / tmXs0 / tmXt0.
+template <int kEpiA, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmXs0,
                          const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmXt0,
@@ -362,7 +385,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
     }
     if (lane == 0) {
       for (int s = 0; s < S; ++s) {
-        tc::mbar_init(full(s), 1);       // used in the leader: its arm + both CTAs' bytes
+        // used in the leader: its arm + both CTAs' bytes (+ both producers'
+        // arrivals when the first product's token rows are gathered)
+        tc::mbar_init(full(s), kGather ? 3 : 1);
         tc::mbar_init(empty(s), 1);      // one multicast commit per use
       }
       for (int a = 0; a < 2; ++a) {
@@ -488,27 +513,122 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
   uint32_t filled = 0, fill_par = 0;   // producer: per stage, ever filled / parity of its last fill
   bool producer = false;
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (tc::elect_one()) {
-      producer = true;
+    if constexpr (!kGather) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      if (tc::elect_one()) {
+        producer = true;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int t_next = rank == 0 ? atomicAdd(next_tile, 1) : 0;
+        for (int seq = 0; ok; ++seq) {
+          int t;
+          if (rank == 0) {
+            t = t_next < total ? t_next : -1;
+            tq_publish(seq, t);
+            if (t >= 0) t_next = atomicAdd(next_tile, 1);   // the following tile, fetched while this one loads
+          } else {
+            t = tq_read(seq);
+            if (t == kTqAbort) { ok = false; break; }
+          }
+          if (t < 0) break;
+          const Tile d = decode(t);
+          // a second-product tile reads hidden rows that other SMs write
+          if (d.p == 1 && !wait_count(ready + d.block, kEpiWarps * nt0, &s_abort)) { ok = false; break; }
+          const CUtensorMap* mX = d.p ? &tmX1 : &tmX0;
+          const CUtensorMap* mXs = d.p ? &tmXs1 : &tmXs0;
+          const CUtensorMap* mW = d.p ? &tmW1 : &tmW0;
+          const int N = d.p ? P1.N : P0.N;
+          const int nk = d.p ? nk1 : nk0;
+          // swapped: this CTA's token rows start half the MMA N into the block
+          const int half = d.mma_n / 2;
+          const int nbox = (half + kBoxB - 1) / kBoxB;
+          const uint32_t tx = d.wide ? 2u * (uint32_t)(kABytes + kBBytes + kTBytes)
+                                     : d.swap ? 2u * (uint32_t)(kABytes + nbox * kBoxBytes) : 2u * kStageBytes;
+          const CUtensorMap* mXt = d.p ? &tmXt1 : &tmXt0;
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
+            const uint32_t fbar = tc::map_peer(full(stage), 0);
+            if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), tx);
+            if (d.wide) {   // A, B = the weight rows of n-tiles n0 and n0 + 256, T = this CTA's token rows
+              tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+              tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
+                                   d.e * N + d.n0 + 2 * kBM + (int)rank * kBM);
+              tc::tma_load_2d_pair(sT + stage * kTBytes, mXt, fbar, kb * kBK, d.row_base + (int)rank * half);
+            } else if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
+              tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+              for (int i = 0; i < nbox; ++i)
+                tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, mXs, fbar, kb * kBK,
+                                     d.row_base + (int)rank * half + i * kBoxB);
+            } else {        // A = this CTA's 128 token rows, B = its 128 weight rows
+              tc::tma_load_2d_pair(sA + stage * kABytes, mX, fbar, kb * kBK, d.row_base + (int)rank * kBM);
+              tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
+                                   (d.p == 0 && kSwiA) ? 2 * d.e * N + (int)rank * N + d.n0
+                                                       : d.e * N + d.n0 + (int)rank * kBNh);
+            }
+            filled |= 1u << stage;
+            fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (!ok) {
+          set_error(err, kDevTimeout);
+          s_abort = 1;
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ gathering producer (both CTAs)
+      // Lane 0 takes the tiles, waits on the ring and issues the TMA copies.
+      // The first product's token rows are copied by the whole warp,
+      // 16 bytes a lane (8 lanes to a row's 128-byte segment, placed in the
+      // 128-byte swizzle the MMA descriptors read); such a stage is signalled
+      // on the leader's `full` barrier only once this warp's copies into it
+      // have landed and been fenced for the tensor cores.
+      producer = lane == 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int t_next = rank == 0 ? atomicAdd(next_tile, 1) : 0;
-      for (int seq = 0; ok; ++seq) {
-        int t;
-        if (rank == 0) {
-          t = t_next < total ? t_next : -1;
-          tq_publish(seq, t);
-          if (t >= 0) t_next = atomicAdd(next_tile, 1);   // the following tile, fetched while this one loads
-        } else {
-          t = tq_read(seq);
-          if (t == kTqAbort) { ok = false; break; }
+      int npend = 0;                              // gathered stages before `stage` not yet signalled
+      const int rg = lane >> 3, ch = lane & 7;   // this lane's rows rg + 4 i, 16-byte chunk ch
+      auto signal = [&](int st) {                // this CTA's part of stage st is in place
+        if (lane == 0) {
+          if (rank == 0) tc::mbar_arrive(full(st));
+          else tc::mbar_arrive_remote(tc::map_peer(full(st), 0));
         }
+      };
+      auto settle = [&](int keep) {              // signal all but the `keep` newest gathered stages
+        if (npend <= keep) return;
+        tc::cp_async_wait_max(keep);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        for (; npend > keep; --npend) signal((stage - npend + S) % S);
+      };
+      int t_next = (rank == 0 && lane == 0) ? atomicAdd(next_tile, 1) : 0;
+      for (int seq = 0; ok; ++seq) {
+        int t = 0;
+        if (lane == 0) {
+          if (rank == 0) {
+            t = t_next < total ? t_next : -1;
+            tq_publish(seq, t);
+            if (t >= 0) t_next = atomicAdd(next_tile, 1);   // the following tile, fetched while this one loads
+          } else {
+            t = tq_read(seq);
+          }
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+        if (t == kTqAbort) { ok = false; break; }
         if (t < 0) break;
         const Tile d = decode(t);
-        // a second-product tile reads hidden rows that other SMs write
-        if (d.p == 1 && !wait_count(ready + d.block, kEpiWarps * nt0, &s_abort)) { ok = false; break; }
+        const bool gat = d.p == 0;
+        // a second-product tile reads hidden rows that other SMs write (and
+        // those may wait on stages this warp has not signalled yet)
+        if (d.p == 1) {
+          settle(0);
+          int w = 1;
+          if (lane == 0) w = wait_count(ready + d.block, kEpiWarps * nt0, &s_abort) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
         const CUtensorMap* mX = d.p ? &tmX1 : &tmX0;
         const CUtensorMap* mXs = d.p ? &tmXs1 : &tmXs0;
         const CUtensorMap* mW = d.p ? &tmW1 : &tmW0;
@@ -517,40 +637,106 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
         // swapped: this CTA's token rows start half the MMA N into the block
         const int half = d.mma_n / 2;
         const int nbox = (half + kBoxB - 1) / kBoxB;
-        const uint32_t tx = d.wide ? 2u * (uint32_t)(kABytes + kBBytes + kTBytes)
-                                   : d.swap ? 2u * (uint32_t)(kABytes + nbox * kBoxBytes) : 2u * kStageBytes;
+        uint32_t tx = d.wide ? 2u * (uint32_t)(kABytes + kBBytes + kTBytes)
+                             : d.swap ? 2u * (uint32_t)(kABytes + nbox * kBoxBytes) : 2u * kStageBytes;
         const CUtensorMap* mXt = d.p ? &tmXt1 : &tmXt0;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs)) { ok = false; break; }
-          const uint32_t fbar = tc::map_peer(full(stage), 0);
-          if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), tx);
-          if (d.wide) {   // A, B = the weight rows of n-tiles n0 and n0 + 256, T = this CTA's token rows
-            tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
-            tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
-                                 d.e * N + d.n0 + 2 * kBM + (int)rank * kBM);
-            tc::tma_load_2d_pair(sT + stage * kTBytes, mXt, fbar, kb * kBK, d.row_base + (int)rank * half);
-          } else if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
-            tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
-            for (int i = 0; i < nbox; ++i)
-              tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, mXs, fbar, kb * kBK,
-                                   d.row_base + (int)rank * half + i * kBoxB);
-          } else {        // A = this CTA's 128 token rows, B = its 128 weight rows
-            tc::tma_load_2d_pair(sA + stage * kABytes, mX, fbar, kb * kBK, d.row_base + (int)rank * kBM);
-            tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
-                                 (d.p == 0 && kSwiA) ? 2 * d.e * N + (int)rank * N + d.n0
-                                                     : d.e * N + d.n0 + (int)rank * kBNh);
+        // gathered: where this lane's rows start in gx (16-byte units), ~0u for
+        // a row past the block's end (its accumulator row is never stored)
+        uint32_t rv[kGatherPer];
+        int nper = 0;
+        if (gat) {
+          tx = d.wide ? 2u * (uint32_t)(kABytes + kBBytes) : d.swap ? 2u * (uint32_t)kABytes : 2u * (uint32_t)kBBytes;
+          const int nload = d.swap ? half : kBM;
+          const int first = d.row_base + (int)rank * nload;
+          nper = (nload + 3) / 4;
+  #pragma unroll
+          for (int i = 0; i < kGatherPer; ++i) {
+            rv[i] = ~0u;
+            const int j = rg + 4 * i, r = first + j;
+            if (i < nper && j < nload && r < d.row_end) {
+              const int sl = P0.gsrc[r];
+              if (sl >= 0 && sl / P0.topk < P0.gtok) rv[i] = (uint32_t)(sl / P0.topk) * (uint32_t)(P0.K / 8);
+              else set_error(err, kDevBadIndex);
+            }
           }
-          filled |= 1u << stage;
-          fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+        }
+        for (int kb = 0; kb < nk; ++kb) {
+          // the slot's previous contents are consumed: while it is not, the
+          // gathered stages still pending are signalled as they land, oldest
+          // first; with none pending lane 0 alone waits (the other lanes
+          // parked, so the warp takes no issue slots from the epilogue warp
+          // beside it)
+          {
+            int r = 0;
+            while (npend > 0) {
+              if (lane == 0) r = tc::mbar_test_wait(empty(stage), phase ^ 1u) ? 1 : 0;
+              r = __shfl_sync(0xffffffffu, r, 0);
+              if (r) break;
+              settle(npend - 1);
+            }
+            if (!r) {
+              if (lane == 0) r = tc::mbar_wait(empty(stage), phase ^ 1u, &s_abort, kWaitNs) ? 1 : 2;
+              r = __shfl_sync(0xffffffffu, r, 0);
+            }
+            if (r != 1) { ok = false; break; }
+          }
+          if (lane == 0) {
+            const uint32_t fbar = tc::map_peer(full(stage), 0);
+            if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), tx);
+            if (d.wide) {   // A, B = the weight rows of n-tiles n0 and n0 + 256, T = this CTA's token rows
+              tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+              tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
+                                   d.e * N + d.n0 + 2 * kBM + (int)rank * kBM);
+              if (!gat)
+                tc::tma_load_2d_pair(sT + stage * kTBytes, mXt, fbar, kb * kBK, d.row_base + (int)rank * half);
+            } else if (d.swap) {   // A = weight rows, B = this CTA's half of the token rows
+              tc::tma_load_2d_pair(sA + stage * kABytes, mW, fbar, kb * kBK, d.e * N + d.n0 + (int)rank * kBM);
+              if (!gat)
+                for (int i = 0; i < nbox; ++i)
+                  tc::tma_load_2d_pair(sB + stage * kBBytes + i * kBoxBytes, mXs, fbar, kb * kBK,
+                                       d.row_base + (int)rank * half + i * kBoxB);
+            } else {        // A = this CTA's 128 token rows, B = its 128 weight rows
+              if (!gat)
+                tc::tma_load_2d_pair(sA + stage * kABytes, mX, fbar, kb * kBK, d.row_base + (int)rank * kBM);
+              tc::tma_load_2d_pair(sB + stage * kBBytes, mW, fbar, kb * kBK,
+                                   (d.p == 0 && kSwiA) ? 2 * d.e * N + (int)rank * N + d.n0
+                                                       : d.e * N + d.n0 + (int)rank * kBNh);
+            }
+            filled |= 1u << stage;
+            fill_par = (fill_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (gat) {
+            // token row j of the stage's token slot: 128 bytes at j * 128, its
+            // 16-byte chunk c stored at chunk c ^ (j & 7) (the slots are
+            // 1024-byte aligned); columns past K are zero-filled
+            const uint32_t dst0 = d.wide ? sT + stage * kTBytes : d.swap ? sB + stage * kBBytes : sA + stage * kABytes;
+            const bool in_k = kb * kBK + ch * 8 < P0.K;
+            const uint4* xs = reinterpret_cast<const uint4*>(P0.gx);
+  #pragma unroll
+            for (int i = 0; i < kGatherPer; ++i) {
+              if (i < nper && rv[i] != ~0u) {
+                const int j = rg + 4 * i;
+                tc::cp_async16(dst0 + j * 128 + ((ch ^ (j & 7)) << 4), xs + rv[i] + (in_k ? kb * (kBK / 8) + ch : 0),
+                               in_k ? 16u : 0u);
+              }
+            }
+            tc::cp_async_commit();
+            ++npend;
+          } else {
+            signal(stage);
+          }
           if (++stage == S) { stage = 0; phase ^= 1u; }
+          if (gat) settle(kGatherLag);
         }
       }
-      if (!ok) {
+      // every copy of this warp has landed, and its stages are signalled, before the CTA goes on
+      settle(0);
+      if (!ok && lane == 0) {
         set_error(err, kDevTimeout);
         s_abort = 1;
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
     if (rank == 0 && tc::elect_one()) {
@@ -570,7 +756,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_
         tc::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * 2 * kBNh);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!tc::mbar_wait(full(stage), phase, &s_abort, kWaitNs)) { ok = false; break; }
+          // gathered stages are completed by both producers' arrivals (cluster acquire)
+          if (!(kGather ? tc::mbar_wait<true>(full(stage), phase, &s_abort, kWaitNs)
+                        : tc::mbar_wait(full(stage), phase, &s_abort, kWaitNs))) {
+            ok = false;
+            break;
+          }
           tc::tc_fence_after();
           const uint32_t a0 = sA + stage * kABytes, b0 = sB + stage * kBBytes;
           if (dt.wide) {
@@ -680,11 +871,11 @@ bool pair_maps(CUtensorMap* mx, CUtensorMap* mxs, CUtensorMap* mw, CUtensorMap* 
 
 // One persistent launch: one resident pair per two SMs, never more pairs
 // than fit at once.
-template <int kEpiA>
+template <int kEpiA, bool kGather = false>
 cudaError_t launch_pair(const CUtensorMap (&m)[8], const int32_t* offs, int E, const PairProduct& P0,
                         const PairProduct& P1, int nphase, int swap_tail, int* next_tile, int* ready, int* err,
                         cudaStream_t st) {
-  auto kern = grouped_gemm_pair_kernel<kEpiA>;
+  auto kern = grouped_gemm_pair_kernel<kEpiA, kGather>;
   cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (r != cudaSuccess) return r;
   int pairs = sm_count() / 2;
@@ -713,7 +904,7 @@ cudaError_t launch_pair(const CUtensorMap (&m)[8], const int32_t* offs, int E, c
 cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                                const void* W1, const float* b1, const void* W2, const float* b2,
                                void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
-                               const CombineInto* comb) {
+                               const CombineInto* comb, const GatherRows* gather) {
   if (!sched) return cudaErrorInvalidValue;
   if (s.dtype != MOE_BF16 || max_rows <= 0 || max_rows >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
   if ((int64_t)s.E * s.F >= ((int64_t)1 << 31) || (int64_t)s.E * s.H >= ((int64_t)1 << 31))
@@ -725,21 +916,31 @@ cudaError_t launch_ffn_tc_pair(const Shape& s, int64_t max_rows, const void* x_p
   if (!pair_maps(&m1[0], &m1[1], &m1[2], &m1[3], x_perm, max_rows, W1, (int64_t)s.E * s.F * (swi ? 2 : 1), s.H) ||
       !pair_maps(&m2[0], &m2[1], &m2[2], &m2[3], h_perm, max_rows, W2, (int64_t)s.E * s.H, s.F))
     return cudaErrorNotSupported;
-  const PairProduct P1{s.F, s.H, b1, (bf16*)h_perm, nullptr, nullptr, nullptr, s.K};
+  if (gather && (!gather->x || !gather->src || s.H % 8 != 0 || s.T >= ((int64_t)1 << 31) ||
+                 s.T * (s.H / 8) >= ((int64_t)1 << 32)))
+    return cudaErrorNotSupported;
+  const PairProduct P1{s.F, s.H, b1, (bf16*)h_perm, nullptr, nullptr, nullptr, s.K,
+                       gather ? (const bf16*)gather->x : nullptr, gather ? gather->src : nullptr, (int)s.T};
   const PairProduct P2{s.H, s.F, b2, (bf16*)y_perm, comb ? comb->src : nullptr, comb ? comb->w : nullptr,
                        comb ? comb->acc : nullptr, s.K};
   if (!(s.flags & MOE_FLAG_FFN_SPLIT)) {
     // both products in one launch: the second's tiles start on row blocks the first has finished
     const CUtensorMap m[8] = {m1[0], m1[1], m1[2], m1[3], m2[0], m2[1], m2[2], m2[3]};
-    cudaError_t r = swi ? launch_pair<kEpiSwiglu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st)
-                        : launch_pair<kEpiGelu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st);
+    cudaError_t r =
+        gather ? (swi ? launch_pair<kEpiSwiglu, true>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st)
+                      : launch_pair<kEpiGelu, true>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st))
+               : (swi ? launch_pair<kEpiSwiglu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st)
+                      : launch_pair<kEpiGelu>(m, offs, s.E, P1, P2, 2, swap_tail, sched, sched + 2, err, st));
     if (r != cudaSuccess) return r;
     prof_mark(kMarkFirst, st);
     return cudaSuccess;
   }
   const CUtensorMap ma[8] = {m1[0], m1[1], m1[2], m1[3], m1[0], m1[1], m1[2], m1[3]};
-  cudaError_t r = swi ? launch_pair<kEpiSwiglu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st)
-                      : launch_pair<kEpiGelu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st);
+  cudaError_t r =
+      gather ? (swi ? launch_pair<kEpiSwiglu, true>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st)
+                    : launch_pair<kEpiGelu, true>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st))
+             : (swi ? launch_pair<kEpiSwiglu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st)
+                    : launch_pair<kEpiGelu>(ma, offs, s.E, P1, P1, 1, swap_tail, sched, nullptr, err, st));
   if (r != cudaSuccess) return r;
   prof_mark(kMarkFirst, st);
   const CUtensorMap mb[8] = {m2[0], m2[1], m2[2], m2[3], m2[0], m2[1], m2[2], m2[3]};

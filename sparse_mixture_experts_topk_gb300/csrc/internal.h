@@ -138,11 +138,17 @@ struct CombineInto {
   float* acc;
 };
 bool combine_fusable(const Shape& s, int64_t max_rows);
+// The first product's token rows read from x by the slot list (kept row r:
+// x row src[r] / K) instead of from x_perm (SM-pair kernels only).
+struct GatherRows {
+  const void* x;
+  const int32_t* src;
+};
 // sched: sched_words(max_rows, E) zeroed ints (the SM-pair kernel's counters)
 cudaError_t launch_ffn(const Shape& s, int64_t max_rows, const void* x_perm, const int32_t* offs,
                        const void* W1, const float* b1, const void* W2, const float* b2,
                        void* h_perm, void* y_perm, int* err, int32_t* sched, cudaStream_t st,
-                       const CombineInto* comb = nullptr);
+                       const CombineInto* comb = nullptr, const GatherRows* gather = nullptr);
 
 // ---------------------------------------------------------------- one-launch decode layer
 // bf16 batches of at most 16 tokens whose rows, score table and weight ring
