@@ -108,6 +108,30 @@ def test_layer_launch_count(lib):
         moe.moe_ffn_kernel(moe.make_desc(8, 3584, 32, 9, 2560))
 
 
+def test_gather_gemm_launch_count(lib):
+    """MOE_FLAG_GATHER_GEMM takes the gather kernel out of the layer call on
+    the SM-pair kernels (one launch fewer, in each half of a host-I/O call
+    too); it does not apply to the one-block dispatch (which has no separate
+    gather), to drop_tokens=False, to the single-SM and CUDA-core kernels or
+    to the decode layer."""
+    G = moe.MOE_FLAG_GATHER_GEMM
+
+    def n(*a, flags=0, **kw):
+        return moe.moe_layer_launches(moe.make_desc(*a, flags=flags, **kw))
+    assert n(8192, 3584, 32, 2, 2560, flags=G) == n(8192, 3584, 32, 2, 2560) - 1
+    assert n(8192, 3584, 32, 2, 2560, flags=G | moe.MOE_FLAG_FFN_SPLIT) == \
+        n(8192, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_FFN_SPLIT) - 1
+    assert n(8192, 3584, 32, 2, 2560, flags=G | moe.MOE_FLAG_HOST_IO) == \
+        n(8192, 3584, 32, 2, 2560, flags=moe.MOE_FLAG_HOST_IO) - 2
+    assert n(8192, 3584, 32, 2, 2560, capacity=512, flags=G) == n(8192, 3584, 32, 2, 2560, capacity=512) - 1
+    for kw in (dict(flags=moe.MOE_FLAG_GEMM_SINGLE), dict(capacity=512, flags=moe.MOE_FLAG_REROUTE),
+               dict(dtype=moe.MOE_F32)):
+        f = kw.pop("flags", 0)
+        assert n(4096, 256, 8, 2, 512, flags=f | G, **kw) == n(4096, 256, 8, 2, 512, flags=f, **kw), kw
+    assert n(300, 200, 8, 2, 264, flags=G | moe.MOE_FLAG_GEMM_PAIR) == n(300, 200, 8, 2, 264, flags=moe.MOE_FLAG_GEMM_PAIR)
+    assert n(8, 3584, 32, 2, 2560, flags=G) == 2
+
+
 @pytest.mark.parametrize("bad", [
     dict(K=0), dict(K=9), dict(E=1, K=2), dict(E=257), dict(H=12), dict(F=4), dict(T=-1),
     dict(dtype=7), dict(T=1 << 30, K=4), dict(temperature=float("nan")), dict(temperature=float("inf")),
