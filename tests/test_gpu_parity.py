@@ -420,3 +420,23 @@ def test_streamed_products_in_one_launch_equal_two_launches(name):
     L = run_layer(dev, flags=0)
     assert L["device_error"] == 0
     np.testing.assert_array_equal(to_np(L["out"]), to_np(one["out"]))
+
+
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("name", ["ragged_bf16", "cap_zipf_k4", "e64_k8", "hot2", "hot2_cap", "swiglu_ragged",
+                                  "h_ragged", "e256_k3"])
+def test_layer_equals_separate_steps_on_pair_gemm(name, split):
+    """The layer call (router, dispatch, both SM-pair expert products, the
+    combine chained by programmatic launch) and the separate entry points
+    (moe_router_topk, moe_dispatch, moe_expert_ffn, moe_combine) compute the
+    same sums in the same order: the outputs are equal bit for bit, with one
+    launch for both products or one per product, empty experts, capacity
+    drops and up to 8 slots a token."""
+    w = SMALL[name]
+    dev = Dev(W.generate(w))
+    flags = moe.MOE_FLAG_GEMM_PAIR | moe.MOE_FLAG_NO_DECODE | (moe.MOE_FLAG_FFN_SPLIT if split else 0)
+    lay = run_layer(dev, flags=flags)
+    stg = run_stages(dev, flags=flags)
+    assert lay["device_error"] == 0 and stg["device_error"] == 0
+    np.testing.assert_array_equal(to_np(lay["out"]), to_np(stg["out"]))
+    np.testing.assert_array_equal(to_np(lay["count"]), to_np(stg["count"]))
