@@ -64,7 +64,18 @@ class _PerExpert:
 @pytest.mark.parametrize("name", ["decode1", "decode8", "decode16r", "prefill", "zipf_cap", "zipf_reroute",
                                   "wide", "prefill_swiglu"])
 def test_full_size(name):
-    w = W.WORKLOADS[name]
+    _check_full(W.WORKLOADS[name], name)
+
+
+def test_full_size_most_experts():
+    """The most experts and slots a token the ABI allows (E = 256, k = 8) on
+    8192 tokens: 65536 kept rows, about 256 per expert, so the expert GEMMs'
+    tile table holds every kind of block (full, tails in row orientation,
+    swapped and wide) for 256 experts, and the combine sums 8 slots."""
+    _check_full(W.small("most_experts", T=8192, H=1024, E=256, K=8, F=512), "most_experts")
+
+
+def _check_full(w, name):
     inp = W.generate(w)
     dev = Dev(inp)
     r = run_stages(dev)
