@@ -338,8 +338,10 @@ dispatch_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ 
 // tiles: every block reads the whole [nblk, E] table of tile counts (eight
 // loads in flight per thread), takes its rank base (the counts of the tiles
 // before it) and the experts' totals and offsets, and places its tile's
-// slots.  Block 0 also writes the counts, offsets, dropped slots,
-// probability sums (added up exactly as the scan kernel does) and the loss.
+// slots.  One more block, the last, places nothing: it writes the counts,
+// offsets, dropped slots, probability sums (added up exactly as the scan
+// kernel does) and the loss, beside the others instead of after one of
+// them (measured: block 0 doing it as well took twice as long as the rest).
 __global__ void __launch_bounds__(kDispThreads)
 dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, int C, int bslots,
                              const int32_t* __restrict__ blk_hist, int64_t nblk, int32_t* __restrict__ count,
@@ -355,7 +357,7 @@ dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, 
   __shared__ float s_pg[256];
   pdl_enter();
   const int e = threadIdx.x;
-  const bool leader = blockIdx.x == 0;
+  const bool leader = blockIdx.x == nblk;   // the statistics block
   const int64_t n = nblk * E;
   for (int64_t i0 = threadIdx.x; i0 < n; i0 += 256 * 8) {
     int h[8];
@@ -396,6 +398,7 @@ dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int64_t S, int E, 
                 leader ? psum_part : nullptr, prows, leader ? psum : nullptr, leader ? aux : nullptr, Tn, K,
                 leader ? count_copy : nullptr, leader ? dropped_copy : nullptr, leader ? sched : nullptr, s_offs,
                 p_pre);
+  if (leader) return;   // it owns no slots
   __syncthreads();
   const int64_t s0 = (int64_t)blockIdx.x * bslots;
   const int64_t s1 = min(S, s0 + bslots);
@@ -551,7 +554,7 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
                              (int)table);
     const int64_t prows = o.psum_part ? router_partial_rows(s) : (int64_t)0;
     if (e == cudaSuccess)
-      e = launch_kernel(dispatch_scan_scatter_kernel, dim3((unsigned)nblk), dim3(kDispThreads), table, st, 1, ids,
+      e = launch_kernel(dispatch_scan_scatter_kernel, dim3((unsigned)nblk + 1), dim3(kDispThreads), table, st, 1, ids,
                         S, s.E, s.C, bslots, (const int32_t*)o.blk_hist, nblk, o.count, o.offs, o.dropped,
                         o.psum_part, prows, o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy, o.sched,
                         o.pos, o.src);
