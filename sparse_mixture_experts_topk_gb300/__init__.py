@@ -24,7 +24,8 @@ __all__ = [
     "moe_router_topk", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_get_device_error", "moe_profile_events", "moe_layer_launches", "moe_ffn_kernel", "moe_layer_decode_fused",
     "MOE_FFN_STREAM", "MOE_FFN_SIMT", "MOE_FFN_TC_SINGLE", "MOE_FFN_TC_PAIRS", "MOE_FFN_TC_FUSED",
-    "MOE_FFN_STREAM_SPLIT", "workspace",
+    "MOE_FFN_STREAM_SPLIT", "workspace", "MOE_OK", "MOE_ERR_INVALID", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE",
+    "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT", "MOE_ERR_DEVICE",
 ]
 
 MOE_F32, MOE_BF16 = 0, 1
@@ -45,7 +46,10 @@ MOE_FLAG_GATHER_GEMM = 1 << 13
 # moe_ffn_kernel results
 MOE_FFN_STREAM, MOE_FFN_SIMT, MOE_FFN_TC_SINGLE, MOE_FFN_TC_PAIRS, MOE_FFN_TC_FUSED, MOE_FFN_STREAM_SPLIT = 0, 1, 2, 3, 4, 5
 
+# status codes (MoeError.code)
 MOE_OK = 0
+MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = \
+    -1, -2, -3, -4, -5, -6
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "_lib", "libmoe.so")

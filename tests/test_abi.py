@@ -37,6 +37,20 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(moe, n), n
 
 
+def test_header_constants_match_the_binding():
+    """Every flag, status and expert-FFN kind that include/moe.h defines has
+    the same name and value in the Python binding (parsed from the header's
+    text, so a constant added on one side only fails here)."""
+    hdr = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defs = {n: int(a) << int(b or 0) for n, a, b in
+            re.findall(r"#define (MOE_(?:FLAG|FFN)_\w+)\s+\(?(\d+)u?(?:\s*<<\s*(\d+))?", hdr)}
+    enums = {n: int(v) for n, v in re.findall(r"\b(MOE_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", hdr)}
+    assert len(defs) >= 20 and len(enums) == 7
+    for n, v in {**defs, **enums}.items():
+        assert getattr(moe, n) == v, n
+        assert n in moe.__all__, n
+
+
 def test_capacity_and_rows(lib):
     assert moe.moe_capacity_default(8192, 32, 2) == 512
     assert moe.moe_capacity_default(16384, 32, 4) == 2048
