@@ -554,8 +554,8 @@ cudaError_t launch_dispatch(const Shape& s, const int32_t* ids, const void* x, v
                              (int)table);
     const int64_t prows = o.psum_part ? router_partial_rows(s) : (int64_t)0;
     if (e == cudaSuccess)
-      e = launch_kernel(dispatch_scan_scatter_kernel, dim3((unsigned)nblk + 1), dim3(kDispThreads), table, st, 1, ids,
-                        S, s.E, s.C, bslots, (const int32_t*)o.blk_hist, nblk, o.count, o.offs, o.dropped,
+      e = launch_kernel(dispatch_scan_scatter_kernel, dim3((unsigned)nblk + 1), dim3(kDispThreads), table, st, 1,
+                        ids, S, s.E, s.C, bslots, (const int32_t*)o.blk_hist, nblk, o.count, o.offs, o.dropped,
                         o.psum_part, prows, o.psum, o.aux, s.T, s.K, o.count_copy, o.dropped_copy, o.sched,
                         o.pos, o.src);
     if (e == cudaSuccess && x && x_perm && S > 0) e = launch_gather(s, x, o.pos, x_perm, st);
